@@ -1,0 +1,319 @@
+// NVFP4 block-scaled quantize and GEMM + top-k: the CPU oracle.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path links,
+// loads or calls this file; only the tests, the smoke check and the bench's
+// CPU-baseline leg do.  It shares no code, header, table or constant
+// generator with the CUDA path.
+//
+// It is a plain, slow, single-threaded restatement of the definitions on the
+// pages of the "nvfp4-megamoe-kernel" repository (DeepSeek-V4-Pro NVFP4
+// inference), step by step:
+//
+//   E2M1 code table      page "commit 0d1cd1e / dsv4/kernels/indexer",
+//                        commit message, "E2M1 encoding (bias=1)" table
+//   activation gs        page "commit 107d62d / single_shot_inference.py",
+//                        "Fix: compute gsa at runtime": gsa = max|x| / (6*448)
+//   amax clamp           page "compare ... v-official-encoding-path",
+//                        PERFORMANCE_AUDIT.md section P0 (clamp(min=1e-8))
+//   16-element blocks    same page, README.md "NVFP4 throughout"
+//                        (E4M3 scales, 16-element micro-blocks)
+//   E4M3 / FP4 maxima    same page, CORRECTNESS_BACKLOG.md section 7
+//                        (E4M3 max 448, FP4 max 6)
+//   dequant formula      page "commit db07d17 / dsv4", weight_scale_2 fix
+//                        (w = lut[w] * weight_scale * weight_scale_2)
+//   GEMM scaling         page "commit 107d62d / single_shot_inference.py",
+//                        global-scale commit ((A*SFA)@(B*SFB), then gsa*gsb)
+//   router epilogue      same commit (sqrt(softplus(logit*gsa*gsb))) and
+//                        CORRECTNESS_BACKLOG.md section 5 (+ e_bias, top-k)
+//   deinterleave         page "commit 0d1cd1e", fused_deinterleave commit;
+//                        docs/PERFORMANCE_AUDIT.md P1 (granularity 8)
+//
+// Readings where the pages are silent (each one is listed in the design
+// notes): block scale s = (bamax / 6) / gs in FP32; E4M3 round-to-nearest-
+// even with saturation to 448; element value v = x / (dec(s) * gs) in FP32;
+// E2M1 round-to-nearest-even with saturation to 6, sign bit kept (a
+// negative value that rounds to zero encodes as 0x8); a block whose scale
+// byte is zero encodes every element as a signed zero; the even element of a
+// pair goes to the low nibble; softplus(z) = z for z > 20.
+//
+// Floating point: every FP32 step is one IEEE single operation (compile with
+// -ffp-contract=off and without fast-math); the GEMM accumulates in double.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+
+namespace {
+
+// E2M1 magnitudes for codes 0..7 (bias 1): 0b000=0, 0b001=0.5, 0b010=1,
+// 0b011=1.5, 0b100=2, 0b101=3, 0b110=4, 0b111=6.
+const double kE2M1Magnitude[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+float bf16_value(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof(f));
+  return f;
+}
+
+// Value of a non-negative E4M3 (FN variant) code: 4 exponent bits with bias
+// 7, 3 mantissa bits; exponent field 0 is subnormal (m * 2^-9).
+double e4m3_value(uint8_t code) {
+  const int e = (code >> 3) & 0xF;
+  const int m = code & 0x7;
+  if (e == 0xF && m == 0x7) return std::numeric_limits<double>::quiet_NaN();
+  double mag = (e == 0) ? std::ldexp(static_cast<double>(m), -9)
+                        : std::ldexp(1.0 + m / 8.0, e - 7);
+  return (code & 0x80) ? -mag : mag;
+}
+
+// The 127 non-negative finite E4M3 values, code order (0 .. 448).
+const std::vector<double>& e4m3_grid() {
+  static const std::vector<double> grid = [] {
+    std::vector<double> g(127);
+    for (int c = 0; c < 127; ++c) g[c] = e4m3_value(static_cast<uint8_t>(c));
+    return g;
+  }();
+  return grid;
+}
+
+}  // namespace
+
+extern "C" {
+
+float orc_bf16_to_f32(uint16_t bits) { return bf16_value(bits); }
+
+double orc_e2m1_decode(uint8_t code) {
+  const double mag = kE2M1Magnitude[code & 7];
+  return (code & 8) ? -mag : mag;
+}
+
+// Nearest E2M1 magnitude to |v| by exhaustive search over the 8 magnitudes;
+// on an exact tie the even code wins (round to nearest, ties to even).  The
+// largest magnitude, 6, is the nearest for everything above 5, so values
+// beyond 6 saturate.  The sign bit is copied from v.
+uint8_t orc_e2m1_encode(float v) {
+  const double a = std::fabs(static_cast<double>(v));
+  const uint8_t sign = std::signbit(v) ? 8 : 0;
+  if (a >= 6.0) return static_cast<uint8_t>(sign | 7);  // saturate (also keeps huge |v| exact)
+  int best = 0;
+  double best_err = a;  // distance to magnitude 0
+  for (int c = 1; c < 8; ++c) {
+    const double err = std::fabs(a - kE2M1Magnitude[c]);
+    if (err < best_err || (err == best_err && (c % 2 == 0) && (best % 2 != 0))) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return static_cast<uint8_t>(sign | best);
+}
+
+float orc_e4m3_decode(uint8_t code) { return static_cast<float>(e4m3_value(code)); }
+
+// Nearest non-negative finite E4M3 value (codes 0..126, max 448) to v >= 0 by
+// exhaustive search; ties go to the even code (even mantissa).  Values above
+// 448 saturate to 448 (code 126).
+uint8_t orc_e4m3_encode(float v) {
+  const double a = static_cast<double>(v);
+  if (a >= 448.0) return 0x7E;  // saturate (also keeps huge values exact)
+  const std::vector<double>& grid = e4m3_grid();
+  int best = 0;
+  double best_err = std::fabs(a);
+  for (int c = 1; c <= 126; ++c) {
+    const double err = std::fabs(a - grid[c]);
+    if (err < best_err || (err == best_err && (c % 2 == 0) && (best % 2 != 0))) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return static_cast<uint8_t>(best);
+}
+
+// amax = max(max_i |x_i|, 1e-8); gs = amax / (6 * 448) in FP32.
+float orc_global_scale(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld) {
+  float amax = 0.0f;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const float a = std::fabs(bf16_value(x[r * ld + c]));
+      if (a > amax) amax = a;
+    }
+  if (amax < 1e-8f) amax = 1e-8f;
+  return amax / 2688.0f;
+}
+
+// Quantize rows [row_begin, row_end) of x (row stride ld elements) with a
+// given global scale gs.  q has cols/2 bytes per row (element 2j in the low
+// nibble of byte j, element 2j+1 in the high nibble); sf has cols/16 E4M3
+// bytes per row.  Outputs are indexed from row_begin (row r goes to row
+// r - row_begin of q and sf).
+void orc_quantize_rows(const uint16_t* x, int64_t cols, int64_t ld, float gs,
+                       int64_t row_begin, int64_t row_end, uint8_t* q, uint8_t* sf) {
+  const int64_t nblocks = cols / 16;
+  for (int64_t r = row_begin; r < row_end; ++r) {
+    const uint16_t* xr = x + r * ld;
+    uint8_t* qr = q + (r - row_begin) * (cols / 2);
+    uint8_t* sr = sf + (r - row_begin) * nblocks;
+    for (int64_t b = 0; b < nblocks; ++b) {
+      float vals[16];
+      float bamax = 0.0f;
+      for (int j = 0; j < 16; ++j) {
+        vals[j] = bf16_value(xr[b * 16 + j]);
+        const float a = std::fabs(vals[j]);
+        if (a > bamax) bamax = a;
+      }
+      const float s = (bamax / 6.0f) / gs;          // block scale before encoding
+      const uint8_t sbyte = orc_e4m3_encode(s);
+      sr[b] = sbyte;
+      const float den = orc_e4m3_decode(sbyte) * gs;  // effective block step
+      uint8_t codes[16];
+      for (int j = 0; j < 16; ++j) {
+        const float v = (den != 0.0f) ? vals[j] / den : std::copysign(0.0f, vals[j]);
+        codes[j] = orc_e2m1_encode(v);
+      }
+      for (int j = 0; j < 8; ++j)
+        qr[b * 8 + j] = static_cast<uint8_t>(codes[2 * j] | (codes[2 * j + 1] << 4));
+    }
+  }
+}
+
+// Whole-tensor quantize: gs from the tensor's own amax, then every row.
+void orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                  uint8_t* q, uint8_t* sf, float* gs_out) {
+  const float gs = orc_global_scale(x, rows, cols, ld);
+  *gs_out = gs;
+  orc_quantize_rows(x, cols, ld, gs, 0, rows, q, sf);
+}
+
+// Deinterleave one [rows, 2I] matrix whose gate/up columns alternate in
+// groups of g: output column j < I is gate column j, taken from input column
+// 2g*floor(j/g) + (j mod g); output column I + j is up column j, taken from
+// input column 2g*floor(j/g) + g + (j mod g).
+void orc_deinterleave(const uint16_t* x, int64_t rows, int64_t inter, int64_t g, uint16_t* out) {
+  const int64_t w = 2 * inter;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t j = 0; j < inter; ++j) {
+      const int64_t base = 2 * g * (j / g) + (j % g);
+      out[r * w + j] = x[r * w + base];
+      out[r * w + inter + j] = x[r * w + base + g];
+    }
+}
+
+// Deinterleave, then quantize the [rows, 2I] result as a whole.
+void orc_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, int64_t g,
+                               uint8_t* q, uint8_t* sf, float* gs_out) {
+  std::vector<uint16_t> tmp(static_cast<size_t>(rows * 2 * inter));
+  orc_deinterleave(x, rows, inter, g, tmp.data());
+  orc_quantize(tmp.data(), rows, 2 * inter, 2 * inter, q, sf, gs_out);
+}
+
+// Dequantize rows of an NVFP4 tensor: out = lut[q] * e4m3(sf) * gs, in double.
+void orc_dequantize(const uint8_t* q, const uint8_t* sf, float gs, int64_t rows, int64_t cols,
+                    double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const uint8_t byte = q[r * (cols / 2) + c / 2];
+      const uint8_t code = (c % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      out[r * cols + c] = orc_e2m1_decode(code) * e4m3_value(sf[r * (cols / 16) + c / 16]) *
+                          static_cast<double>(gs);
+    }
+}
+
+// Block-scaled GEMM logits for rows [row_begin, row_end):
+//   acc[m,n] = sum_k lut(qa[m,k]) * sfa[m,k/16] * lut(qb[n,k]) * sfb[n,k/16]   (double)
+//   logit[m,n] = float(acc * gsa * gsb)
+// A is M x K (K/2 bytes per row), B is N x K; out is (row_end-row_begin) x N.
+void orc_gemm_logits(const uint8_t* qa, const uint8_t* sfa, float gsa,
+                     const uint8_t* qb, const uint8_t* sfb, float gsb,
+                     int64_t N, int64_t K, int64_t row_begin, int64_t row_end, float* out) {
+  // lut(q) * e4m3(sf) for every element of B, then for each row of A.
+  std::vector<double> b(static_cast<size_t>(N * K));
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t byte = qb[n * (K / 2) + k / 2];
+      const uint8_t code = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      b[n * K + k] = orc_e2m1_decode(code) * e4m3_value(sfb[n * (K / 16) + k / 16]);
+    }
+  std::vector<double> a(static_cast<size_t>(K));
+  for (int64_t m = row_begin; m < row_end; ++m) {
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t byte = qa[m * (K / 2) + k / 2];
+      const uint8_t code = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      a[k] = orc_e2m1_decode(code) * e4m3_value(sfa[m * (K / 16) + k / 16]);
+    }
+    for (int64_t n = 0; n < N; ++n) {
+      const double* bn = b.data() + n * K;
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += a[k] * bn[k];
+      out[(m - row_begin) * N + n] =
+          static_cast<float>(acc * static_cast<double>(gsa) * static_cast<double>(gsb));
+    }
+  }
+}
+
+// Epilogue on a rows x N logit matrix.
+//   epilogue 0 (identity, indexer-shaped): score = weight = logit
+//   epilogue 1 (router-shaped): weight = sqrt(softplus(logit)),
+//                               score = weight + bias[n]
+// softplus(z) = log(1 + e^z), taken as z itself above 20.  Double, then float.
+void orc_epilogue(const float* logits, int64_t rows, int64_t N, int epilogue, const float* bias,
+                  float* score, float* weight) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t n = 0; n < N; ++n) {
+      const double z = logits[r * N + n];
+      if (epilogue == 0) {
+        score[r * N + n] = static_cast<float>(z);
+        if (weight) weight[r * N + n] = static_cast<float>(z);
+      } else {
+        const double sp = (z > 20.0) ? z : std::log1p(std::exp(z));
+        const double w = std::sqrt(sp);
+        score[r * N + n] = static_cast<float>(w + static_cast<double>(bias[n]));
+        if (weight) weight[r * N + n] = static_cast<float>(w);
+      }
+    }
+}
+
+// Per-row top-k of a rows x N score matrix: the k largest scores in
+// descending order, equal scores ordered by lower column index.  Slots past
+// N get index -1, score -inf, weight 0.
+void orc_topk(const float* score, const float* weight, int64_t rows, int64_t N, int k,
+              int32_t* idx_out, float* score_out, float* weight_out) {
+  std::vector<int64_t> order(static_cast<size_t>(N));
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* s = score + r * N;
+    for (int64_t n = 0; n < N; ++n) order[n] = n;
+    const int64_t take = std::min<int64_t>(k, N);
+    std::partial_sort(order.begin(), order.begin() + take, order.end(),
+                      [s](int64_t i, int64_t j) { return s[i] > s[j] || (s[i] == s[j] && i < j); });
+    for (int64_t t = 0; t < k; ++t) {
+      if (t < take) {
+        idx_out[r * k + t] = static_cast<int32_t>(order[t]);
+        score_out[r * k + t] = s[order[t]];
+        if (weight_out) weight_out[r * k + t] = weight ? weight[r * N + order[t]] : 0.0f;
+      } else {
+        idx_out[r * k + t] = -1;
+        score_out[r * k + t] = -std::numeric_limits<float>::infinity();
+        if (weight_out) weight_out[r * k + t] = 0.0f;
+      }
+    }
+  }
+}
+
+// The whole GEMM + epilogue + top-k for rows [row_begin, row_end).
+void orc_gemm_topk_rows(const uint8_t* qa, const uint8_t* sfa, float gsa,
+                        const uint8_t* qb, const uint8_t* sfb, float gsb,
+                        int64_t N, int64_t K, int epilogue, const float* bias, int k,
+                        int64_t row_begin, int64_t row_end,
+                        int32_t* idx_out, float* score_out, float* weight_out) {
+  const int64_t rows = row_end - row_begin;
+  std::vector<float> logits(static_cast<size_t>(rows * N));
+  std::vector<float> score(static_cast<size_t>(rows * N));
+  std::vector<float> weight(static_cast<size_t>(rows * N));
+  orc_gemm_logits(qa, sfa, gsa, qb, sfb, gsb, N, K, row_begin, row_end, logits.data());
+  orc_epilogue(logits.data(), rows, N, epilogue, bias, score.data(), weight.data());
+  orc_topk(score.data(), weight.data(), rows, N, k, idx_out, score_out, weight_out);
+}
+
+}  // extern "C"

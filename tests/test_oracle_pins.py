@@ -1,0 +1,350 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against something fixed independently: the
+pages' E2M1 table and scale constants (tests/golden), PyTorch's own
+float8_e4m3fn conversion (a library routine), numpy matmul / logaddexp,
+closed forms, inputs built exactly on the NVFP4 grid, and brute force on
+tiny inputs.  They are chosen so that a dropped term, a wrong sign or index,
+a swapped nibble or a transposed operand in the oracle fails at least one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import read_golden
+from workloads import bf16_bits, bf16_to_f32
+
+E2M1_TABLE = {int(c, 2): float(v) for c, v in read_golden("e2m1_table.txt")}
+CONST = {k: float(v) for k, v in read_golden("scale_constants.txt")}
+E2M1_VALUES = [E2M1_TABLE[c] for c in range(8)]
+
+
+# ---------------------------------------------------------------- E2M1 codec
+
+def test_e2m1_table_from_page():
+    assert len(E2M1_TABLE) == 8
+    for code, value in E2M1_TABLE.items():
+        assert oracle.e2m1_decode(code) == value
+        assert oracle.e2m1_decode(code | 8) == -value
+    # the two codes the pages single out
+    assert oracle.e2m1_decode(0b101) == 3.0 and oracle.e2m1_decode(0b110) == 4.0
+    # the bug the pages fixed: magnitude bits are not an integer
+    assert any(oracle.e2m1_decode(c) != float(c) for c in range(8))
+
+
+def test_e2m1_encode_inverts_decode():
+    for code in range(8):
+        assert oracle.e2m1_encode(E2M1_TABLE[code]) == code
+        assert oracle.e2m1_encode(-E2M1_TABLE[code]) == code | 8
+
+
+def test_e2m1_encode_midpoints_round_to_even():
+    # Exact midpoints between neighbouring magnitudes go to the even code.
+    expected = {0.25: 0b000, 0.75: 0b010, 1.25: 0b010, 1.75: 0b100,
+                2.5: 0b100, 3.5: 0b110, 5.0: 0b110}
+    for v, code in expected.items():
+        assert oracle.e2m1_encode(v) == code, v
+        assert oracle.e2m1_encode(-v) == code | 8, v
+        lo = np.nextafter(np.float32(v), np.float32(0))
+        hi = np.nextafter(np.float32(v), np.float32(10))
+        # just below / above the midpoint: the nearer neighbour
+        below = max(c for c in range(8) if E2M1_VALUES[c] < v)
+        above = min(c for c in range(8) if E2M1_VALUES[c] > v)
+        assert oracle.e2m1_encode(float(lo)) == below
+        assert oracle.e2m1_encode(float(hi)) == above
+
+
+def test_e2m1_encode_nearest_and_saturating():
+    grid = np.array(E2M1_VALUES)
+    for v in np.linspace(0.0, 9.0, 4001, dtype=np.float32):
+        code = oracle.e2m1_encode(float(v))
+        d = abs(float(v) - E2M1_VALUES[code])
+        assert d <= np.min(np.abs(grid - float(v))) + 1e-12
+        if v > 6.0:
+            assert code == 7
+    for v in (6.0, 7.5, 1e6, 1e30, 3.4e38):
+        assert oracle.e2m1_encode(v) == 7 and oracle.e2m1_encode(-v) == 15
+    # sign of values that round to zero is kept
+    assert oracle.e2m1_encode(-0.1) == 0b1000
+    assert oracle.e2m1_encode(-0.0) == 0b1000
+    assert oracle.e2m1_encode(0.1) == 0
+
+
+# ---------------------------------------------------------------- E4M3 codec
+
+def test_e4m3_decode_matches_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float().numpy()
+    for c in range(256):
+        v = oracle.e4m3_decode(c)
+        if c in (0x7F, 0xFF):
+            assert math.isnan(v)
+        else:
+            assert v == ref[c], c
+    assert oracle.e4m3_decode(0x7E) == CONST["e4m3_max"]
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_rne():
+    vals = [oracle.e4m3_decode(c) for c in range(127)]
+    mids = [(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])]
+    sweep = np.concatenate([
+        np.float32(vals), np.float32(mids),
+        np.nextafter(np.float32(mids), np.float32(0)), np.nextafter(np.float32(mids), np.float32(1e9)),
+        np.random.default_rng(11).uniform(0, 464, 20000).astype(np.float32),
+        np.float32([0.0, 1e-30, 2.0 ** -10, 448.0, 460.0, 464.0]),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(sweep).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in sweep], np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e4m3_encode_inverts_decode_and_saturates():
+    for c in range(127):
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
+    for v in (448.0, 464.0, 465.0, 1000.0, 1e30):
+        assert oracle.e4m3_encode(v) == 0x7E
+
+
+# ---------------------------------------------------------------- global scale
+
+def _bf16(a):
+    return bf16_bits(np.asarray(a, np.float32))
+
+
+def test_global_scale_closed_form():
+    assert CONST["gs_divisor"] == CONST["fp4_max"] * CONST["e4m3_max"]
+    x = np.zeros((3, 32), np.float32)
+    x[1, 7] = -2688.0
+    assert oracle.global_scale(_bf16(x)) == np.float32(1.0)
+    x[1, 7] = 1.0
+    assert oracle.global_scale(_bf16(x)) == np.float32(1.0) / np.float32(2688.0)
+    # all zero: amax clamps to 1e-8
+    z = np.zeros((2, 16), np.float32)
+    assert oracle.global_scale(_bf16(z)) == np.float32(1e-8) / np.float32(2688.0)
+
+
+# ---------------------------------------------------------------- quantize
+
+def _grid_tensor(rng, rows, cols):
+    """x on the NVFP4 grid with gs = 1: block b has scale 2^e_b, entries code * 2^e_b."""
+    x = np.zeros((rows, cols), np.float32)
+    exps = rng.integers(-6, 9, size=(rows, cols // 16))  # 2^-6 .. 2^8: normal E4M3 scales
+    vals = rng.choice(np.array(E2M1_VALUES + [-v for v in E2M1_VALUES[1:]], np.float32),
+                      size=(rows, cols))
+    for r in range(rows):
+        for b in range(cols // 16):
+            blk = vals[r, b * 16:(b + 1) * 16].copy()
+            blk[rng.integers(0, 16)] = 6.0 * rng.choice([-1, 1])  # block max exactly 6 * 2^e
+            x[r, b * 16:(b + 1) * 16] = blk * np.float32(2.0 ** exps[r, b])
+    # one block at the top scale 448 holds the tensor max 2688 = 6 * 448 -> gs = 1
+    x[0, :16] = np.float32(448.0) * vals[0, :16]
+    x[0, 3] = 2688.0
+    return x
+
+
+def test_quantize_exact_on_grid_and_nibble_order():
+    rng = np.random.default_rng(1)
+    x = _grid_tensor(rng, 5, 64)
+    xb = _bf16(x)
+    assert np.array_equal(bf16_to_f32(xb), x)  # the grid is exact in bf16
+    q, sf, gs = oracle.quantize(xb)
+    assert gs == np.float32(1.0)
+    # scale bytes: 448 for block 0 of row 0, 2^e elsewhere (from torch's E4M3 encoder)
+    assert sf[0, 0] == 0x7E
+    # codes: the even element sits in the low nibble; values from the page's table
+    sign = lambda v: 8 if v < 0 else 0
+    val_to_code = {v: c for c, v in E2M1_TABLE.items()}
+    for r in range(5):
+        for b in range(4):
+            s = float(torch.tensor([float(sf[r, b])]).to(torch.uint8).view(torch.float8_e4m3fn).float())
+            for j in range(16):
+                v = x[r, b * 16 + j] / s
+                code = sign(v) | val_to_code[abs(float(v))]
+                byte = q[r, (b * 16 + j) // 2]
+                got = (byte & 0xF) if j % 2 == 0 else (byte >> 4)
+                assert got == code, (r, b, j)
+    deq = oracle.dequantize(q, sf, gs)
+    np.testing.assert_array_equal(deq, x.astype(np.float64))
+
+
+def _half_gap(v):
+    a = abs(v)
+    if a <= 2.0:
+        return 0.25
+    if a <= 4.0:
+        return 0.5
+    return 1.0
+
+
+def test_quantize_roundtrip_error_bound():
+    rng = np.random.default_rng(2)
+    x32 = rng.standard_normal((16, 256)).astype(np.float32)
+    x32.reshape(-1)[rng.integers(0, x32.size, 40)] *= 100.0
+    xb = _bf16(x32)
+    x = bf16_to_f32(xb).astype(np.float64)
+    q, sf, gs = oracle.quantize(xb)
+    assert gs == np.float32(np.abs(x).max()) / np.float32(2688.0)
+    deq = oracle.dequantize(q, sf, gs)
+    e4 = torch.from_numpy(sf.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    assert sf.max() <= 0x7E  # no block scale above 448
+    for r in range(x.shape[0]):
+        for b in range(x.shape[1] // 16):
+            den = e4[r, b] * float(gs)
+            blk = x[r, b * 16:(b + 1) * 16]
+            for j in range(16):
+                v = blk[j] / den
+                bound = den * (_half_gap(v) + max(0.0, abs(v) - 6.0)) * (1 + 1e-6) + 1e-30
+                assert abs(blk[j] - deq[r, b * 16 + j]) <= bound
+            if e4[r, b] >= 2.0 ** -6:  # normal scale: the block max lands on magnitude 6
+                jmax = int(np.argmax(np.abs(blk)))
+                byte = q[r, (b * 16 + jmax) // 2]
+                code = (byte & 0xF) if jmax % 2 == 0 else (byte >> 4)
+                assert code & 7 == 7
+    # the block holding the tensor max gets scale 448 (x/gsa <= 2688 exactly reached)
+    r, c = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert sf[r, c // 16] == 0x7E
+
+
+def test_quantize_zero_and_tiny_blocks():
+    z = np.zeros((2, 32), np.float32)
+    q, sf, gs = oracle.quantize(_bf16(z))
+    assert not q.any() and not sf.any()
+    # a block far below the tensor max gets scale byte 0: all codes are signed zeros
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 1000.0
+    x[0, 16:] = -1e-4
+    q, sf, gs = oracle.quantize(_bf16(x))
+    assert sf[0, 1] == 0
+    assert (q[0, 8:] == 0x88).all()
+
+
+# ---------------------------------------------------------------- deinterleave
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
+def test_deinterleave_layout(g):
+    inter = 32
+    gate = np.arange(inter, dtype=np.uint16) + 100
+    up = np.arange(inter, dtype=np.uint16) + 1000
+    # interleave: groups of g gate columns alternate with groups of g up columns
+    row = np.stack([gate.reshape(-1, g), up.reshape(-1, g)], axis=1).reshape(-1)
+    x = np.stack([row, row + 1]).astype(np.uint16)
+    out = oracle.deinterleave(x, g)
+    np.testing.assert_array_equal(out[0], np.concatenate([gate, up]))
+    np.testing.assert_array_equal(out[1], np.concatenate([gate, up]) + 1)
+
+
+def test_deinterleave_quantize_is_quantize_of_deinterleaved():
+    rng = np.random.default_rng(3)
+    x = _bf16(rng.standard_normal((3, 128)).astype(np.float32))
+    q1, sf1, gs1 = oracle.deinterleave_quantize(x, 8)
+    q2, sf2, gs2 = oracle.quantize(oracle.deinterleave(x, 8))
+    assert gs1 == gs2 and np.array_equal(q1, q2) and np.array_equal(sf1, sf2)
+
+
+# ---------------------------------------------------------------- GEMM
+
+def test_gemm_textbook_case():
+    # Unit scales (E4M3 1.0 = 0x38) and unit global scales: logits are plain dot
+    # products of table values, unpacked here by hand (low nibble = even element).
+    rng = np.random.default_rng(4)
+    M, N, K = 3, 5, 64
+    qa = rng.integers(0, 256, (M, K // 2)).astype(np.uint8)
+    qb = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    sfa = np.full((M, K // 16), 0x38, np.uint8)
+    sfb = np.full((N, K // 16), 0x38, np.uint8)
+
+    def val(nib):
+        return (-1 if nib & 8 else 1) * E2M1_TABLE[nib & 7]
+
+    def row_vals(q):
+        out = []
+        for byte in q:
+            out += [val(byte & 0xF), val(byte >> 4)]
+        return out
+
+    got = oracle.gemm_logits(qa, sfa, 1.0, qb, sfb, 1.0)
+    for m in range(M):
+        a = row_vals(qa[m])
+        for n in range(N):
+            b = row_vals(qb[n])
+            assert got[m, n] == np.float32(sum(x * y for x, y in zip(a, b)))
+
+
+def test_gemm_matches_dequant_matmul():
+    rng = np.random.default_rng(5)
+    xa = _bf16(rng.standard_normal((7, 512)).astype(np.float32))
+    xb = _bf16((rng.standard_normal((9, 512)) * 0.02).astype(np.float32))
+    qa, sfa, gsa = oracle.quantize(xa)
+    qb, sfb, gsb = oracle.quantize(xb)
+    A = oracle.dequantize(qa, sfa, 1.0) * np.float64(gsa)
+    B = oracle.dequantize(qb, sfb, 1.0) * np.float64(gsb)
+    ref = A @ B.T
+    got = oracle.gemm_logits(qa, sfa, gsa, qb, sfb, gsb).astype(np.float64)
+    scale = np.abs(A) @ np.abs(B).T
+    assert np.all(np.abs(got - ref) <= 2 ** -23 * np.abs(ref) + 1e-12 * scale)
+    # operand order matters: the transposed product is a different matrix
+    assert got.shape == (7, 9)
+    # row range selects the same rows
+    np.testing.assert_array_equal(oracle.gemm_logits(qa, sfa, gsa, qb, sfb, gsb, 2, 5), got[2:5])
+    # dequant formula: lut[q] * sf * gs on one element by hand
+    byte = qb[4, 10]
+    code = byte >> 4  # element 21 (odd) -> high nibble
+    e4 = float(torch.tensor([int(sfb[4, 21 // 16])], dtype=torch.uint8).view(torch.float8_e4m3fn).float())
+    by_hand = (-1 if code & 8 else 1) * E2M1_TABLE[code & 7] * e4 * float(gsb)
+    assert oracle.dequantize(qb, sfb, gsb)[4, 21] == by_hand
+
+
+# ---------------------------------------------------------------- epilogue + top-k
+
+def test_epilogue_closed_forms():
+    logits = np.array([[0.0, 30.0, -30.0, 2.0, -3.5]], np.float32)
+    bias = np.array([0.1, -0.2, 0.0, 0.5, 0.25], np.float32)
+    s, w = oracle.epilogue(logits, 1, bias)
+    assert w[0, 0] == np.float32(math.sqrt(math.log(2.0)))
+    ref_w = np.sqrt(np.logaddexp(0.0, logits[0].astype(np.float64)))
+    np.testing.assert_allclose(w[0], ref_w, rtol=1e-6)
+    np.testing.assert_allclose(s[0], ref_w + bias, rtol=1e-6, atol=1e-7)
+    assert abs(w[0, 2] - math.exp(-15.0)) < 1e-9
+    s0, w0 = oracle.epilogue(logits, 0, None)
+    np.testing.assert_array_equal(s0, logits)
+    np.testing.assert_array_equal(w0, logits)
+
+
+def _brute_topk(row, k):
+    order = sorted(range(len(row)), key=lambda i: (-float(row[i]), i))[:k]
+    return order
+
+
+def test_topk_bruteforce_with_ties():
+    rng = np.random.default_rng(6)
+    for trial in range(50):
+        rows, N = 4, int(rng.integers(1, 65))
+        k = int(rng.integers(1, 12))
+        s = rng.integers(-5, 6, (rows, N)).astype(np.float32)  # many exact ties
+        idx, val, _ = oracle.topk(s, k)
+        for r in range(rows):
+            ref = _brute_topk(s[r], k)
+            take = min(k, N)
+            assert list(idx[r, :take]) == ref
+            np.testing.assert_array_equal(val[r, :take], s[r, ref])
+            assert (idx[r, take:] == -1).all() and np.isneginf(val[r, take:]).all()
+
+
+def test_gemm_topk_composes_steps():
+    d = __import__("workloads").router_tiny(0)
+    qa, sfa, gsa = oracle.quantize(d["x"])
+    qb, sfb, gsb = oracle.quantize(d["w"])
+    logits = oracle.gemm_logits(qa, sfa, gsa, qb, sfb, gsb)
+    score, weight = oracle.epilogue(logits, 1, d["bias"])
+    idx, val, wt = oracle.gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, d["bias"], d["k"])
+    for r in range(logits.shape[0]):
+        ref = _brute_topk(score[r], d["k"])
+        assert list(idx[r]) == ref
+        np.testing.assert_array_equal(val[r], score[r, ref])
+        np.testing.assert_array_equal(wt[r], weight[r, ref])
+    idx2, _, _ = oracle.gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, d["bias"], d["k"], threads=3)
+    np.testing.assert_array_equal(idx, idx2)
