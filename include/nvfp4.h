@@ -1,0 +1,171 @@
+/*
+ * nvfp4.h — C ABI of the GB300 (sm_103a) NVFP4 block-scaled quantize and
+ * GEMM + top-k library (libnvfp4.so).
+ *
+ * The operations are those of the NVFP4 inference path described on the
+ * "nvfp4-megamoe-kernel" repository pages (DeepSeek-V4-Pro on Blackwell):
+ *
+ *   nvfp4_quantize               activation quantize: grid-wide amax ->
+ *                                global scale, E4M3 block scales, E2M1 codes
+ *   nvfp4_deinterleave_quantize  the same for an interleaved SwiGLU gate/up
+ *                                output, deinterleaved to [gate | up] first
+ *   nvfp4_gemm_topk              block-scaled FP4 GEMM with a fused scoring
+ *                                epilogue and per-row top-k
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or keeps them.
+ *   - Every call is asynchronous on the given stream (0 = legacy default
+ *     stream) and performs no host synchronisation.  Global scales stay on
+ *     the device.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     call that returns an error has launched nothing.
+ *   - bf16 data is passed as its 16-bit patterns (uint16_t).
+ *   - NVFP4 tensor of logical shape [rows, cols]:
+ *       q  : uint8 [rows, cols/2], row-major; element 2j of a row is the
+ *            low nibble of byte j, element 2j+1 the high nibble; a nibble
+ *            is sign bit (bit 3) + E2M1 magnitude code (bits 0-2)
+ *       sf : uint8 [rows, cols/16], row-major E4M3 (FN) block scales, one
+ *            per 16 consecutive elements of a row
+ *       gs : one FP32 global scale (device)
+ *     value(r, c) = e2m1(q nibble) * e4m3(sf[r, c/16]) * gs
+ *   - Workspace: a small device buffer of nvfp4_workspace_bytes() bytes,
+ *     zeroed once by nvfp4_workspace_init() (or cudaMemsetAsync) before its
+ *     first use.  Each call leaves it as it found it.  Calls that share one
+ *     workspace must be ordered (same stream or explicit events).
+ *
+ * Return value of every int function: an nvfp4_status.
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID = 1,      /* null pointer, negative size, bad enum, k out of range */
+  NVFP4_ERR_UNSUPPORTED = 2,  /* shape or alignment outside what the kernels take */
+  NVFP4_ERR_WORKSPACE = 3,    /* ws null or ws_bytes < nvfp4_workspace_bytes() */
+  NVFP4_ERR_CUDA = 4          /* a CUDA call failed; see nvfp4_last_cuda_error() */
+} nvfp4_status;
+
+typedef enum nvfp4_epilogue {
+  /* score = logit (indexer-shaped scoring) */
+  NVFP4_EPILOGUE_IDENTITY = 0,
+  /* weight = sqrt(softplus(logit)), score = weight + bias[n] (router-shaped) */
+  NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS = 1
+} nvfp4_epilogue;
+
+/* Device-side status bits a kernel may record in the workspace. */
+#define NVFP4_DEVICE_TIMEOUT 0x1u /* a bounded wait inside a kernel gave up */
+
+/* Bytes of workspace every call needs (a small constant). */
+size_t nvfp4_workspace_bytes(void);
+
+/* Zero a workspace on `stream` (cudaMemsetAsync).  Needed once per buffer. */
+int nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Activation quantize.  Source: commit 107d62d ("Fix: compute gsa at
+ * runtime ... gsa = max(|x|) / (6.0 * 448.0)") and the dsv4/ops/quantize.py
+ * commit ("Two-kernel approach (correct, zero CPU syncs)"); 16-element E4M3
+ * blocks per the compare view's README "NVFP4 throughout"; the E2M1 table of
+ * commit 0d1cd1e.
+ *
+ *   amax  = max(max |x|, 1e-8);  gs = amax / 2688                  (FP32)
+ *   per 16-element block of a row: s = (max|x_block| / 6) / gs     (FP32)
+ *     sf    = E4M3(s), round to nearest even, saturating at 448
+ *     den   = e4m3(sf) * gs                                        (FP32)
+ *     code  = sign(x) | E2M1(|x| / den), round to nearest even,
+ *             saturating at 6; den == 0 gives signed zero codes
+ *
+ * x     : bf16 [rows, cols] with row stride ld_x elements; 16-byte aligned,
+ *         ld_x a multiple of 8, ld_x >= cols.
+ * cols  : multiple of 16.  rows >= 0 (rows == 0 still writes gs for amax 1e-8;
+ *         x, q and sf may then be NULL).
+ * q     : [rows, cols/2] bytes, 8-byte aligned.   sf : [rows, cols/16] bytes.
+ * gs    : one float on the device, written by the call (4-byte aligned).
+ * Two kernels: a grid-wide amax whose last block writes gs, then the
+ * quantize pass, which reads gs from device memory.
+ */
+int nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
+                   uint8_t* q, uint8_t* sf, float* gs,
+                   void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Deinterleave + quantize for a SwiGLU output whose gate and up columns
+ * alternate in groups of `granularity` (commit 0d1cd1e,
+ * "fused_deinterleave_amax_quantize.cu"; the compare view's
+ * docs/PERFORMANCE_AUDIT.md P1, granularity 8).
+ *
+ * x    : bf16 [rows, 2*inter], contiguous rows, 16-byte aligned.  Input
+ *        column 2g*floor(j/g) + (j mod g) is gate column j, and
+ *        2g*floor(j/g) + g + (j mod g) is up column j (g = granularity).
+ * The result is nvfp4_quantize of the [rows, 2*inter] matrix
+ * [gate_0 .. gate_{inter-1} | up_0 .. up_{inter-1}]:
+ * q [rows, inter] bytes (8-byte aligned), sf [rows, inter/8], gs one float.
+ * inter: multiple of 16.  granularity: 1, 2, 4, 8 or 16.
+ */
+int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, int granularity,
+                                uint8_t* q, uint8_t* sf, float* gs,
+                                void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Block-scaled FP4 GEMM + fused epilogue + per-row top-k.  Sources: the
+ * dequant formula of commit db07d17 (w = lut[w] * weight_scale *
+ * weight_scale_2), the global-scale commit of 107d62d ((A*SFA) @ (B*SFB),
+ * then * gsa * gsb), the router score of the same commit and of the compare
+ * view's CORRECTNESS_BACKLOG.md section 5 (sqrt(softplus) + e_bias, top-k),
+ * and the fused router kernel of commit db07d17 (no FP32 logits in GMEM).
+ *
+ *   logit[m, n] = gsa * gsb * sum_k A[m, k] * B[n, k]      (A, B NVFP4 values
+ *                 without their global scales; FP32 tensor-core accumulation)
+ *   epilogue IDENTITY:           weight = score = logit
+ *   epilogue SQRT_SOFTPLUS_BIAS: weight = sqrt(softplus(logit)),
+ *                                score  = weight + bias[n]
+ *   per row m: the k largest scores, in descending order; equal scores are
+ *   ordered by lower n.
+ *
+ * A: qa [M, K/2] (16-byte aligned), sfa [M, K/16] (4-byte aligned), gsa.
+ * B: qb [N, K/2] (16-byte aligned), sfb [N, K/16] (4-byte aligned), gsb.
+ *    (B row n holds output column n: the checkpoint's N x K weight layout.)
+ * M >= 0 (M == 0 launches nothing; qa, sfa and the outputs may then be NULL),
+ * N >= 1, K a positive multiple of 64.  1 <= k <= 1024; for k > 32
+ * the N scores of a row must fit on chip (N <= 4096).
+ * bias: N floats, required for SQRT_SOFTPLUS_BIAS, ignored for IDENTITY.
+ * Outputs, each [M, k] row-major: topk_idx (int32), topk_score (float),
+ * topk_weight (float, may be NULL).  Slots beyond N hold idx -1,
+ * score -inf, weight 0.
+ * logits: NULL in production; if non-NULL, [M, N] FP32 logits are also
+ * written (for testing the GEMM stage on its own).
+ */
+int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
+                    const uint8_t* qb, const uint8_t* sfb, const float* gsb,
+                    int64_t M, int64_t N, int64_t K,
+                    int epilogue, const float* bias, int k,
+                    int32_t* topk_idx, float* topk_score, float* topk_weight,
+                    float* logits, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Diagnostic: synchronise `stream`, copy the workspace's device status bits
+ * (NVFP4_DEVICE_*) to *status, and clear them.  Not for the hot path.
+ */
+int nvfp4_read_device_status(void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* nvfp4_status_string(int status);
+
+/* The cudaError_t of the last call that returned NVFP4_ERR_CUDA on this thread. */
+int nvfp4_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

@@ -1,0 +1,193 @@
+"""Python binding of libnvfp4 (GB300 / sm_103a NVFP4 quantize and GEMM + top-k).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels, reached through its C ABI (``include/nvfp4.h``) with ``ctypes``.
+PyTorch supplies device memory and streams.  There is no fallback: if
+``libnvfp4.so`` has not been built (``quantize_block_scaled_gb300.build``) or
+cannot be loaded, every call raises.
+
+The three entry points keep the C names:
+
+* ``nvfp4_quantize(x, q, sf, gs, ws, stream=None)``
+* ``nvfp4_deinterleave_quantize(x, granularity, q, sf, gs, ws, stream=None)``
+* ``nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, idx, score,
+  weight=None, logits=None, ws=..., stream=None)``
+
+plus allocating conveniences (``quantize``, ``deinterleave_quantize``,
+``gemm_topk``, ``workspace``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+
+EPILOGUE_IDENTITY = 0
+EPILOGUE_SQRT_SOFTPLUS_BIAS = 1
+DEVICE_TIMEOUT = 0x1
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or alignment",
+           3: "workspace missing or too small", 4: "CUDA error"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        msg = f"{fn}: {_STATUS.get(status, 'unknown status')} (status {status})"
+        if status == 4:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libnvfp4.so (raises if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run quantize_block_scaled_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        L.nvfp4_workspace_bytes.restype = SZ
+        L.nvfp4_workspace_bytes.argtypes = []
+        L.nvfp4_workspace_init.restype = I
+        L.nvfp4_workspace_init.argtypes = [P, SZ, P]
+        L.nvfp4_quantize.restype = I
+        L.nvfp4_quantize.argtypes = [P, I64, I64, I64, P, P, P, P, SZ, P]
+        L.nvfp4_deinterleave_quantize.restype = I
+        L.nvfp4_deinterleave_quantize.argtypes = [P, I64, I64, I, P, P, P, P, SZ, P]
+        L.nvfp4_gemm_topk.restype = I
+        L.nvfp4_gemm_topk.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, P, I, P, P, P, P, P, SZ, P]
+        L.nvfp4_read_device_status.restype = I
+        L.nvfp4_read_device_status.argtypes = [P, SZ, ctypes.POINTER(ctypes.c_uint32), P]
+        L.nvfp4_status_string.restype = ctypes.c_char_p
+        L.nvfp4_status_string.argtypes = [I]
+        L.nvfp4_last_cuda_error.restype = I
+        L.nvfp4_last_cuda_error.argtypes = []
+        _lib = L
+        return L
+
+
+EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
+                    "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
+                    "nvfp4_status_string", "nvfp4_last_cuda_error")
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise NVFP4Error(fn, status, lib().nvfp4_last_cuda_error() if status == 4 else 0)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libnvfp4 must be CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _bf16_bits(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype == torch.bfloat16:
+        return x
+    if x.dtype in (torch.int16, torch.uint16):
+        return x
+    raise TypeError("x must be bfloat16 (or its bit patterns as int16/uint16)")
+
+
+# ---------------------------------------------------------------- raw entry points
+
+def workspace_bytes() -> int:
+    return int(lib().nvfp4_workspace_bytes())
+
+
+def workspace(device=None, stream=None) -> torch.Tensor:
+    """A zeroed workspace buffer for the calls below (one per stream)."""
+    ws = torch.empty(workspace_bytes(), dtype=torch.uint8, device=device or "cuda")
+    _check("nvfp4_workspace_init", lib().nvfp4_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def nvfp4_quantize(x, q, sf, gs, ws, stream=None):
+    x = _bf16_bits(x)
+    rows, cols = x.shape
+    _check("nvfp4_quantize", lib().nvfp4_quantize(
+        _ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def nvfp4_deinterleave_quantize(x, granularity, q, sf, gs, ws, stream=None):
+    x = _bf16_bits(x)
+    rows, width = x.shape
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    _check("nvfp4_deinterleave_quantize", lib().nvfp4_deinterleave_quantize(
+        _ptr(x), rows, width // 2, int(granularity), _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, idx, score, weight=None,
+                    logits=None, ws=None, stream=None):
+    M = qa.shape[0]
+    K = qa.shape[1] * 2
+    N = qb.shape[0]
+    _check("nvfp4_gemm_topk", lib().nvfp4_gemm_topk(
+        _ptr(qa), _ptr(sfa), _ptr(gsa), _ptr(qb), _ptr(sfb), _ptr(gsb), M, N, K, int(epilogue),
+        _ptr(bias), int(k), _ptr(idx), _ptr(score), _ptr(weight), _ptr(logits), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def read_device_status(ws, stream=None) -> int:
+    """Synchronising diagnostic: device status bits recorded in ws (then cleared)."""
+    out = ctypes.c_uint32(0)
+    _check("nvfp4_read_device_status", lib().nvfp4_read_device_status(
+        _ptr(ws), ws.numel(), ctypes.byref(out), _stream(stream)))
+    return int(out.value)
+
+
+# ---------------------------------------------------------------- allocating helpers
+
+def quantize(x: torch.Tensor, ws: torch.Tensor, stream=None):
+    """(q [rows, cols/2] u8, sf [rows, cols/16] u8, gs [1] f32) of a bf16 [rows, cols] tensor."""
+    rows, cols = x.shape
+    q = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=x.device)
+    gs = torch.empty(1, dtype=torch.float32, device=x.device)
+    nvfp4_quantize(x, q, sf, gs, ws, stream)
+    return q, sf, gs
+
+
+def deinterleave_quantize(x: torch.Tensor, granularity: int, ws: torch.Tensor, stream=None):
+    rows, width = x.shape
+    q = torch.empty(rows, width // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(rows, width // 16, dtype=torch.uint8, device=x.device)
+    gs = torch.empty(1, dtype=torch.float32, device=x.device)
+    nvfp4_deinterleave_quantize(x, granularity, q, sf, gs, ws, stream)
+    return q, sf, gs
+
+
+def gemm_topk(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, ws, want_weight=True,
+              want_logits=False, stream=None):
+    M, N = qa.shape[0], qb.shape[0]
+    dev = qa.device
+    idx = torch.empty(M, k, dtype=torch.int32, device=dev)
+    score = torch.empty(M, k, dtype=torch.float32, device=dev)
+    weight = torch.empty(M, k, dtype=torch.float32, device=dev) if want_weight else None
+    logits = torch.empty(M, N, dtype=torch.float32, device=dev) if want_logits else None
+    nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, idx, score, weight, logits,
+                    ws, stream)
+    return idx, score, weight, logits

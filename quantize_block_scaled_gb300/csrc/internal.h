@@ -1,0 +1,55 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace nvfp4 {
+
+// Layout of the caller's workspace.  Every kernel that touches a field puts
+// it back to zero before it finishes, so the buffer stays zeroed between
+// calls.
+struct Workspace {
+  uint32_t amax_bits;  // running max of |x| as FP32 bits (valid for x >= 0)
+  uint32_t done;       // blocks of the amax kernel that have finished
+  uint32_t status;     // NVFP4_DEVICE_* bits; cleared by nvfp4_read_device_status
+  uint32_t reserved[61];
+};
+static_assert(sizeof(Workspace) == 256, "workspace layout");
+constexpr size_t kWorkspaceBytes = sizeof(Workspace);
+
+int sm_count();
+
+cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
+                        Workspace* ws, cudaStream_t stream);
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,
+                            uint8_t* sf, const float* gs, cudaStream_t stream);
+
+cudaError_t launch_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, int g,
+                                         uint8_t* q, uint8_t* sf, const float* gs,
+                                         cudaStream_t stream);
+
+struct GemmTopkArgs {
+  const uint8_t* qa;
+  const uint8_t* sfa;
+  const float* gsa;
+  const uint8_t* qb;
+  const uint8_t* sfb;
+  const float* gsb;
+  int64_t M, N, K;
+  int epilogue;
+  const float* bias;
+  int k;
+  int32_t* topk_idx;
+  float* topk_score;
+  float* topk_weight;
+  float* logits;
+  Workspace* ws;
+};
+
+// Returns an nvfp4_status; on NVFP4_ERR_CUDA the CUDA error is in *err.
+int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* err);
+
+}  // namespace nvfp4

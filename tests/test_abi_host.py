@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must build, load, and export every function include/nvfp4.h
+declares.  Argument validation runs on the host before any CUDA call, so
+invalid calls can be exercised here with fake (never dereferenced) pointers.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantize_block_scaled_gb300 import build as b
+    b.build()
+    import quantize_block_scaled_gb300 as q
+    return q.lib()
+
+
+def test_header_declares_the_three_entry_points():
+    fns = _declared_functions()
+    for name in ("nvfp4_quantize", "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(L):
+    import quantize_block_scaled_gb300 as q
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    assert set(_declared_functions()) == set(q.EXPORTED_SYMBOLS)
+
+
+def test_status_strings_and_workspace_size(L):
+    assert L.nvfp4_status_string(0) == b"ok"
+    assert L.nvfp4_status_string(2) == b"unsupported shape or alignment"
+    assert L.nvfp4_workspace_bytes() == 256
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_quantize_validation(L):
+    ws = _p(FAKE)
+    # null input (allowed only when there are no rows), null gs
+    assert L.nvfp4_quantize(None, 4, 32, 32, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 1
+    assert L.nvfp4_quantize(_p(FAKE), 4, 32, 32, _p(FAKE), _p(FAKE), None, ws, 256, None) == 1
+    # negative rows, ld < cols
+    assert L.nvfp4_quantize(_p(FAKE), -1, 32, 32, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 1
+    assert L.nvfp4_quantize(_p(FAKE), 4, 32, 16, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 1
+    # cols not a multiple of 16, misaligned x, ld not a multiple of 8
+    assert L.nvfp4_quantize(_p(FAKE), 4, 40, 40, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 2
+    assert L.nvfp4_quantize(_p(FAKE + 2), 4, 32, 32, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 2
+    assert L.nvfp4_quantize(_p(FAKE), 4, 32, 36, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 2
+    # workspace missing or short
+    assert L.nvfp4_quantize(_p(FAKE), 4, 32, 32, _p(FAKE), _p(FAKE), _p(FAKE), None, 256, None) == 3
+    assert L.nvfp4_quantize(_p(FAKE), 4, 32, 32, _p(FAKE), _p(FAKE), _p(FAKE), ws, 64, None) == 3
+
+
+def test_deinterleave_validation(L):
+    ws = _p(FAKE)
+    assert L.nvfp4_deinterleave_quantize(_p(FAKE), 2, 64, 3, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 2
+    assert L.nvfp4_deinterleave_quantize(_p(FAKE), 2, 40, 8, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 2
+    assert L.nvfp4_deinterleave_quantize(_p(FAKE), 2, 0, 8, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 1
+    assert L.nvfp4_deinterleave_quantize(None, 2, 64, 8, _p(FAKE), _p(FAKE), _p(FAKE), ws, 256, None) == 1
+
+
+def _gemm(L, M=4, N=64, K=512, epilogue=1, bias=FAKE, k=6, qa=FAKE, sfa=FAKE, ws=FAKE, ws_bytes=256):
+    P = _p
+    return L.nvfp4_gemm_topk(P(qa), P(sfa), P(FAKE), P(FAKE), P(FAKE), P(FAKE), M, N, K, epilogue,
+                             P(bias) if bias else None, k, P(FAKE), P(FAKE), None, None,
+                             P(ws) if ws else None, ws_bytes, None)
+
+
+def test_gemm_validation(L):
+    assert _gemm(L, k=0) == 1
+    assert _gemm(L, k=1025) == 1
+    assert _gemm(L, epilogue=2) == 1
+    assert _gemm(L, epilogue=1, bias=0) == 1       # router epilogue needs a bias
+    assert _gemm(L, M=-1) == 1
+    assert _gemm(L, N=0) == 1
+    assert _gemm(L, K=480) == 2                    # K must be a multiple of 64
+    assert _gemm(L, k=512, N=8192) == 2            # large k needs N <= 4096
+    assert _gemm(L, qa=FAKE + 8) == 2              # codes must be 16-byte aligned
+    assert _gemm(L, sfa=FAKE + 2) == 2             # scales 4-byte aligned
+    assert _gemm(L, ws=0) == 3
+    assert _gemm(L, ws_bytes=16) == 3
