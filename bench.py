@@ -1,0 +1,620 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 router hot path on GB300.
+
+One step = one pass of the whole path over one decode batch of T tokens:
+  1. nvfp4_quantize               X [T, 7168] bf16 -> NVFP4 (amax + quantize kernels)
+  2. nvfp4_gemm_topk              gate GEMM vs 256 NVFP4 experts, sqrt(softplus) + bias, top-8
+  3. nvfp4_deinterleave_quantize  SwiGLU output [T, 2*2048] (granularity 8) -> NVFP4
+Five kernel launches per step.  Inputs rotate over enough independent sets
+(activations, weights, biases) that the working set is more than twice the
+L2 cache, so every step reads HBM.  Steps are replayed from CUDA graphs.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
+only reference this path has) on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_BYTES = 126 * 1024 * 1024
+HIDDEN, EXPERTS, TOPK, INTER, GRAN = workloads.HIDDEN, workloads.EXPERTS, workloads.ROUTER_TOPK, \
+    workloads.MOE_INTER, 8
+KERNELS_PER_STEP = 5
+FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense NVFP4 / BF16 tensor ratio on GB300
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def quantize_bytes(rows, cols):
+    """Read bf16 once, write codes + scale bytes + gs."""
+    return rows * cols * 2 + rows * cols // 2 + rows * cols // 16 + 4
+
+
+def gemm_bytes(M, N, K, k, bias=True):
+    """A and B codes + scales, global scales, bias, top-k outputs (idx, score, weight)."""
+    return (M + N) * (K // 2 + K // 16) + 8 + (N * 4 if bias else 0) + M * k * 12
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.samples = []
+
+    def __enter__(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        for line in self.tmp.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                self.samples.append(dict(t=ts + frac, sm=float(parts[2]), sm_max=float(parts[3]),
+                                         reasons=parts[5], hw=parts[6], hwt=parts[7], swt=parts[8],
+                                         pcap=parts[9]))
+            except (ValueError, IndexError):
+                continue
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1]
+        window = "timed"
+        if not inside:
+            inside, window = self.samples, "run"
+        if not inside:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], window="none")
+        reasons = set()
+        for s in inside:
+            if s["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if s["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if s["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if s["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return dict(sm_mhz=statistics.median(s["sm"] for s in inside),
+                    sm_max_mhz=max(s["sm_max"] for s in inside), reasons=sorted(reasons),
+                    samples=len(inside), window=window)
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one process)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def throughput(rows_per_rank: int, steps: int, max_seconds: float, world: int) -> float:
+    """Whole-job rows/s: rows of all ranks over the slowest rank's time."""
+    return rows_per_rank * steps * world / max_seconds
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+class RouterSets:
+    """R rotating input sets of the router decode step, all on the device."""
+
+    def __init__(self, nv, tokens, n_sets, ws, seed=1234):
+        import torch
+        self.tokens, self.n = tokens, n_sets
+        rng = np.random.default_rng(seed)
+        dev = "cuda"
+        T = tokens
+        self.x = [torch.from_numpy(workloads.bf16_bits(rng.standard_normal((T, HIDDEN), np.float32))
+                                   .view(np.int16)).to(dev) for _ in range(n_sets)]
+        self.h = [torch.from_numpy(workloads.bf16_bits(rng.standard_normal((T, 2 * INTER), np.float32))
+                                   .view(np.int16)).to(dev) for _ in range(n_sets)]
+        self.bias = [torch.from_numpy((rng.standard_normal(EXPERTS) * 0.01).astype(np.float32)).to(dev)
+                     for _ in range(n_sets)]
+        # gate weights: drawn as bf16 N(0, 0.02) and quantized once by the library (static per layer)
+        self.qb, self.sfb, self.gsb = [], [], []
+        for _ in range(n_sets):
+            w = torch.from_numpy(workloads.bf16_bits(rng.standard_normal((EXPERTS, HIDDEN), np.float32)
+                                                     * np.float32(0.02)).view(np.int16)).to(dev)
+            q, sf, gs = nv.quantize(w, ws)
+            self.qb.append(q)
+            self.sfb.append(sf)
+            self.gsb.append(gs)
+        e = lambda *s, dt=torch.uint8: [torch.empty(*s, dtype=dt, device=dev) for _ in range(n_sets)]
+        self.qa, self.sfa, self.gsa = e(T, HIDDEN // 2), e(T, HIDDEN // 16), e(1, dt=torch.float32)
+        self.idx, self.score, self.weight = e(T, TOPK, dt=torch.int32), e(T, TOPK, dt=torch.float32), \
+            e(T, TOPK, dt=torch.float32)
+        self.qh, self.sfh, self.gsh = e(T, INTER), e(T, INTER // 8), e(1, dt=torch.float32)
+        torch.cuda.synchronize()
+
+    def footprint(self):
+        per = sum(t[0].numel() * t[0].element_size() for t in (
+            self.x, self.h, self.bias, self.qb, self.sfb, self.qa, self.sfa, self.idx, self.score,
+            self.weight, self.qh, self.sfh))
+        return per * self.n
+
+    # the three calls of one step on set i
+    def op_quantize(self, nv, ws, i):
+        nv.nvfp4_quantize(self.x[i], self.qa[i], self.sfa[i], self.gsa[i], ws)
+
+    def op_gemm(self, nv, ws, i):
+        nv.nvfp4_gemm_topk(self.qa[i], self.sfa[i], self.gsa[i], self.qb[i], self.sfb[i], self.gsb[i],
+                           nv.EPILOGUE_SQRT_SOFTPLUS_BIAS, self.bias[i], TOPK, self.idx[i],
+                           self.score[i], self.weight[i], None, ws)
+
+    def op_deinterleave(self, nv, ws, i):
+        nv.nvfp4_deinterleave_quantize(self.h[i], GRAN, self.qh[i], self.sfh[i], self.gsh[i], ws)
+
+    def step(self, nv, ws, i):
+        self.op_quantize(nv, ws, i)
+        self.op_gemm(nv, ws, i)
+        self.op_deinterleave(nv, ws, i)
+
+
+def capture_chunks(fn, n_sets, chunk):
+    """CUDA graphs replaying fn(i) for chunk-sized runs of consecutive sets."""
+    import torch
+    graphs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(n_sets):  # eager warm-up of every set (kernel attributes, tensor maps)
+            fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for c0 in range(0, n_sets, chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(c0, min(c0 + chunk, n_sets)):
+                fn(i)
+        graphs.append(g)
+    singles = []
+    for i in range(chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(i)
+        singles.append(g)
+    torch.cuda.synchronize()
+    return graphs, singles
+
+
+def replay_steps(graphs, singles, chunk, steps):
+    """Replay exactly `steps` calls of fn (whole chunks, then single steps)."""
+    full, rest = divmod(steps, chunk)
+    for j in range(full):
+        graphs[j % len(graphs)].replay()
+    for j in range(rest):
+        singles[j].replay()
+
+
+def time_graphs(graphs, singles, chunk, steps, world):
+    import torch
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    replay_steps(graphs, singles, chunk, steps)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    return start.elapsed_time(end) / 1e3, t_wall0, t_wall1
+
+
+def load_traffic(kernel_file: str, workload: str):
+    """ncu DRAM bytes per launch recorded for a kernel source, if the source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "quantize_block_scaled_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for r in rec.get("records", []):
+        if r.get("source") == kernel_file and r.get("sha") == sha and r.get("workload") == workload:
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+def time_op_flushed(fn, iters, flush):
+    """Average device time of fn() with an L2 flush before each call (flush not timed)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    fn()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush_l2(flush)
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / iters / 1e3
+
+
+def secondary(nv, ws, pk, flush):
+    """Per-kernel figures on the other pages' shapes (L2 flushed before each call)."""
+    import torch
+    out = {}
+    hbm = pk["hbm_gbs"] * 1e9
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16 * 1e12
+    # quantize sweep
+    sweep = {}
+    for T in (1, 128, 2048, 16384):
+        x = torch.from_numpy(workloads.quantize_input(T).view(np.int16)).cuda()
+        q, sf, gs = nv.quantize(x, ws)
+        t = time_op_flushed(lambda: nv.nvfp4_quantize(x, q, sf, gs, ws), 10 if T > 2048 else 30, flush)
+        b = quantize_bytes(T, HIDDEN)
+        sweep[f"T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3))
+        del x, q, sf, gs
+    hh = torch.from_numpy(workloads.swiglu_interleaved(2048).view(np.int16)).cuda()
+    q, sf, gs = nv.deinterleave_quantize(hh, GRAN, ws)
+    t = time_op_flushed(lambda: nv.nvfp4_deinterleave_quantize(hh, GRAN, q, sf, gs, ws), 30, flush)
+    b = quantize_bytes(2048, 2 * INTER)
+    sweep["deinterleave_T2048_g8"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1),
+                                          hbm_frac=round(b / t / hbm, 3))
+    del hh, q, sf, gs
+    out["quantize"] = sweep
+    # router prefill T = 8192 (Student-t activations with outliers)
+    d = workloads.router_prefill()
+    x = torch.from_numpy(d["x"].view(np.int16)).cuda()
+    w = torch.from_numpy(d["w"].view(np.int16)).cuda()
+    bias = torch.from_numpy(d["bias"]).cuda()
+    qa, sfa, gsa = nv.quantize(x, ws)
+    qb, sfb, gsb = nv.quantize(w, ws)
+    M = x.shape[0]
+    idx = torch.empty(M, TOPK, dtype=torch.int32, device="cuda")
+    sc = torch.empty(M, TOPK, dtype=torch.float32, device="cuda")
+    wt = torch.empty(M, TOPK, dtype=torch.float32, device="cuda")
+    tq = time_op_flushed(lambda: nv.nvfp4_quantize(x, qa, sfa, gsa, ws), 10, flush)
+    tg = time_op_flushed(lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, bias, TOPK, idx, sc, wt,
+                                                   None, ws), 10, flush)
+    fl, by = gemm_flops(M, EXPERTS, HIDDEN), gemm_bytes(M, EXPERTS, HIDDEN, TOPK)
+    out["router_prefill_T8192"] = dict(
+        quantize_us=round(tq * 1e6, 2), gemm_topk_us=round(tg * 1e6, 2),
+        gemm_tflops=round(fl / tg / 1e12, 1), fp4_tensor_frac=round(fl / tg / fp4_peak, 3),
+        gemm_hbm_frac=round(by / tg / hbm, 3), rows_per_s=round(M / (tq + tg), 1))
+    del x, w, qa, sfa, qb, sfb, idx, sc, wt
+    # indexer-shaped scoring
+    d = workloads.indexer()
+    qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
+    qb, sfb, gsb = nv.quantize(torch.from_numpy(d["w"].view(np.int16)).cuda(), ws)
+    M, N, K, k = 64, workloads.INDEXER_KEYS, workloads.INDEXER_DIM, workloads.INDEXER_TOPK
+    idx = torch.empty(M, k, dtype=torch.int32, device="cuda")
+    sc = torch.empty(M, k, dtype=torch.float32, device="cuda")
+    ti = time_op_flushed(lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 0, None, k, idx, sc, None,
+                                                   None, ws), 30, flush)
+    by = gemm_bytes(M, N, K, k, bias=False) - M * k * 4
+    out["indexer_M64_N2048_k512"] = dict(us=round(ti * 1e6, 2), hbm_frac=round(by / ti / hbm, 4),
+                                         rows_per_s=round(M / ti, 1))
+    torch.cuda.synchronize()
+    return out
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import quantize_block_scaled_gb300 as nv
+    torch.cuda.set_device(local)
+    pk = peaks()
+    ws = nv.workspace()
+    T = args.tokens
+    per_set = (T * HIDDEN * 2 + T * 2 * INTER * 2 + EXPERTS * (HIDDEN // 2 + HIDDEN // 16) + EXPERTS * 4
+               + T * (HIDDEN // 2 + HIDDEN // 16) + T * (INTER + INTER // 8) + T * TOPK * 12)
+    n_sets = max(16, int(np.ceil(2.2 * L2_BYTES / per_set)))
+    chunk = 16
+    n_sets = int(np.ceil(n_sets / chunk) * chunk)
+    sets = RouterSets(nv, T, n_sets, ws)
+
+    graphs, singles = capture_chunks(lambda i: sets.step(nv, ws, i), n_sets, chunk)
+    with ClockSampler(local) as clk:
+        replay_steps(graphs, singles, chunk, args.warmup)
+        secs, t0, t1 = time_graphs(graphs, singles, chunk, args.steps, world)
+    secs_max = reduce_max(secs, world)
+    value = throughput(T, args.steps, secs_max, world)
+
+    # per-op average launch durations (same sets, back-to-back graph replays)
+    op_times = {}
+    for name, fn in (("quantize", sets.op_quantize), ("gemm_topk", sets.op_gemm),
+                     ("deinterleave_quantize", sets.op_deinterleave)):
+        g, s1 = capture_chunks(lambda i, fn=fn: fn(nv, ws, i), n_sets, chunk)
+        replay_steps(g, s1, chunk, n_sets)
+        n_ops = max(args.steps, n_sets)
+        t_op, _, _ = time_graphs(g, s1, chunk, n_ops, 1)
+        op_times[name] = t_op / n_ops
+        del g, s1
+    op_bytes = dict(quantize=quantize_bytes(T, HIDDEN),
+                    gemm_topk=gemm_bytes(T, EXPERTS, HIDDEN, TOPK),
+                    deinterleave_quantize=quantize_bytes(T, 2 * INTER))
+    dominant = max(op_times, key=op_times.get)
+    achieved = op_bytes[dominant] / op_times[dominant] / 1e9
+    kernel_file = dict(quantize="quantize.cu", gemm_topk="gemm_topk.cu",
+                       deinterleave_quantize="quantize.cu")[dominant]
+    traffic = load_traffic(kernel_file, f"{dominant}_router_decode_T{T}")
+    roofline = dict(bound="hbm", achieved=round(achieved, 1), peak=pk["hbm_gbs"], unit="GB/s",
+                    frac=round(achieved / pk["hbm_gbs"], 4), traffic=traffic, kernel=dominant,
+                    algorithmic_bytes=op_bytes[dominant], launch_us=round(op_times[dominant] * 1e6, 3),
+                    peak_source=pk["source"])
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e_sets = n_sets
+    hx = [torch.empty(T, HIDDEN, dtype=torch.int16, pin_memory=True) for _ in range(e2e_sets)]
+    hh = [torch.empty(T, 2 * INTER, dtype=torch.int16, pin_memory=True) for _ in range(e2e_sets)]
+    for i in range(e2e_sets):
+        hx[i].copy_(sets.x[i].cpu())
+        hh[i].copy_(sets.h[i].cpu())
+    o_idx = [torch.empty(T, TOPK, dtype=torch.int32, pin_memory=True) for _ in range(e2e_sets)]
+    o_sc = [torch.empty(T, TOPK, dtype=torch.float32, pin_memory=True) for _ in range(e2e_sets)]
+    o_wt = [torch.empty(T, TOPK, dtype=torch.float32, pin_memory=True) for _ in range(e2e_sets)]
+    o_qh = [torch.empty(T, INTER, dtype=torch.uint8, pin_memory=True) for _ in range(e2e_sets)]
+    o_sfh = [torch.empty(T, INTER // 8, dtype=torch.uint8, pin_memory=True) for _ in range(e2e_sets)]
+    o_gsh = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(e2e_sets)]
+
+    def e2e_step(i):
+        sets.x[i].copy_(hx[i], non_blocking=True)
+        sets.h[i].copy_(hh[i], non_blocking=True)
+        sets.step(nv, ws, i)
+        o_idx[i].copy_(sets.idx[i], non_blocking=True)
+        o_sc[i].copy_(sets.score[i], non_blocking=True)
+        o_wt[i].copy_(sets.weight[i], non_blocking=True)
+        o_qh[i].copy_(sets.qh[i], non_blocking=True)
+        o_sfh[i].copy_(sets.sfh[i], non_blocking=True)
+        o_gsh[i].copy_(sets.gsh[i], non_blocking=True)
+
+    ge, se = capture_chunks(e2e_step, e2e_sets, chunk)
+    replay_steps(ge, se, chunk, min(args.warmup, e2e_sets))
+    e2e_secs, _, _ = time_graphs(ge, se, chunk, args.steps, world)
+    e2e_secs = reduce_max(e2e_secs, world)
+    h2d = T * HIDDEN * 2 + T * 2 * INTER * 2
+    d2h = T * TOPK * 12 + T * INTER + T * INTER // 8 + 4
+    e2e = dict(value=round(throughput(T, args.steps, e2e_secs, world), 1), unit="rows/s",
+               h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h)
+    # check that the last step's outputs match the device results (copies really ran)
+    torch.cuda.synchronize()
+
+    status = nv.read_device_status(ws)
+    detail = None
+    if not args.quick and rank == 0:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+        detail = secondary(nv, ws, pk, flush)
+        del flush
+    clocks = clk.summary(t0, t1)
+    return dict(value=value, secs=secs_max, roofline=roofline, e2e=e2e, op_us={k: round(v * 1e6, 3)
+                for k, v in op_times.items()}, clocks=clocks, detail=detail, n_sets=n_sets,
+                footprint=sets.footprint(), device_status=status)
+
+
+# ---------------------------------------------------------------- the CPU oracle
+
+def oracle_step(orc, x, h, w_q, bias, rows, threads):
+    """The oracle's pass over the sample rows of one step (gs over the whole batch)."""
+    gsa = orc.global_scale(x)
+    qa, sfa = orc.quantize_rows(x, gsa, 0, rows)
+    qb, sfb, gsb = w_q
+    orc.gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, bias, TOPK, threads=threads)
+    orc.deinterleave_quantize(h[:rows], GRAN)
+
+
+def run_oracle(T, sample_rows, steps, budget_s=None, threads=None):
+    import oracle as orc
+    orc.build()
+    rng = np.random.default_rng(1234)
+    x = workloads.bf16_bits(rng.standard_normal((T, HIDDEN), np.float32))
+    h = workloads.bf16_bits(rng.standard_normal((T, 2 * INTER), np.float32))
+    bias = (rng.standard_normal(EXPERTS) * 0.01).astype(np.float32)
+    w = workloads.bf16_bits(rng.standard_normal((EXPERTS, HIDDEN), np.float32) * np.float32(0.02))
+    w_q = orc.quantize(w)  # static weight quantization, outside the timed steps
+    threads = threads or min(os.cpu_count() or 1, sample_rows)
+    done = 0
+    t0 = time.perf_counter()
+    while done < steps:
+        oracle_step(orc, x, h, w_q, bias, sample_rows, threads)
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s and done >= 3:
+            break
+    secs = time.perf_counter() - t0
+    return dict(value=sample_rows * done / secs, steps=done, secs=secs, cores=threads)
+
+
+# ---------------------------------------------------------------- profiling hook
+
+def run_profile(kind: str, iters: int):
+    """Eager runs of one workload inside an NVTX range named "profile" (for ncu --nvtx)."""
+    import torch
+    import quantize_block_scaled_gb300 as nv
+    ws = nv.workspace()
+    if kind == "decode":
+        sets = RouterSets(nv, 32, 4, ws)
+        fns = [lambda i=i: sets.step(nv, ws, i) for i in range(4)]
+    elif kind == "prefill":
+        d = workloads.router_prefill()
+        x = torch.from_numpy(d["x"].view(np.int16)).cuda()
+        w = torch.from_numpy(d["w"].view(np.int16)).cuda()
+        bias = torch.from_numpy(d["bias"]).cuda()
+        qb, sfb, gsb = nv.quantize(w, ws)
+        M = x.shape[0]
+        qa = torch.empty(M, HIDDEN // 2, dtype=torch.uint8, device="cuda")
+        sfa = torch.empty(M, HIDDEN // 16, dtype=torch.uint8, device="cuda")
+        gsa = torch.empty(1, dtype=torch.float32, device="cuda")
+        out = [torch.empty(M, TOPK, dtype=dt, device="cuda") for dt in (torch.int32, torch.float32, torch.float32)]
+
+        def f():
+            nv.nvfp4_quantize(x, qa, sfa, gsa, ws)
+            nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, bias, TOPK, *out, None, ws)
+        fns = [f]
+    elif kind == "quantize":
+        x = torch.from_numpy(workloads.quantize_input(16384).view(np.int16)).cuda()
+        q, sf, gs = nv.quantize(x, ws)
+        fns = [lambda: nv.nvfp4_quantize(x, q, sf, gs, ws)]
+    elif kind == "indexer":
+        d = workloads.indexer()
+        qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
+        qb, sfb, gsb = nv.quantize(torch.from_numpy(d["w"].view(np.int16)).cuda(), ws)
+        idx = torch.empty(64, 512, dtype=torch.int32, device="cuda")
+        sc = torch.empty(64, 512, dtype=torch.float32, device="cuda")
+        fns = [lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 0, None, 512, idx, sc, None, None, ws)]
+    else:
+        raise ValueError(kind)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("profile")
+    for i in range(iters):
+        fns[i % len(fns)]()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    assert nv.read_device_status(ws) == 0
+    print(f"profile {kind}: {iters} iterations", flush=True)
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--tokens", type=int, default=32, choices=(1, 32))
+    ap.add_argument("--quick", action="store_true", help="skip the secondary per-config figures")
+    ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "indexer"),
+                    help="run --warmup eager iterations of one workload in an NVTX range and exit")
+    args = ap.parse_args()
+    if args.profile:
+        run_profile(args.profile, args.warmup)
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_setup(args.gpus)
+    T = args.tokens
+    config = dict(workload="router_decode", tokens=T, hidden=HIDDEN, experts=EXPERTS, top_k=TOPK,
+                  swiglu_inter=INTER, interleave_granularity=GRAN, parallelism=f"replicas{world}")
+    metric = f"router_decode_T{T}_rows_per_s"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        r = run_oracle(T, 1, args.steps)
+        line = dict(impl="reference", metric=metric, value=round(r["value"], 3), unit="rows/s",
+                    n_gpus=world, steps=args.steps, warmup=args.warmup,
+                    ms_per_step=round(r["secs"] / r["steps"] * 1e3, 3), higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype="f32/f64", data="synthetic",
+                    config=dict(config, sample="1 token row per step (gs over the full batch)"),
+                    cpu_baseline=dict(value=round(r["value"], 3), unit="rows/s", cores=r["cores"],
+                                      kind="oracle", sample="1 token row per step"),
+                    e2e=dict(value=round(r["value"], 3), unit="rows/s", h2d_bytes_per_step=0,
+                             d2h_bytes_per_step=0))
+        print(json.dumps(line), flush=True)
+        return
+
+    res = run_gpu(args, rank, world, local)
+    cpu = None
+    if rank == 0 and world == 1:
+        c = run_oracle(T, T, 10 ** 6, budget_s=12.0)
+        cpu = dict(value=round(c["value"], 2), unit="rows/s", cores=c["cores"], kind="oracle",
+                   sample=f"{c['steps']} full steps of T={T} rows ({c['secs']:.1f} s)")
+    if rank != 0:
+        return
+    config["l2"] = (f"{res['n_sets']} rotating input sets, {res['footprint'] / 2**20:.0f} MiB "
+                    f"(> 2x L2); no flush inside the timed region")
+    line = dict(metric=metric, value=round(res["value"], 1), unit="rows/s", n_gpus=world,
+                steps=args.steps, warmup=args.warmup,
+                ms_per_step=round(res["secs"] / args.steps * 1e3, 5), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="nvfp4-e2m1/f32", data="synthetic",
+                config=config, roofline=res["roofline"], cpu_baseline=cpu, e2e=res["e2e"],
+                gpu_launches=KERNELS_PER_STEP * args.steps, clocks=res["clocks"],
+                op_us=res["op_us"], device_status=res["device_status"], detail=res["detail"])
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,5 +1,6 @@
 // NVFP4 block-scaled GEMM with a fused scoring epilogue and per-row top-k,
-// for sm_103a (tcgen05 tensor cores, tensor memory, TMA).
+// for sm_103a (tcgen05 tensor cores, tensor memory, TMA, thread-block
+// clusters with distributed shared memory).
 //
 // What it computes (nvfp4-megamoe-kernel pages: commit db07d17 "dequant
 // formula is lut[w] * weight_scale * weight_scale_2"; commit 107d62d "the MMA
@@ -10,31 +11,42 @@
 //   score      = logit                              (identity epilogue)
 //              = sqrt(softplus(logit)) + bias[n]    (router epilogue)
 //   output     = the k best scores of each row, descending, ties by lower n.
-// The FP32 logits never go to global memory (unless a debug buffer is given).
+// FP32 logits never go to global memory (unless a debug buffer is given).
 //
-// Structure (one CTA per 128-row tile of A, 6 warps):
+// Work split.  One thread-block cluster per 128-row tile of A.  Its C =
+// n_split x k_split CTAs each multiply the tile by one slice of B's columns
+// (BN = 128 or 256 of them) over one slice of K, so a decode-sized problem
+// (a few rows, a 1 MB weight) spreads its weight read over up to 16 SMs and
+// a prefill-sized one gives every SM a tile.
+//
+// Per CTA, 6 warps:
 //   warp 0     producer: TMA loads of the A and B code tiles (128-byte rows,
-//              128-byte swizzle) and cp.async of the E4M3 scale words, which
-//              it scatters straight into the layout tcgen05.cp expects;
-//              multi-stage ring of shared-memory buffers with mbarriers.
-//   warp 1     MMA issuer (one thread): per stage, tcgen05.cp of the scale
-//              factors into tensor memory, then four 128x128x64
-//              kind::mxf4nvf4 block-scaled MMAs into a TMEM accumulator.
-//              Two accumulators alternate over the N tiles, so the epilogue
-//              of one tile overlaps the main loop of the next.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = row),
-//              scale by gsa*gsb, activation + bias, and either a register
-//              top-k per thread (k <= 32), or scores kept in shared memory for
-//              a few rows followed by a warp-level radix select + bitonic sort
-//              (k > 32, e.g. the indexer's top-512).
+//              128-byte swizzle) and of the E4M3 scale tiles (row-major
+//              boxes, K % 256 == 0) or cp.async of the scale words scattered
+//              straight into MMA layout (other K); multi-stage mbarrier ring.
+//   warp 1     MMA issuer (one thread): tcgen05.cp of the scale factors into
+//              tensor memory, then four 128 x BN x 64 kind::mxf4nvf4
+//              block-scaled MMAs per stage into one TMEM accumulator.
+//   warps 2-5  during the main loop: rearrange each stage's scale tiles into
+//              the layout tcgen05.cp 32x128b.warpx4 reads (one 128-row atom
+//              per warp); afterwards: tcgen05.ld the accumulator and store the
+//              FP32 tile to this CTA's shared memory (column-major, odd row
+//              stride so later row reads hit distinct banks).
+// Then a cluster barrier, and every CTA takes its share of the tile's rows:
+// one warp per row gathers the row's N partial sums from the cluster's
+// shared memories (summing the K slices in a fixed order), applies gsa*gsb,
+// the activation and the bias, and selects the top k: k rounds of a warp
+// arg-max for k <= 32 and N <= 256, else a radix select + bitonic sort on
+// keys kept in shared memory (the indexer's top-512).  A second cluster
+// barrier keeps every tile alive until all readers are done.
 //
-// The design of the pages' WIP fused router kernel (TMA warp, MMA warp, four
-// epilogue warps with per-thread heaps) is prior art; the tile sizes, the
-// scale-factor path and the selection scheme here are this library's own.
+// The pages' WIP fused router kernel (TMA warp, MMA warp, four epilogue warps
+// with per-thread heaps) is prior art; the split, the scale-factor path and
+// the selection scheme here are this library's own.
 //
 // Every wait on an mbarrier is bounded: after ~1 s of SM clock it records
-// NVFP4_DEVICE_TIMEOUT in the workspace, tells the other warps to stop, lets
-// the copies already issued land, frees tensor memory and returns.
+// NVFP4_DEVICE_TIMEOUT in the workspace, tells the CTA's other warps to stop,
+// lets the copies already issued land, frees tensor memory and returns.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -52,24 +64,38 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128;                  // MMA M: rows of A per tile
-constexpr int BN = 128;                  // MMA N: rows of B (output columns) per tile
-constexpr int BKB = 128;                 // bytes of a K tile per row = 256 FP4 elements
-constexpr int kThreads = 192;            // 6 warps
-constexpr uint32_t kABytes = BM * BKB;   // 16 KB
-constexpr uint32_t kBBytes = BN * BKB;   // 16 KB
-constexpr uint32_t kSfChunk = 512;       // scales of 128 rows for one MMA (K = 64)
-constexpr uint32_t kSfBytes = 4 * kSfChunk;
-constexpr uint32_t kStageBytes = kABytes + kBBytes + 2 * kSfBytes;  // 36 KB, 1 KB multiple
+constexpr int BM = 128;              // MMA M: rows of A per tile
+constexpr int BKB = 128;             // bytes of a K tile per row = 256 FP4 elements
+constexpr int kThreads = 192;        // 6 warps
+constexpr int kWarps = 6;
 constexpr int kMaxStages = 4;
+constexpr int kMaxCluster = 16;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;                  // FP32 accumulator: one column per n
-constexpr uint32_t kSfTmemBase = 2 * kAccCols;     // after the two accumulators
-constexpr uint32_t kSfTmemPerStage = 32;           // 16 columns SFA + 16 columns SFB
+constexpr uint32_t kSfTmemBase = 256;  // scale factors live after the (<= 256-column) accumulator
+constexpr uint32_t kSfChunk = 512;     // scales of 128 rows for one MMA (K = 64)
 constexpr uint32_t kCtrlBytes = 256;
-constexpr long long kWaitLimit = 2000000000LL;     // SM cycles (~1 s)
+constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
+constexpr int kSmallCols = 8;        // small row path: <= 8 columns per lane (N <= 256)
 
-static_assert(kSfTmemBase + kMaxStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
+template <int BN>
+struct Layout {
+  static constexpr int kAtomsB = BN / 128;
+  static constexpr uint32_t kA = BM * BKB;
+  static constexpr uint32_t kB = BN * BKB;
+  static constexpr uint32_t kSfaStage = BM * 16;  // TMA box of scale bytes, row-major
+  static constexpr uint32_t kSfbStage = BN * 16;
+  static constexpr uint32_t kSfaMma = 4 * kSfChunk;
+  static constexpr uint32_t kSfbMma = 4 * kAtomsB * kSfChunk;
+  static constexpr uint32_t offB = kA;
+  static constexpr uint32_t offSfaStage = kA + kB;
+  static constexpr uint32_t offSfbStage = offSfaStage + kSfaStage;
+  static constexpr uint32_t offSfaMma = offSfbStage + kSfbStage;
+  static constexpr uint32_t offSfbMma = offSfaMma + kSfaMma;
+  static constexpr uint32_t kStage = offSfbMma + kSfbMma;  // 40 KB (BN 128) / 60 KB (BN 256)
+  static constexpr uint32_t kSfTmemPerStage = 16 + 16 * kAtomsB;
+  static_assert(kStage % 1024 == 0, "stages must keep 1 KB alignment for the 128-byte swizzle");
+  static_assert(kSfTmemBase + kMaxStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
+};
 
 struct Params {
   const uint8_t* sfa;
@@ -86,10 +112,14 @@ struct Params {
   int k;
   int epilogue;
   int num_k_tiles;
-  int num_n_tiles;
+  int n_split, k_split;
   int stages;
-  int rows_per_cta;  // select mode: rows whose scores this CTA keeps
-  int cand_cap;      // select mode: power of two >= k
+  int tma_sf;             // scale tiles by TMA (needs K % 256 == 0)
+  uint32_t region_bytes;  // pipeline ring / accumulator tile region (1 KB multiple)
+  int large;              // row phase through shared-memory keys (k > 32 or N > 256)
+  int sel_warps;          // warps that own a key buffer in the large path
+  int cand_cap;           // large path: power of two >= k
+  uint32_t row_bytes;     // large path: bytes of one warp's key buffer (16-byte multiple)
 };
 
 // Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1), E4M3
@@ -106,9 +136,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
 }
 
-__device__ __forceinline__ void record_timeout(const Params& p, volatile uint32_t* abort) {
+__device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort) {
   *abort = 1u;
-  atomicOr(p.status, NVFP4_DEVICE_TIMEOUT);
+  atomicOr(status, NVFP4_DEVICE_TIMEOUT);
 }
 
 // Order-preserving map of a float to an unsigned key (larger float, larger key).
@@ -119,80 +149,139 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
-
-__device__ __forceinline__ void score_of(float logit, int epilogue, const float* bias, int n,
-                                         float& score, float& weight) {
-  if (epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
-    const float sp = logit > 20.0f ? logit : log1pf(expf(logit));
-    weight = sqrtf(sp);
-    score = weight + __ldg(bias + n);
-  } else {
-    weight = logit;
-    score = logit;
-  }
+// (score key, column) packed so that a larger value is a better entry:
+// higher score first, then lower column.
+__device__ __forceinline__ uint64_t entry(float s, int n) {
+  return (static_cast<uint64_t>(float_key(s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
+}
+__device__ __forceinline__ int entry_col(uint64_t e) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
 
-// Sorted (descending) insertion into a KMAX-entry register list; equal
-// scores keep the earlier (lower) column ahead.
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float (&tw)[KMAX],
-                                            float s, int n, float w) {
+// sqrt(softplus(z)) with softplus(z) = max(z, 0) + log1p(exp(-|z|)).  For
+// u = exp(-|z|) < 2^-5 log1p(u) is taken from the first three terms of its
+// Mercator series u - u^2/2 + u^3/3 (truncation below u^4/4, relative 8e-6);
+// otherwise from the fast log of 1 + u.  Relative error ~1e-5, far inside the
+// 1e-3 the scores are held to.
+__device__ __forceinline__ float router_weight(float z) {
+  const float u = __expf(-fabsf(z));
+  const float l = (u < 0.03125f) ? u * (1.0f - u * (0.5f - u * 0.333333343f)) : __logf(1.0f + u);
+  return sqrtf(fmaxf(z, 0.0f) + l);
+}
+
+struct RowCtx {
+  uint32_t dump_addr;  // shared address of this CTA's accumulator tile
+  int dr;              // tile row stride (floats)
+  int n_split, k_split, bn;
+  float gab;
+};
+
+// Logit of (tile row r, column n): the K slices' partial sums in rank order.
+__device__ __forceinline__ float gather_logit(const RowCtx& c, int r, int n) {
+  const int nidx = n / c.bn;
+  const uint32_t off = static_cast<uint32_t>(((n - nidx * c.bn) * c.dr + r) * 4);
+  float acc = 0.0f;
+  for (int ks = 0; ks < c.k_split; ++ks)
+    acc += ld_cluster_f32(mapa_shared(c.dump_addr, static_cast<uint32_t>(ks * c.n_split + nidx)) + off);
+  return acc * c.gab;
+}
+
+__device__ __forceinline__ float score_of(const Params& p, float z, int n) {
+  return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) + __ldg(p.bias + n) : z;
+}
+__device__ __forceinline__ float weight_of(const Params& p, float z) {
+  return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) : z;
+}
+
+// k <= 32, N <= 256: each lane holds up to 8 columns (lane + 32 i) in
+// registers; k rounds of a warp arg-max over (score, -column).
+__device__ void row_small(const Params& p, const RowCtx& c, int r, int64_t grow) {
+  const uint32_t lane = lane_id();
+  uint64_t e[kSmallCols];
+  float zv[kSmallCols];
 #pragma unroll
-  for (int i = KMAX - 1; i > 0; --i) {
-    if (s > tv[i - 1]) {
-      tv[i] = tv[i - 1];
-      ti[i] = ti[i - 1];
-      tw[i] = tw[i - 1];
-    } else if (s > tv[i]) {
-      tv[i] = s;
-      ti[i] = n;
-      tw[i] = w;
+  for (int i = 0; i < kSmallCols; ++i) {
+    const int n = static_cast<int>(lane) + 32 * i;
+    e[i] = 0ull;
+    zv[i] = 0.0f;
+    if (n < p.N) {
+      const float z = gather_logit(c, r, n);
+      if (p.logits != nullptr) p.logits[grow * p.N + n] = z;
+      zv[i] = z;
+      e[i] = entry(score_of(p, z, n), n);
     }
   }
-  if (s > tv[0]) {
-    tv[0] = s;
-    ti[0] = n;
-    tw[0] = w;
+  const int want = p.k < p.N ? p.k : p.N;
+  uint64_t mine = 0ull;
+  float mine_z = 0.0f;
+  for (int t = 0; t < want; ++t) {
+    uint64_t best = e[0];
+#pragma unroll
+    for (int i = 1; i < kSmallCols; ++i) best = e[i] > best ? e[i] : best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      best = other > best ? other : best;
+    }
+    float zb = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kSmallCols; ++i) {
+      if (e[i] == best) {
+        zb = zv[i];
+        e[i] = 0ull;
+      }
+    }
+    zb = __shfl_sync(0xFFFFFFFFu, zb, entry_col(best) & 31);
+    if (static_cast<int>(lane) == t) {
+      mine = best;
+      mine_z = zb;
+    }
+  }
+  if (static_cast<int>(lane) < p.k) {
+    const int64_t o = grow * p.k + lane;
+    if (static_cast<int>(lane) < want) {
+      p.topk_idx[o] = entry_col(mine);
+      p.topk_score[o] = key_float(static_cast<uint32_t>(mine >> 32));
+      if (p.topk_weight) p.topk_weight[o] = weight_of(p, mine_z);
+    } else {
+      p.topk_idx[o] = -1;
+      p.topk_score[o] = -__int_as_float(0x7F800000);
+      if (p.topk_weight) p.topk_weight[o] = 0.0f;
+    }
   }
 }
 
-template <int KMAX>
-__device__ __forceinline__ float kth_value(const float (&tv)[KMAX], int k) {
-  float t = tv[0];
-#pragma unroll
-  for (int i = 1; i < KMAX; ++i)
-    if (i == k - 1) t = tv[i];
-  return t;
-}
-
-// Warp-level top-k of n scores held in shared memory (overwritten by their
-// keys): 4-pass radix select of the k-th largest key, in-order compaction
-// (keys above it, then the lowest-index ties), bitonic sort of the picks.
-__device__ void select_row_topk(float* row_scores, int n, int k, uint32_t* hist, uint64_t* cand,
-                                int cand_cap, const Params& p, int64_t row) {
+// General row: keys of all N scores in shared memory, 4-pass radix select
+// of the k-th largest key, in-order compaction (keys above it, then the
+// lowest-column ties), bitonic sort of the picks, outputs.
+__device__ void row_large(const Params& p, const RowCtx& c, int r, int64_t grow, uint32_t* keys,
+                          uint32_t* hist, uint64_t* cand) {
   const uint32_t lane = lane_id();
-  uint32_t* keys = reinterpret_cast<uint32_t*>(row_scores);
-  for (int i = lane; i < n; i += 32) keys[i] = float_key(row_scores[i]);
+  const int n_all = p.N;
+  for (int n = lane; n < n_all; n += 32) {
+    const float z = gather_logit(c, r, n);
+    if (p.logits != nullptr) p.logits[grow * n_all + n] = z;
+    keys[n] = float_key(score_of(p, z, n));
+  }
   __syncwarp();
-  const int want = k < n ? k : n;
+  const int want = p.k < n_all ? p.k : n_all;
   uint32_t prefix = 0, pmask = 0;
   int remaining = want;
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
-    for (int i = lane; i < n; i += 32) {
+    for (int i = lane; i < n_all; i += 32) {
       const uint32_t u = keys[i];
       if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
     }
     __syncwarp();
-    // lane l owns digits 255-8l down to 248-8l
-    uint32_t c[8];
+    uint32_t cnt[8];
     uint32_t local = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      c[j] = hist[255 - 8 * lane - j];
-      local += c[j];
+    for (int j = 0; j < 8; ++j) {  // lane l owns digits 255-8l down to 248-8l
+      cnt[j] = hist[255 - 8 * lane - j];
+      local += cnt[j];
     }
     uint32_t incl = local;
 #pragma unroll
@@ -201,23 +290,23 @@ __device__ void select_row_topk(float* row_scores, int n, int k, uint32_t* hist,
       if (lane >= static_cast<uint32_t>(o)) incl += t;
     }
     const uint32_t excl = incl - local;
-    const bool mine = excl < static_cast<uint32_t>(remaining) && incl >= static_cast<uint32_t>(remaining);
+    const bool owner = excl < static_cast<uint32_t>(remaining) && incl >= static_cast<uint32_t>(remaining);
     uint32_t digit = 0, above = 0;
-    if (mine) {
+    if (owner) {
       uint32_t acc = excl;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
+        if (acc + cnt[j] >= static_cast<uint32_t>(remaining)) {
           digit = 255 - 8 * lane - j;
           above = acc;
           break;
         }
-        acc += c[j];
+        acc += cnt[j];
       }
     }
-    const uint32_t owner = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
-    digit = __shfl_sync(0xFFFFFFFFu, digit, owner);
-    above = __shfl_sync(0xFFFFFFFFu, above, owner);
+    const uint32_t src = __ffs(__ballot_sync(0xFFFFFFFFu, owner)) - 1;
+    digit = __shfl_sync(0xFFFFFFFFu, digit, src);
+    above = __shfl_sync(0xFFFFFFFFu, above, src);
     remaining -= static_cast<int>(above);
     prefix |= digit << shift;
     pmask |= 255u << shift;
@@ -227,27 +316,26 @@ __device__ void select_row_topk(float* row_scores, int n, int k, uint32_t* hist,
   const int need_eq = remaining;
   int out = 0, eq_seen = 0;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < n; base += 32) {
+  for (int base = 0; base < n_all; base += 32) {
     const int i = base + static_cast<int>(lane);
-    const uint32_t u = i < n ? keys[i] : 0u;
-    const bool gt = i < n && u > kth;
-    const bool eq = i < n && u == kth;
+    const uint32_t u = i < n_all ? keys[i] : 0u;
+    const bool gt = i < n_all && u > kth;
+    const bool eq = i < n_all && u == kth;
     const uint32_t beq = __ballot_sync(0xFFFFFFFFu, eq);
     const int eq_rank = eq_seen + __popc(beq & lt_mask);
     const bool take = gt || (eq && eq_rank < need_eq);
     const uint32_t btake = __ballot_sync(0xFFFFFFFFu, take);
     if (take)
       cand[out + __popc(btake & lt_mask)] =
-          (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(i));
+          (static_cast<uint64_t>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
     out += __popc(btake);
     eq_seen += __popc(beq);
   }
-  for (int i = out + static_cast<int>(lane); i < cand_cap; i += 32) cand[i] = 0ull;
+  for (int i = out + static_cast<int>(lane); i < p.cand_cap; i += 32) cand[i] = 0ull;
   __syncwarp();
-  // Bitonic sort, descending on (key, -index).
-  for (int size = 2; size <= cand_cap; size <<= 1) {
+  for (int size = 2; size <= p.cand_cap; size <<= 1) {  // bitonic sort, descending
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = lane; t < cand_cap / 2; t += 32) {
+      for (int t = lane; t < p.cand_cap / 2; t += 32) {
         const int lo = 2 * stride * (t / stride) + (t % stride);
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
@@ -260,68 +348,70 @@ __device__ void select_row_topk(float* row_scores, int n, int k, uint32_t* hist,
       __syncwarp();
     }
   }
-  for (int t = lane; t < k; t += 32) {
-    int32_t idx = -1;
-    float s = -__int_as_float(0x7F800000);
-    float w = 0.0f;
+  for (int t = lane; t < p.k; t += 32) {
+    const int64_t o = grow * p.k + t;
     if (t < out) {
       const uint64_t v = cand[t];
-      idx = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(v & 0xFFFFFFFFu));
-      s = key_float(static_cast<uint32_t>(v >> 32));
-      w = (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) ? s - __ldg(p.bias + idx) : s;
+      const int n = entry_col(v);
+      p.topk_idx[o] = n;
+      p.topk_score[o] = key_float(static_cast<uint32_t>(v >> 32));
+      if (p.topk_weight) p.topk_weight[o] = weight_of(p, gather_logit(c, r, n));
+    } else {
+      p.topk_idx[o] = -1;
+      p.topk_score[o] = -__int_as_float(0x7F800000);
+      if (p.topk_weight) p.topk_weight[o] = 0.0f;
     }
-    p.topk_idx[row * p.k + t] = idx;
-    p.topk_score[row * p.k + t] = s;
-    if (p.topk_weight) p.topk_weight[row * p.k + t] = w;
   }
   __syncwarp();
 }
 
-// Shared-memory bytes of the per-row score buffers in select mode (16-byte rounded).
-__host__ __device__ inline size_t select_scores_bytes(int rows, int n) {
-  return (static_cast<size_t>(rows) * n * 4 + 15) & ~static_cast<size_t>(15);
-}
-
-template <int KMAX, bool SELECT>
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_topk_kernel(const __grid_constant__ CUtensorMap tma_a,
-                     const __grid_constant__ CUtensorMap tma_b, const Params p) {
+                     const __grid_constant__ CUtensorMap tma_b,
+                     const __grid_constant__ CUtensorMap tma_sfa,
+                     const __grid_constant__ CUtensorMap tma_sfb, const __grid_constant__ Params p) {
+  using L = Layout<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const int S = p.stages;
-  uint8_t* ctrl = smem + S * kStageBytes;
+  uint8_t* ctrl = smem + p.region_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
-  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 132);
   auto full_bar = [&](int s) { return smem_addr(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_addr(&bars[kMaxStages + s]); };
-  auto tfull_bar = [&](int b) { return smem_addr(&bars[2 * kMaxStages + b]); };
-  auto tempty_bar = [&](int b) { return smem_addr(&bars[2 * kMaxStages + 2 + b]); };
-  const uint32_t drain_bar = smem_addr(&bars[2 * kMaxStages + 4]);
+  auto sfready_bar = [&](int s) { return smem_addr(&bars[2 * kMaxStages + s]); };
+  const uint32_t tfull_bar = smem_addr(&bars[3 * kMaxStages]);
+  const uint32_t drain_bar = smem_addr(&bars[3 * kMaxStages + 1]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
+  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 132);
+  uint8_t* rowmem = ctrl + kCtrlBytes;
 
-  int m0, row_lo, row_hi;
-  if (SELECT) {
-    row_lo = blockIdx.x * p.rows_per_cta;
-    row_hi = min(row_lo + p.rows_per_cta, p.M);
-    m0 = (row_lo / BM) * BM;
-  } else {
-    m0 = blockIdx.x * BM;
-    row_lo = m0;
-    row_hi = min(m0 + BM, p.M);
-  }
+  const int csize = p.n_split * p.k_split;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int mt = blockIdx.x / csize;
+  const int n_idx = rank % p.n_split;
+  const int k_idx = rank / p.n_split;
+  const int m0 = mt * BM;
+  const int n0 = n_idx * BN;
+  const int vr = min(BM, p.M - m0);  // valid rows of this tile
+  const int kt0 = k_idx * p.num_k_tiles / p.k_split;
+  const int nk = (k_idx + 1) * p.num_k_tiles / p.k_split - kt0;
+  const int ncols = min(BN, p.N - n0);
+  const int mma_n = min(BN, (ncols + 15) & ~15);
+  const int dr = vr | 1;
+  constexpr int kUnits = 1 + L::kAtomsB;  // scale atoms per stage: SFA + SFB's
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1 + 32);  // expect_tx arrival + one cp.async arrival per lane
+      mbar_init(full_bar(s), p.tma_sf ? 1 : 1 + 32);  // + one cp.async arrival per producer lane
       mbar_init(empty_bar(s), 1);
+      mbar_init(sfready_bar(s), kUnits);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
-    }
+    mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
     *abort = 0u;
     fence_mbar_init();
@@ -333,6 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tma_a);
     prefetch_tensormap(&tma_b);
+    if (p.tma_sf) {
+      prefetch_tensormap(&tma_sfa);
+      prefetch_tensormap(&tma_sfb);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -341,201 +435,186 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const int kk = lane & 3;        // which MMA (K = 64) of the tile this lane's scale words feed
-    const int rsub = lane >> 2;     // row offset 0..7 within each group of 8 rows
-    const int kwords = p.K / 64;    // 4-byte scale words per row
-    const int sf_ld = p.K / 16;     // scale bytes per row
-    int issued_phase[kMaxStages];
-    bool issued[kMaxStages];
-    for (int s = 0; s < kMaxStages; ++s) issued[s] = false, issued_phase[s] = 0;
-    int it = 0;
-    bool ok = true;
-    for (int nt = 0; nt < p.num_n_tiles && ok; ++nt) {
-      const int n0 = nt * BN;
-      for (int kt = 0; kt < p.num_k_tiles; ++kt, ++it) {
-        const int s = it % S;
-        const uint32_t ph = (it / S) & 1;
-        if (!warp_wait(empty_bar(s), ph ^ 1u, abort)) {
-          if (lane == 0) record_timeout(p, abort);
-          ok = false;
-          break;
+    const int kwords = p.K / 64;
+    const int sf_ld = p.K / 16;
+    const int kk = lane & 3;
+    const int rsub = lane >> 2;
+    const uint32_t tx = L::kA + L::kB + (p.tma_sf ? L::kSfaStage + L::kSfbStage : 0u);
+    int last = -1;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S;
+      const uint32_t ph = (i / S) & 1;
+      if (!warp_wait(empty_bar(s), ph ^ 1u, abort)) {
+        if (lane == 0) record_timeout(p.status, abort);
+        break;
+      }
+      const uint32_t st = sbase + s * L::kStage;
+      const int kt = kt0 + i;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full_bar(s), tx);
+        tma_load_2d(st, &tma_a, full_bar(s), kt * BKB, m0);
+        tma_load_2d(st + L::offB, &tma_b, full_bar(s), kt * BKB, n0);
+        if (p.tma_sf) {
+          tma_load_2d(st + L::offSfaStage, &tma_sfa, full_bar(s), kt * 16, m0);
+          tma_load_2d(st + L::offSfbStage, &tma_sfb, full_bar(s), kt * 16, n0);
         }
-        uint8_t* st = smem + s * kStageBytes;
-        const uint32_t a_dst = smem_addr(st);
-        const uint32_t b_dst = a_dst + kABytes;
-        const uint32_t sfa_dst = b_dst + kBBytes + kk * kSfChunk;
-        const uint32_t sfb_dst = sfa_dst + kSfBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full_bar(s), kABytes + kBBytes);
-          tma_load_2d(a_dst, &tma_a, full_bar(s), kt * BKB, m0);
-          tma_load_2d(b_dst, &tma_b, full_bar(s), kt * BKB, n0);
-        }
+      }
+      if (!p.tma_sf) {
         // Scale word (row r, MMA kk) goes to byte (r % 32) * 16 + (r / 32) * 4
-        // of chunk kk: the 32 x 128-bit matrix that tcgen05.cp 32x128b.warpx4
-        // turns into the per-row scale columns of one MMA.
+        // of the row's 128-row atom in chunk kk.
         const int kw = kt * 4 + kk;
         const bool kvalid = kw < kwords;
-#pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < BM / 8; ++j) {
           const int r = rsub + 8 * j;
-          const uint32_t off = (r & 31) * 16 + (r >> 5) * 4;
           const int ra = m0 + r;
           const bool va = kvalid && ra < p.M;
-          cp_async_4(sfa_dst + off, va ? p.sfa + static_cast<int64_t>(ra) * sf_ld + kw * 4 : p.sfa,
-                     va ? 4u : 0u);
+          cp_async_4(st + L::offSfaMma + kk * kSfChunk + (r & 31) * 16 + (r >> 5) * 4,
+                     va ? p.sfa + static_cast<int64_t>(ra) * sf_ld + kw * 4 : p.sfa, va ? 4u : 0u);
+        }
+        for (int j = 0; j < BN / 8; ++j) {
+          const int r = rsub + 8 * j;
+          const int rr = r & 127;
           const int rb = n0 + r;
           const bool vb = kvalid && rb < p.N;
-          cp_async_4(sfb_dst + off, vb ? p.sfb + static_cast<int64_t>(rb) * sf_ld + kw * 4 : p.sfb,
-                     vb ? 4u : 0u);
+          cp_async_4(st + L::offSfbMma + kk * (L::kAtomsB * kSfChunk) + (r >> 7) * kSfChunk +
+                         (rr & 31) * 16 + (rr >> 5) * 4,
+                     vb ? p.sfb + static_cast<int64_t>(rb) * sf_ld + kw * 4 : p.sfb, vb ? 4u : 0u);
         }
         cp_async_arrive_noinc(full_bar(s));
-        issued[s] = true;
-        issued_phase[s] = ph;
       }
+      last = i;
     }
-    // Let every copy this warp issued land before the CTA can exit.
-    if (lane == 0) {
+    if (lane == 0) {  // let every copy issued here land before the CTA can exit
       uint32_t never = 0;
-      for (int s = 0; s < S; ++s)
-        if (issued[s] && !mbar_wait_bounded(full_bar(s), issued_phase[s], &never, kWaitLimit))
-          record_timeout(p, abort);
+      for (int s = 0; s < S; ++s) {
+        const int i_s = last - (((last - s) % S) + S) % S;
+        if (last >= 0 && i_s >= 0 &&
+            !mbar_wait_bounded(full_bar(s), (i_s / S) & 1, &never, kWaitLimit))
+          record_timeout(p.status, abort);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = make_idesc(BM, BN);
-    int it = 0;
+    const uint32_t idesc = make_idesc(BM, mma_n);
     bool ok = true;
-    for (int nt = 0; nt < p.num_n_tiles && ok; ++nt) {
-      const int buf = nt & 1;
-      const uint32_t acc = tmem + buf * kAccCols;
-      if (nt >= 2 && !warp_wait(tempty_bar(buf), ((nt >> 1) + 1) & 1u, abort)) {
-        if (lane == 0) record_timeout(p, abort);
-        break;
-      }
-      tc_fence_after();
-      for (int kt = 0; kt < p.num_k_tiles; ++kt, ++it) {
-        const int s = it % S;
-        const uint32_t ph = (it / S) & 1;
-        if (!warp_wait(full_bar(s), ph, abort)) {
-          if (lane == 0) record_timeout(p, abort);
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          fence_proxy_async_smem();  // scale words arrived through cp.async (generic proxy)
-          tc_fence_after();
-          const uint32_t a_addr = smem_addr(smem + s * kStageBytes);
-          const uint32_t b_addr = a_addr + kABytes;
-          const uint32_t sfa_addr = b_addr + kBBytes;
-          const uint32_t sfb_addr = sfa_addr + kSfBytes;
-          const uint32_t sf_col = tmem + kSfTmemBase + s * kSfTmemPerStage;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(sfa_addr + kk * kSfChunk, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4, smem_desc(sfb_addr + kk * kSfChunk, 0, 128, 0));
-          }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_addr + kk * 32, 16, 1024, 2);
-            tc_mma_nvf4(acc, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
-                        (kt | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(tfull_bar(buf));
-      __syncwarp();
-    }
-    if (lane == 0) {
-      uint32_t never = 0;
-      tc_commit(drain_bar);
-      if (!mbar_wait_bounded(drain_bar, 0, &never, kWaitLimit)) record_timeout(p, abort);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    const int row = m0 + quarter * 32 + static_cast<int>(lane);
-    const float gab = __ldg(p.gsa) * __ldg(p.gsb);
-    float* scores = reinterpret_cast<float*>(ctrl + kCtrlBytes);
-    const bool keep = SELECT ? (row >= row_lo && row < row_hi) : (row < p.M);
-    float tv[KMAX];
-    int ti[KMAX];
-    float tw[KMAX];
-#pragma unroll
-    for (int i = 0; i < KMAX; ++i) {
-      tv[i] = -__int_as_float(0x7F800000);
-      ti[i] = -1;
-      tw[i] = 0.0f;
-    }
-    float thr = tv[0];
-    bool ok = true;
-    for (int nt = 0; nt < p.num_n_tiles; ++nt) {
-      const int buf = nt & 1;
-      if (!warp_wait(tfull_bar(buf), (nt >> 1) & 1u, abort)) {
-        if (lane == 0) record_timeout(p, abort);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S;
+      const uint32_t ph = (i / S) & 1;
+      if (!warp_wait(full_bar(s), ph, abort) || !warp_wait(sfready_bar(s), ph, abort)) {
+        if (lane == 0) record_timeout(p.status, abort);
         ok = false;
         break;
       }
-      tc_fence_after();
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + buf * kAccCols + c * 32 + (static_cast<uint32_t>(quarter * 32) << 16), r);
-        tmem_wait_ld();
-        const int nbase = nt * BN + c * 32;
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t st = sbase + s * L::kStage;
+        const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int n = nbase + j;
-          if (n < p.N) {
-            const float logit = __uint_as_float(r[j]) * gab;
-            if (p.logits != nullptr && keep) p.logits[static_cast<int64_t>(row) * p.N + n] = logit;
-            float s, w;
-            score_of(logit, p.epilogue, p.bias, n, s, w);
-            if (SELECT) {
-              if (keep) scores[(row - row_lo) * p.N + n] = s;
-            } else if (s > thr) {
-              topk_insert<KMAX>(tv, ti, tw, s, n, w);
-              thr = kth_value<KMAX>(tv, p.k);
-            }
-          }
+        for (int kk = 0; kk < 4; ++kk) {
+          tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(st + L::offSfaMma + kk * kSfChunk, 0, 128, 0));
+#pragma unroll
+          for (int a = 0; a < L::kAtomsB; ++a)
+            tc_cp_32x128b_warpx4(
+                sf_col + 16 + kk * 4 * L::kAtomsB + a * 4,
+                smem_desc(st + L::offSfbMma + (kk * L::kAtomsB + a) * kSfChunk, 0, 128, 0));
         }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          tc_mma_nvf4(tmem, smem_desc(st + kk * 32, 16, 1024, 2),
+                      smem_desc(st + L::offB + kk * 32, 16, 1024, 2), idesc, sf_col + kk * 4,
+                      sf_col + 16 + kk * 4 * L::kAtomsB, (i | kk) != 0 ? 1u : 0u);
+        }
+        tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
       }
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
     }
-    if (!SELECT) {
-      if (ok && keep) {
-        const int64_t o = static_cast<int64_t>(row) * p.k;
+    if (lane == 0) {
+      if (ok) tc_commit(tfull_bar);
+      uint32_t never = 0;
+      tc_commit(drain_bar);
+      if (!mbar_wait_bounded(drain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ scale layout, then the tile dump
+    const int unit = warp - 2;
+    if (unit < kUnits) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
+        if (!warp_wait(full_bar(s), ph, abort)) {
+          if (lane == 0) record_timeout(p.status, abort);
+          break;
+        }
+        if (p.tma_sf) {
+          // Staged rows r0 + 32 r1 (r1 = 0..3) of one 128-row atom, 16 bytes
+          // (4 MMA words) each -> chunk kk gets the 16 bytes
+          // {word kk of rows r0, r0+32, r0+64, r0+96} at offset 16 * r0.
+          const uint32_t st = sbase + s * L::kStage;
+          const uint32_t src = unit == 0 ? st + L::offSfaStage : st + L::offSfbStage + (unit - 1) * 2048;
+          const uint32_t dst = unit == 0 ? st + L::offSfaMma : st + L::offSfbMma + (unit - 1) * kSfChunk;
+          const uint32_t chunk = unit == 0 ? kSfChunk : L::kAtomsB * kSfChunk;
+          uint32_t w0[4], w1[4], w2[4], w3[4];
+          ld_shared_v4(src + (0 * 32 + lane) * 16, w0);
+          ld_shared_v4(src + (1 * 32 + lane) * 16, w1);
+          ld_shared_v4(src + (2 * 32 + lane) * 16, w2);
+          ld_shared_v4(src + (3 * 32 + lane) * 16, w3);
 #pragma unroll
-        for (int i = 0; i < KMAX; ++i) {
-          if (i < p.k) {
-            p.topk_idx[o + i] = ti[i];
-            p.topk_score[o + i] = tv[i];
-            if (p.topk_weight) p.topk_weight[o + i] = tw[i];
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            st_shared_v4(dst + kk * chunk + lane * 16, w0[kk], w1[kk], w2[kk], w3[kk]);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfready_bar(s));
+      }
+    }
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + static_cast<int>(lane);
+    if (!warp_wait(tfull_bar, 0, abort)) {
+      if (lane == 0) record_timeout(p.status, abort);
+    } else {
+      tc_fence_after();
+      float* tile = reinterpret_cast<float*>(smem);
+      for (int c0 = 0; c0 < mma_n; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+        tmem_wait_ld();
+        if (row < vr) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < ncols) tile[(c0 + j) * dr + row] = __uint_as_float(v[j]);
         }
       }
-    } else {
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
-      if (ok && !*abort) {
-        const int ew = warp - 2;
-        uint8_t* sel = ctrl + kCtrlBytes + select_scores_bytes(p.rows_per_cta, p.N);
-        uint32_t* hist = reinterpret_cast<uint32_t*>(sel) + ew * 256;
-        uint64_t* cand = reinterpret_cast<uint64_t*>(sel + 4 * 256 * 4) + static_cast<size_t>(ew) * p.cand_cap;
-        for (int rr = ew; rr < row_hi - row_lo; rr += 4)
-          select_row_topk(scores + static_cast<size_t>(rr) * p.N, p.N, p.k, hist, cand, p.cand_cap, p,
-                          row_lo + rr);
-      }
     }
+    tc_fence_before();
   }
 
-  tc_fence_before();
-  __syncthreads();
+  // ------------------------------------------------------------ row phase
+  cluster_sync();
+  {
+    RowCtx c;
+    c.dump_addr = sbase;
+    c.dr = dr;
+    c.n_split = p.n_split;
+    c.k_split = p.k_split;
+    c.bn = BN;
+    c.gab = __ldg(p.gsa) * __ldg(p.gsb);
+    const int r_begin = rank * vr / csize;
+    const int r_end = (rank + 1) * vr / csize;
+    if (!p.large) {
+      for (int r = r_begin + warp; r < r_end; r += kWarps) row_small(p, c, r, m0 + r);
+    } else if (warp < p.sel_warps) {
+      uint8_t* mine = rowmem + warp * (p.row_bytes + 1024 + p.cand_cap * 8);
+      uint32_t* keys = reinterpret_cast<uint32_t*>(mine);
+      uint32_t* hist = reinterpret_cast<uint32_t*>(mine + p.row_bytes);
+      uint64_t* cand = reinterpret_cast<uint64_t*>(mine + p.row_bytes + 1024);
+      for (int r = r_begin + warp; r < r_end; r += p.sel_warps) row_large(p, c, r, m0 + r, keys, hist, cand);
+    }
+  }
+  cluster_sync();  // every CTA's tile stays valid until the whole cluster has read it
+
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -558,35 +637,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D map over a [rows, K/2]-byte code matrix, boxes of 128 bytes x box_rows
-// rows with the 128-byte swizzle; reads past the matrix return zeros.
-bool make_code_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, int box_rows) {
+// 2-D byte matrix [rows, width] (row stride = width), boxes of box_w x box_rows,
+// optional 128-byte swizzle; reads past the matrix return zeros.
+bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t width, int box_w,
+              int box_rows, bool swizzle128) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BKB), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(width)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_w), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
-}
-
-template <int KMAX, bool SELECT>
-cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid,
-                           size_t smem, cudaStream_t stream) {
-  auto kern = gemm_topk_kernel<KMAX, SELECT>;
-  static int configured = 0;  // largest dynamic smem size set so far for this variant
-  if (static_cast<int>(smem) > configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = static_cast<int>(smem);
-  }
-  kern<<<grid, kThreads, smem, stream>>>(ma, mb, p);
-  return cudaGetLastError();
 }
 
 int next_pow2(int v) {
@@ -595,14 +660,182 @@ int next_pow2(int v) {
   return p;
 }
 
+struct Plan {
+  int bn;
+  int n_split, k_split;
+  int stages;
+  int large, sel_warps, cand_cap;
+  uint32_t row_bytes;
+  uint32_t region;
+  size_t smem;
+};
+
+// Pick the split and the shared-memory layout of one problem; false if it
+// cannot be laid out.
+bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, int max_cluster,
+               Plan* out) {
+  Plan pl{};
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  const int kt = static_cast<int>((K / 2 + BKB - 1) / BKB);
+  if (N <= 128) {
+    pl.bn = 128;
+  } else if (N <= 256 && m_tiles * 2 >= sms / 2) {
+    pl.bn = 128;  // many row tiles: two 128-column halves give twice the CTAs
+  } else {
+    pl.bn = 256;
+  }
+  pl.n_split = static_cast<int>((N + pl.bn - 1) / pl.bn);
+  if (pl.n_split > max_cluster) return false;
+  pl.k_split = 1;
+  if (m_tiles * pl.n_split < sms / 2) {  // few tiles: spread K over the rest of the cluster
+    const int64_t want = (sms + m_tiles * pl.n_split - 1) / (m_tiles * pl.n_split);
+    int ks = static_cast<int>(want < max_cluster / pl.n_split ? want : max_cluster / pl.n_split);
+    if (ks > kt) ks = kt;
+    pl.k_split = ks < 1 ? 1 : ks;
+  }
+  pl.large = (k > 32 || N > 32 * kSmallCols) ? 1 : 0;
+  pl.cand_cap = pl.large ? next_pow2(k) : 0;
+  pl.row_bytes = pl.large ? static_cast<uint32_t>((N * 4 + 15) & ~15) : 0u;
+  const int nk_max = (kt + pl.k_split - 1) / pl.k_split;
+  const uint32_t sb = pl.bn == 128 ? Layout<128>::kStage : Layout<256>::kStage;
+  const int vr_max = static_cast<int>(M < BM ? M : BM);
+  const uint32_t dump = static_cast<uint32_t>(pl.bn) * static_cast<uint32_t>(vr_max | 1) * 4u;
+  pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
+  pl.sel_warps = pl.large ? kWarps : 0;
+  auto total = [&]() {
+    uint32_t region = pl.stages * sb > dump ? pl.stages * sb : dump;
+    region = (region + 1023u) & ~1023u;
+    pl.region = region;
+    const size_t sel = pl.large ? static_cast<size_t>(pl.sel_warps) *
+                                      (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8)
+                                : 0;
+    return 1024 + static_cast<size_t>(region) + kCtrlBytes + sel;
+  };
+  while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
+  while (total() > static_cast<size_t>(smem_optin) && pl.sel_warps > 1) --pl.sel_warps;
+  pl.smem = total();
+  if (pl.smem > static_cast<size_t>(smem_optin)) return false;
+  *out = pl;
+  return true;
+}
+
+template <int BN>
+cudaLaunchConfig_t launch_config(int grid, int cluster, size_t smem, cudaStream_t stream,
+                                 cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Function attributes the launch needs (idempotent).
+template <int BN>
+cudaError_t configure(size_t smem, int cluster) {
+  auto kern = gemm_topk_kernel<BN>;
+  static std::mutex mu;
+  static int configured = 0;  // largest dynamic smem size set so far for this variant
+  static bool nonportable = false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(smem) > configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = static_cast<int>(smem);
+  }
+  if (cluster > 8 && !nonportable) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    nonportable = true;
+  }
+  return cudaSuccess;
+}
+
+// Whether clusters of this size and shared-memory footprint can be resident
+// at all (answers cached per device and configuration).
+template <int BN>
+bool cluster_fits(int cluster, size_t smem) {
+  if (cluster <= 1) return true;
+  static std::mutex mu;
+  static int cache_dev[64], cache_cluster[64];
+  static size_t cache_smem[64];
+  static bool cache_ok[64];
+  static int n_cache = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache_dev[i] == dev && cache_cluster[i] == cluster && cache_smem[i] == smem) return cache_ok[i];
+  bool ok = false;
+  if (configure<BN>(smem, cluster) == cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config<BN>(cluster, cluster, smem, nullptr, attr);
+    int n = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN>, &cfg) == cudaSuccess && n > 0;
+  }
+  cudaGetLastError();  // a refused query leaves no error behind
+  if (n_cache < 64) {
+    cache_dev[n_cache] = dev;
+    cache_cluster[n_cache] = cluster;
+    cache_smem[n_cache] = smem;
+    cache_ok[n_cache] = ok;
+    ++n_cache;
+  }
+  return ok;
+}
+
+template <int BN>
+cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
+                           const CUtensorMap& msb, const Params& p, int grid, int cluster,
+                           size_t smem, cudaStream_t stream) {
+  const cudaError_t e = configure<BN>(smem, cluster);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config<BN>(grid, cluster, smem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gemm_topk_kernel<BN>, ma, mb, msa, msb, p);
+}
+
 }  // namespace
 
 int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* err) {
   *err = cudaSuccess;
   if (a.M == 0) return NVFP4_OK;
-  CUtensorMap ma, mb;
-  if (!make_code_map(&ma, a.qa, a.M, a.K, BM) || !make_code_map(&mb, a.qb, a.N, a.K, BN))
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int smem_optin = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  // Largest cluster (16, else 8, 4, ...) whose CTAs can be co-resident.
+  Plan pl;
+  int cap = kMaxCluster;
+  for (;;) {
+    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, &pl)) return NVFP4_ERR_UNSUPPORTED;
+    const int c = pl.n_split * pl.k_split;
+    const bool fits = pl.bn == 128 ? cluster_fits<128>(c, pl.smem) : cluster_fits<256>(c, pl.smem);
+    if (fits) break;
+    if (c <= 1 || cap <= 1) return NVFP4_ERR_UNSUPPORTED;
+    cap = c / 2;
+  }
+
+  const bool tma_sf = (a.K % 256) == 0;
+  CUtensorMap ma, mb, msa, msb;
+  if (!make_map(&ma, a.qa, a.M, a.K / 2, BKB, BM, true) ||
+      !make_map(&mb, a.qb, a.N, a.K / 2, BKB, pl.bn, true))
     return NVFP4_ERR_UNSUPPORTED;
+  if (tma_sf) {
+    if (!make_map(&msa, a.sfa, a.M, a.K / 16, 16, BM, false) ||
+        !make_map(&msb, a.sfb, a.N, a.K / 16, 16, pl.bn, false))
+      return NVFP4_ERR_UNSUPPORTED;
+  } else {
+    msa = ma;  // unused
+    msb = mb;
+  }
   Params p;
   std::memset(&p, 0, sizeof(p));
   p.sfa = a.sfa;
@@ -621,41 +854,20 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.k = a.k;
   p.epilogue = a.epilogue;
   p.num_k_tiles = static_cast<int>((a.K / 2 + BKB - 1) / BKB);
-  p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
-
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int smem_optin = 0;
-  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const size_t fixed = 1024 + kCtrlBytes;
-  cudaError_t e = cudaSuccess;
-
-  if (a.k <= 32) {
-    p.stages = kMaxStages;
-    const size_t smem = fixed + p.stages * kStageBytes;
-    const int grid = static_cast<int>((a.M + BM - 1) / BM);
-    if (a.k <= 8)
-      e = launch_variant<8, false>(ma, mb, p, grid, smem, stream);
-    else if (a.k <= 16)
-      e = launch_variant<16, false>(ma, mb, p, grid, smem, stream);
-    else
-      e = launch_variant<32, false>(ma, mb, p, grid, smem, stream);
-  } else {
-    p.cand_cap = next_pow2(a.k);
-    const size_t sel_bytes = 4 * 256 * 4 + 4 * static_cast<size_t>(p.cand_cap) * 8;
-    // Fewer pipeline stages and as many rows as fit, at most 8 per CTA.
-    int stages = 2, rows = 8;
-    auto need = [&](int st, int r) {
-      return fixed + st * kStageBytes + select_scores_bytes(r, static_cast<int>(a.N)) + sel_bytes;
-    };
-    while (rows > 1 && need(stages, rows) > static_cast<size_t>(smem_optin)) rows >>= 1;
-    if (need(stages, rows) > static_cast<size_t>(smem_optin)) return NVFP4_ERR_UNSUPPORTED;
-    while (stages < kMaxStages && need(stages + 1, rows) <= static_cast<size_t>(smem_optin)) ++stages;
-    p.stages = stages;
-    p.rows_per_cta = rows;
-    const int grid = static_cast<int>((a.M + rows - 1) / rows);
-    e = launch_variant<1, true>(ma, mb, p, grid, need(stages, rows), stream);
-  }
+  p.n_split = pl.n_split;
+  p.k_split = pl.k_split;
+  p.stages = pl.stages;
+  p.tma_sf = tma_sf ? 1 : 0;
+  p.region_bytes = pl.region;
+  p.large = pl.large;
+  p.sel_warps = pl.sel_warps;
+  p.cand_cap = pl.cand_cap;
+  p.row_bytes = pl.row_bytes;
+  const int cluster = pl.n_split * pl.k_split;
+  const int grid = static_cast<int>((a.M + BM - 1) / BM) * cluster;
+  const cudaError_t e =
+      pl.bn == 128 ? launch_variant<128>(ma, mb, msa, msb, p, grid, cluster, pl.smem, stream)
+                   : launch_variant<256>(ma, mb, msa, msb, p, grid, cluster, pl.smem, stream);
   if (e != cudaSuccess) {
     *err = e;
     return NVFP4_ERR_CUDA;
