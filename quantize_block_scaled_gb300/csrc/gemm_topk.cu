@@ -19,7 +19,7 @@
 // (a few rows, a 1 MB weight) spreads its weight read over up to 16 SMs and
 // a prefill-sized one gives every SM a tile.
 //
-// Per CTA, 6 warps:
+// Per CTA, 6 warps during the main loop:
 //   warp 0     producer: TMA loads of the A and B code tiles (128-byte rows,
 //              128-byte swizzle) and of the E4M3 scale tiles (row-major
 //              boxes, K % 256 == 0) or cp.async of the scale words scattered
@@ -27,22 +27,27 @@
 //   warp 1     MMA issuer (one thread): tcgen05.cp of the scale factors into
 //              tensor memory, then four 128 x BN x 64 kind::mxf4nvf4
 //              block-scaled MMAs per stage into one TMEM accumulator.
-//   warps 2-5  during the main loop: rearrange each stage's scale tiles into
-//              the layout tcgen05.cp 32x128b.warpx4 reads (one 128-row atom
-//              per warp); afterwards: tcgen05.ld the accumulator and store the
-//              FP32 tile to this CTA's shared memory (column-major, odd row
-//              stride so later row reads hit distinct banks).
-// Then a cluster barrier, and every CTA takes its share of the tile's rows:
-// one warp per row gathers the row's N partial sums from the cluster's
-// shared memories (summing the K slices in a fixed order), applies gsa*gsb,
-// the activation and the bias, and selects the top k: k rounds of a warp
-// arg-max for k <= 32 and N <= 256, else a radix select + bitonic sort on
-// keys kept in shared memory (the indexer's top-512).  A second cluster
-// barrier keeps every tile alive until all readers are done.
+//   warps 2-5  rearrange each stage's scale tiles into the layout
+//              tcgen05.cp 32x128b.warpx4 reads (one 128-row atom per warp).
+//
+// Then one of two epilogues.
+//  Direct (no K split, k <= 32): the thread that owns TMEM lane r owns row
+//    r.  It walks its columns 32 at a time, skips every column whose logit
+//    cannot reach the current k-th best score (a bound on the logit derived
+//    once per threshold change, so most columns cost a multiply and a
+//    compare), scores the rest, and keeps a sorted register list.  With an N
+//    split, each CTA pushes its per-row lists to the row's owner in the
+//    cluster (remote shared-memory stores), which merges them.
+//  Reduce (K split, or k > 32): each CTA pushes its FP32 partial sums to the
+//    owner of each row, laid out [K slice][column][row]; the owner's warps
+//    then take one row each, sum the K slices in a fixed order, score, and
+//    select: a 5-level butterfly of sorted 8-lists for k <= 8, k rounds of
+//    a warp arg-max for k <= 32, and a radix select + bitonic sort on keys in
+//    shared memory otherwise (the indexer's top-512).
 //
 // The pages' WIP fused router kernel (TMA warp, MMA warp, four epilogue warps
-// with per-thread heaps) is prior art; the split, the scale-factor path and
-// the selection scheme here are this library's own.
+// with per-thread heaps) is prior art; the split, the scale-factor path, the
+// threshold filter and the selection schemes here are this library's own.
 //
 // Every wait on an mbarrier is bounded: after ~1 s of SM clock it records
 // NVFP4_DEVICE_TIMEOUT in the workspace, tells the CTA's other warps to stop,
@@ -74,8 +79,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;  // scale factors live after the (<= 256-column) accumulator
 constexpr uint32_t kSfChunk = 512;     // scales of 128 rows for one MMA (K = 64)
 constexpr uint32_t kCtrlBytes = 256;
+constexpr uint32_t kScratchStride = 33;  // direct epilogue: floats per thread of staged logits
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
-constexpr int kSmallCols = 8;        // small row path: <= 8 columns per lane (N <= 256)
+constexpr int kSmallCols = 8;        // reduce path, small rows: <= 8 columns per lane (N <= 256)
 
 template <int BN>
 struct Layout {
@@ -115,8 +121,11 @@ struct Params {
   int n_split, k_split;
   int stages;
   int tma_sf;             // scale tiles by TMA (needs K % 256 == 0)
-  uint32_t region_bytes;  // pipeline ring / accumulator tile region (1 KB multiple)
-  int large;              // row phase through shared-memory keys (k > 32 or N > 256)
+  uint32_t region_bytes;  // pipeline ring, reused after the main loop (1 KB multiple)
+  int direct;             // direct epilogue (k_split == 1, k <= 32)
+  int ro;                 // rows of a tile owned by each CTA of the cluster
+  int rst;                // reduce path: row stride of the pushed partials (ro | 1)
+  int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 256)
   int sel_warps;          // warps that own a key buffer in the large path
   int cand_cap;           // large path: power of two >= k
   uint32_t row_bytes;     // large path: bytes of one warp's key buffer (16-byte multiple)
@@ -150,12 +159,15 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 // (score key, column) packed so that a larger value is a better entry:
-// higher score first, then lower column.
+// higher score first, then lower column.  0 is below every real entry.
 __device__ __forceinline__ uint64_t entry(float s, int n) {
   return (static_cast<uint64_t>(float_key(s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
 }
 __device__ __forceinline__ int entry_col(uint64_t e) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+__device__ __forceinline__ float entry_score(uint64_t e) {
+  return key_float(static_cast<uint32_t>(e >> 32));
 }
 
 // sqrt(softplus(z)) with softplus(z) = max(z, 0) + log1p(exp(-|z|)).  For
@@ -169,23 +181,6 @@ __device__ __forceinline__ float router_weight(float z) {
   return sqrtf(fmaxf(z, 0.0f) + l);
 }
 
-struct RowCtx {
-  uint32_t dump_addr;  // shared address of this CTA's accumulator tile
-  int dr;              // tile row stride (floats)
-  int n_split, k_split, bn;
-  float gab;
-};
-
-// Logit of (tile row r, column n): the K slices' partial sums in rank order.
-__device__ __forceinline__ float gather_logit(const RowCtx& c, int r, int n) {
-  const int nidx = n / c.bn;
-  const uint32_t off = static_cast<uint32_t>(((n - nidx * c.bn) * c.dr + r) * 4);
-  float acc = 0.0f;
-  for (int ks = 0; ks < c.k_split; ++ks)
-    acc += ld_cluster_f32(mapa_shared(c.dump_addr, static_cast<uint32_t>(ks * c.n_split + nidx)) + off);
-  return acc * c.gab;
-}
-
 __device__ __forceinline__ float score_of(const Params& p, float z, int n) {
   return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) + __ldg(p.bias + n) : z;
 }
@@ -193,56 +188,176 @@ __device__ __forceinline__ float weight_of(const Params& p, float z) {
   return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) : z;
 }
 
-// k <= 32, N <= 256: each lane holds up to 8 columns (lane + 32 i) in
-// registers; k rounds of a warp arg-max over (score, -column).
-__device__ void row_small(const Params& p, const RowCtx& c, int r, int64_t grow) {
+// Lowest logit that can still score above t (router: given the largest bias
+// bmax of the columns in play), minus a wide margin; -inf when every logit
+// can.  sqrt(softplus(z)) + b > t needs softplus(z) > (t - bmax)^2, i.e.
+// z > log(exp(y^2) - 1) with y = t - bmax.  The margin (1e-3 absolute +
+// 1e-3 relative, with y shrunk by 1e-4 first) dwarfs the ~1e-5 error of the
+// fast functions on both sides, so no column that scores above t is skipped.
+__device__ __forceinline__ float logit_floor(int epilogue, float t, float bmax) {
+  if (epilogue != NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) return t;
+  const float y = (t - bmax) * 0.9999f;
+  if (!(y > 0.0f)) return -__int_as_float(0x7F800000);
+  const float y2 = y * y;
+  const float g = y2 > 20.0f ? y2 : (y2 < 1e-3f ? __logf(y2) : __logf(__expf(y2) - 1.0f));
+  return g - 1e-3f * (1.0f + fabsf(g));
+}
+
+// Sorted (descending) insertion into a KMAX-entry register list; equal
+// scores keep the earlier entry ahead.
+template <int KMAX>
+__device__ __forceinline__ void list_insert(float (&tv)[KMAX], int (&ti)[KMAX], float (&tw)[KMAX],
+                                            float s, int n, float w) {
+#pragma unroll
+  for (int i = KMAX - 1; i > 0; --i) {
+    if (s > tv[i - 1]) {
+      tv[i] = tv[i - 1];
+      ti[i] = ti[i - 1];
+      tw[i] = tw[i - 1];
+    } else if (s > tv[i]) {
+      tv[i] = s;
+      ti[i] = n;
+      tw[i] = w;
+    }
+  }
+  if (s > tv[0]) {
+    tv[0] = s;
+    ti[0] = n;
+    tw[0] = w;
+  }
+}
+
+// The k-th best score of a sorted list: the minimum over its first k slots
+// (a predicated reduction; selecting slot k-1 directly would make the
+// compiler index the array and move it to local memory).
+template <int KMAX>
+__device__ __forceinline__ float list_kth(const float (&tv)[KMAX], int k) {
+  float t = __int_as_float(0x7F800000);
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) t = fminf(t, i < k ? tv[i] : __int_as_float(0x7F800000));
+  return t;
+}
+
+template <int KMAX>
+__device__ __forceinline__ void list_init(float (&tv)[KMAX], int (&ti)[KMAX], float (&tw)[KMAX]) {
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) {
+    tv[i] = -__int_as_float(0x7F800000);
+    ti[i] = -1;
+    tw[i] = 0.0f;
+  }
+}
+
+template <int KMAX>
+__device__ __forceinline__ void list_store(const Params& p, int64_t grow, const float (&tv)[KMAX],
+                                           const int (&ti)[KMAX], const float (&tw)[KMAX]) {
+  const int64_t o = grow * p.k;
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) {
+    if (i < p.k) {  // empty slots hold -1 / -inf / 0 already
+      p.topk_idx[o + i] = ti[i];
+      p.topk_score[o + i] = tv[i];
+      if (p.topk_weight) p.topk_weight[o + i] = tw[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- reduce-path rows
+
+struct RowCtx {
+  const float* recv;  // pushed partials of this CTA's rows: [k_split][N][rst]
+  int rst;
+  int k_split;
+  float gab;
+};
+
+// Logit of owned row rr, column n: the K slices' partial sums in slice order.
+__device__ __forceinline__ float row_logit(const Params& p, const RowCtx& c, int rr, int n) {
+  float acc = 0.0f;
+  for (int ks = 0; ks < c.k_split; ++ks) acc += c.recv[(static_cast<int64_t>(ks) * p.N + n) * c.rst + rr];
+  return acc * c.gab;
+}
+
+__device__ __forceinline__ void ce_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b;
+  const uint64_t lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Sort 8 entries descending (Batcher's odd-even merge sort network, 19 comparators).
+__device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
+  ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
+  ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
+  ce_desc(v[1], v[2]); ce_desc(v[5], v[6]);
+  ce_desc(v[0], v[4]); ce_desc(v[1], v[5]); ce_desc(v[2], v[6]); ce_desc(v[3], v[7]);
+  ce_desc(v[2], v[4]); ce_desc(v[3], v[5]);
+  ce_desc(v[1], v[2]); ce_desc(v[3], v[4]); ce_desc(v[5], v[6]);
+}
+
+// The 8 best entries of the whole warp, in every lane: each lane sorts its 8,
+// then 5 butterfly levels each keep the top 8 of two sorted lists (the
+// elementwise max against the partner's reversed list is bitonic and holds
+// them; a bitonic merge sorts it).
+__device__ __forceinline__ void warp_top8(uint64_t (&v)[8]) {
+  sort8_desc(v);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint64_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = v[i] > w[7 - i] ? v[i] : w[7 - i];
+    ce_desc(v[0], v[4]); ce_desc(v[1], v[5]); ce_desc(v[2], v[6]); ce_desc(v[3], v[7]);
+    ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
+    ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
+  }
+}
+
+// k <= 32, N <= 256: columns lane + 32 i in registers.
+__device__ void row_small(const Params& p, const RowCtx& c, int rr, int64_t grow) {
   const uint32_t lane = lane_id();
   uint64_t e[kSmallCols];
-  float zv[kSmallCols];
 #pragma unroll
   for (int i = 0; i < kSmallCols; ++i) {
     const int n = static_cast<int>(lane) + 32 * i;
     e[i] = 0ull;
-    zv[i] = 0.0f;
     if (n < p.N) {
-      const float z = gather_logit(c, r, n);
+      const float z = row_logit(p, c, rr, n);
       if (p.logits != nullptr) p.logits[grow * p.N + n] = z;
-      zv[i] = z;
       e[i] = entry(score_of(p, z, n), n);
     }
   }
   const int want = p.k < p.N ? p.k : p.N;
   uint64_t mine = 0ull;
-  float mine_z = 0.0f;
-  for (int t = 0; t < want; ++t) {
-    uint64_t best = e[0];
+  if (p.k <= 8) {
+    warp_top8(e);
 #pragma unroll
-    for (int i = 1; i < kSmallCols; ++i) best = e[i] > best ? e[i] : best;
+    for (int i = 0; i < 8; ++i)
+      if (static_cast<int>(lane) == i) mine = e[i];
+  } else {
+    for (int t = 0; t < want; ++t) {  // k rounds of a warp arg-max
+      uint64_t best = e[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      best = other > best ? other : best;
-    }
-    float zb = 0.0f;
+      for (int i = 1; i < kSmallCols; ++i) best = e[i] > best ? e[i] : best;
 #pragma unroll
-    for (int i = 0; i < kSmallCols; ++i) {
-      if (e[i] == best) {
-        zb = zv[i];
-        e[i] = 0ull;
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
       }
-    }
-    zb = __shfl_sync(0xFFFFFFFFu, zb, entry_col(best) & 31);
-    if (static_cast<int>(lane) == t) {
-      mine = best;
-      mine_z = zb;
+#pragma unroll
+      for (int i = 0; i < kSmallCols; ++i)
+        if (e[i] == best) e[i] = 0ull;
+      if (static_cast<int>(lane) == t) mine = best;
     }
   }
   if (static_cast<int>(lane) < p.k) {
     const int64_t o = grow * p.k + lane;
     if (static_cast<int>(lane) < want) {
-      p.topk_idx[o] = entry_col(mine);
-      p.topk_score[o] = key_float(static_cast<uint32_t>(mine >> 32));
-      if (p.topk_weight) p.topk_weight[o] = weight_of(p, mine_z);
+      const int n = entry_col(mine);
+      p.topk_idx[o] = n;
+      p.topk_score[o] = entry_score(mine);
+      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(p, c, rr, n));
     } else {
       p.topk_idx[o] = -1;
       p.topk_score[o] = -__int_as_float(0x7F800000);
@@ -254,12 +369,12 @@ __device__ void row_small(const Params& p, const RowCtx& c, int r, int64_t grow)
 // General row: keys of all N scores in shared memory, 4-pass radix select
 // of the k-th largest key, in-order compaction (keys above it, then the
 // lowest-column ties), bitonic sort of the picks, outputs.
-__device__ void row_large(const Params& p, const RowCtx& c, int r, int64_t grow, uint32_t* keys,
+__device__ void row_large(const Params& p, const RowCtx& c, int rr, int64_t grow, uint32_t* keys,
                           uint32_t* hist, uint64_t* cand) {
   const uint32_t lane = lane_id();
   const int n_all = p.N;
   for (int n = lane; n < n_all; n += 32) {
-    const float z = gather_logit(c, r, n);
+    const float z = row_logit(p, c, rr, n);
     if (p.logits != nullptr) p.logits[grow * n_all + n] = z;
     keys[n] = float_key(score_of(p, z, n));
   }
@@ -354,8 +469,8 @@ __device__ void row_large(const Params& p, const RowCtx& c, int r, int64_t grow,
       const uint64_t v = cand[t];
       const int n = entry_col(v);
       p.topk_idx[o] = n;
-      p.topk_score[o] = key_float(static_cast<uint32_t>(v >> 32));
-      if (p.topk_weight) p.topk_weight[o] = weight_of(p, gather_logit(c, r, n));
+      p.topk_score[o] = entry_score(v);
+      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(p, c, rr, n));
     } else {
       p.topk_idx[o] = -1;
       p.topk_score[o] = -__int_as_float(0x7F800000);
@@ -365,7 +480,9 @@ __device__ void row_large(const Params& p, const RowCtx& c, int r, int64_t grow,
   __syncwarp();
 }
 
-template <int BN>
+// ---------------------------------------------------------------- the kernel
+
+template <int BN, int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_topk_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b,
@@ -402,7 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = (k_idx + 1) * p.num_k_tiles / p.k_split - kt0;
   const int ncols = min(BN, p.N - n0);
   const int mma_n = min(BN, (ncols + 15) & ~15);
-  const int dr = vr | 1;
   constexpr int kUnits = 1 + L::kAtomsB;  // scale atoms per stage: SFA + SFB's
 
   if (threadIdx.x == 0) {
@@ -432,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  bool acc_ready = false;  // epilogue warps: the accumulator is complete
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -538,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ scale layout, then the tile dump
+    // ------------------------------------------------------------ scale layout
     const int unit = warp - 2;
     if (unit < kUnits) {
       for (int i = 0; i < nk; ++i) {
@@ -570,51 +687,153 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(sfready_bar(s));
       }
     }
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + static_cast<int>(lane);
-    if (!warp_wait(tfull_bar, 0, abort)) {
-      if (lane == 0) record_timeout(p.status, abort);
-    } else {
+    if (warp_wait(tfull_bar, 0, abort)) {
+      acc_ready = true;
       tc_fence_after();
-      float* tile = reinterpret_cast<float*>(smem);
+    } else if (lane == 0) {
+      record_timeout(p.status, abort);
+    }
+  }
+
+  const float gab = __ldg(p.gsa) * __ldg(p.gsb);
+  const int quarter = warp & 3;  // epilogue warps read TMEM lanes 32*quarter .. +31
+  const int row = quarter * 32 + static_cast<int>(lane);
+
+  if (p.direct) {
+    // ------------------------------------------------------------ direct epilogue
+    if (warp >= 2) {
+      float tv[KMAX], tw[KMAX];
+      int ti[KMAX];
+      list_init<KMAX>(tv, ti, tw);
+      float bmax = -__int_as_float(0x7F800000);
+      if (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
+        for (int c = lane; c < ncols; c += 32) bmax = fmaxf(bmax, __ldg(p.bias + n0 + c));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, o));
+      }
+      float kth = -__int_as_float(0x7F800000);
+      float zfloor = -__int_as_float(0x7F800000);
+      float* scratch = reinterpret_cast<float*>(smem) + row * kScratchStride;
+      if (acc_ready) {
+        for (int c0 = 0; c0 < mma_n; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+          tmem_wait_ld();
+          uint32_t mask = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float z = __uint_as_float(v[j]) * gab;
+            scratch[j] = z;
+            if (c0 + j < ncols && z > zfloor) mask |= 1u << j;
+          }
+          if (row >= vr) mask = 0;
+          if (p.logits != nullptr && row < vr) {
+            for (int j = 0; j < 32 && c0 + j < ncols; ++j)
+              p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = scratch[j];
+          }
+          while (mask) {
+            const int j = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const float z = scratch[j];
+            const int n = n0 + c0 + j;
+            const float s = score_of(p, z, n);
+            if (s > kth) {
+              list_insert<KMAX>(tv, ti, tw, s, n, weight_of(p, z));
+              kth = list_kth<KMAX>(tv, p.k);
+              zfloor = logit_floor(p.epilogue, kth, bmax);
+            }
+          }
+        }
+      }
+      if (p.n_split == 1) {
+        if (row < vr) list_store<KMAX>(p, m0 + row, tv, ti, tw);
+      } else if (row < vr) {
+        // push the row's list to its owner: [n slice][owned row][KMAX] x 16 bytes
+        const int owner = row / p.ro;
+        const uint32_t dst = mapa_shared(smem_addr(rowmem), static_cast<uint32_t>(owner)) +
+                             static_cast<uint32_t>(((n_idx * p.ro + (row - owner * p.ro)) * KMAX) * 16);
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i)
+          st_cluster_v4(dst + i * 16, __float_as_uint(tv[i]), static_cast<uint32_t>(ti[i]),
+                        __float_as_uint(tw[i]), 0u);
+      }
+    }
+    if (p.n_split > 1) {
+      tc_fence_before();
+      cluster_sync();  // every CTA's lists have arrived at their owners
+      tc_fence_after();
+      const int r0 = rank * p.ro;
+      const int owned = min(p.ro, vr - r0);
+      const int t = static_cast<int>(threadIdx.x);
+      if (t < owned) {
+        float tv[KMAX], tw[KMAX];
+        int ti[KMAX];
+        list_init<KMAX>(tv, ti, tw);
+        float kth = -__int_as_float(0x7F800000);
+        const uint32_t* lists = reinterpret_cast<const uint32_t*>(rowmem);
+        for (int ni = 0; ni < p.n_split; ++ni) {  // slices in column order: ties stay by lower n
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) {
+            const uint32_t* e = lists + ((ni * p.ro + t) * KMAX + i) * 4;
+            const float s = __uint_as_float(e[0]);
+            if (s > kth) {
+              list_insert<KMAX>(tv, ti, tw, s, static_cast<int>(e[1]), __uint_as_float(e[2]));
+              kth = list_kth<KMAX>(tv, p.k);
+            }
+          }
+        }
+        list_store<KMAX>(p, m0 + r0 + t, tv, ti, tw);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ reduce epilogue
+    tc_fence_before();
+    cluster_sync();  // every main loop in the cluster is over: stage regions take pushes
+    tc_fence_after();
+    if (warp >= 2 && acc_ready) {  // warp-uniform: tcgen05.ld is warp-collective
+      const bool live = row < vr;
+      const int owner = live ? row / p.ro : 0;
+      const uint32_t base = mapa_shared(sbase, static_cast<uint32_t>(owner)) +
+                            static_cast<uint32_t>(live ? row - owner * p.ro : 0) * 4u;
       for (int c0 = 0; c0 < mma_n; c0 += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
         tmem_wait_ld();
-        if (row < vr) {
+        if (live) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < ncols) tile[(c0 + j) * dr + row] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) {
+            if (c0 + j < ncols) {
+              const int64_t slot = (static_cast<int64_t>(k_idx) * p.N + n0 + c0 + j) * p.rst;
+              st_cluster_f32(base + static_cast<uint32_t>(slot * 4), __uint_as_float(v[j]));
+            }
+          }
         }
       }
     }
     tc_fence_before();
-  }
-
-  // ------------------------------------------------------------ row phase
-  cluster_sync();
-  {
+    cluster_sync();  // all partial sums of this CTA's rows have arrived
+    tc_fence_after();
     RowCtx c;
-    c.dump_addr = sbase;
-    c.dr = dr;
-    c.n_split = p.n_split;
+    c.recv = reinterpret_cast<const float*>(smem);
+    c.rst = p.rst;
     c.k_split = p.k_split;
-    c.bn = BN;
-    c.gab = __ldg(p.gsa) * __ldg(p.gsb);
-    const int r_begin = rank * vr / csize;
-    const int r_end = (rank + 1) * vr / csize;
+    c.gab = gab;
+    const int r0 = rank * p.ro;
+    const int owned = min(p.ro, vr - r0);
     if (!p.large) {
-      for (int r = r_begin + warp; r < r_end; r += kWarps) row_small(p, c, r, m0 + r);
+      for (int rr = warp; rr < owned; rr += kWarps) row_small(p, c, rr, m0 + r0 + rr);
     } else if (warp < p.sel_warps) {
       uint8_t* mine = rowmem + warp * (p.row_bytes + 1024 + p.cand_cap * 8);
       uint32_t* keys = reinterpret_cast<uint32_t*>(mine);
       uint32_t* hist = reinterpret_cast<uint32_t*>(mine + p.row_bytes);
       uint64_t* cand = reinterpret_cast<uint64_t*>(mine + p.row_bytes + 1024);
-      for (int r = r_begin + warp; r < r_end; r += p.sel_warps) row_large(p, c, r, m0 + r, keys, hist, cand);
+      for (int rr = warp; rr < owned; rr += p.sel_warps)
+        row_large(p, c, rr, m0 + r0 + rr, keys, hist, cand);
     }
   }
-  cluster_sync();  // every CTA's tile stays valid until the whole cluster has read it
 
+  tc_fence_before();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -661,17 +880,18 @@ int next_pow2(int v) {
 }
 
 struct Plan {
-  int bn;
+  int bn, kmax;
   int n_split, k_split;
   int stages;
+  int direct, ro, rst;
   int large, sel_warps, cand_cap;
   uint32_t row_bytes;
   uint32_t region;
   size_t smem;
 };
 
-// Pick the split and the shared-memory layout of one problem; false if it
-// cannot be laid out.
+// Pick the split, epilogue and shared-memory layout of one problem; false if
+// it cannot be laid out.
 bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, int max_cluster,
                Plan* out) {
   Plan pl{};
@@ -693,23 +913,35 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
     if (ks > kt) ks = kt;
     pl.k_split = ks < 1 ? 1 : ks;
   }
-  pl.large = (k > 32 || N > 32 * kSmallCols) ? 1 : 0;
+  const int csize = pl.n_split * pl.k_split;
+  const int vr_max = static_cast<int>(M < BM ? M : BM);
+  pl.ro = (vr_max + csize - 1) / csize;
+  pl.rst = pl.ro | 1;
+  pl.direct = (pl.k_split == 1 && k <= 32) ? 1 : 0;
+  pl.kmax = k <= 8 ? 8 : (k <= 16 ? 16 : 32);
+  pl.large = (!pl.direct && (k > 32 || N > 32 * kSmallCols)) ? 1 : 0;
   pl.cand_cap = pl.large ? next_pow2(k) : 0;
   pl.row_bytes = pl.large ? static_cast<uint32_t>((N * 4 + 15) & ~15) : 0u;
   const int nk_max = (kt + pl.k_split - 1) / pl.k_split;
   const uint32_t sb = pl.bn == 128 ? Layout<128>::kStage : Layout<256>::kStage;
-  const int vr_max = static_cast<int>(M < BM ? M : BM);
-  const uint32_t dump = static_cast<uint32_t>(pl.bn) * static_cast<uint32_t>(vr_max | 1) * 4u;
+  // Stage region reuse after the main loop: the direct epilogue's staged
+  // logits, or the reduce epilogue's pushed partial sums.
+  const uint32_t reuse = pl.direct ? BM * kScratchStride * 4u
+                                   : static_cast<uint32_t>(pl.k_split) * static_cast<uint32_t>(N) *
+                                         static_cast<uint32_t>(pl.rst) * 4u;
   pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
   pl.sel_warps = pl.large ? kWarps : 0;
   auto total = [&]() {
-    uint32_t region = pl.stages * sb > dump ? pl.stages * sb : dump;
+    uint32_t region = pl.stages * sb > reuse ? pl.stages * sb : reuse;
     region = (region + 1023u) & ~1023u;
     pl.region = region;
-    const size_t sel = pl.large ? static_cast<size_t>(pl.sel_warps) *
-                                      (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8)
-                                : 0;
-    return 1024 + static_cast<size_t>(region) + kCtrlBytes + sel;
+    size_t extra = 0;
+    if (pl.direct && pl.n_split > 1)
+      extra = static_cast<size_t>(pl.n_split) * pl.ro * pl.kmax * 16;  // merged per-row lists
+    if (pl.large)
+      extra = static_cast<size_t>(pl.sel_warps) *
+              (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8);
+    return 1024 + static_cast<size_t>(region) + kCtrlBytes + extra;
   };
   while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
   while (total() > static_cast<size_t>(smem_optin) && pl.sel_warps > 1) --pl.sel_warps;
@@ -719,7 +951,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   return true;
 }
 
-template <int BN>
+template <int BN, int KMAX>
 cudaLaunchConfig_t launch_config(int grid, int cluster, size_t smem, cudaStream_t stream,
                                  cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -737,9 +969,9 @@ cudaLaunchConfig_t launch_config(int grid, int cluster, size_t smem, cudaStream_
 }
 
 // Function attributes the launch needs (idempotent).
-template <int BN>
+template <int BN, int KMAX>
 cudaError_t configure(size_t smem, int cluster) {
-  auto kern = gemm_topk_kernel<BN>;
+  auto kern = gemm_topk_kernel<BN, KMAX>;
   static std::mutex mu;
   static int configured = 0;  // largest dynamic smem size set so far for this variant
   static bool nonportable = false;
@@ -760,7 +992,7 @@ cudaError_t configure(size_t smem, int cluster) {
 
 // Whether clusters of this size and shared-memory footprint can be resident
 // at all (answers cached per device and configuration).
-template <int BN>
+template <int BN, int KMAX>
 bool cluster_fits(int cluster, size_t smem) {
   if (cluster <= 1) return true;
   static std::mutex mu;
@@ -774,11 +1006,11 @@ bool cluster_fits(int cluster, size_t smem) {
   for (int i = 0; i < n_cache; ++i)
     if (cache_dev[i] == dev && cache_cluster[i] == cluster && cache_smem[i] == smem) return cache_ok[i];
   bool ok = false;
-  if (configure<BN>(smem, cluster) == cudaSuccess) {
+  if (configure<BN, KMAX>(smem, cluster) == cudaSuccess) {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config<BN>(cluster, cluster, smem, nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(cluster, cluster, smem, nullptr, attr);
     int n = 0;
-    ok = cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN>, &cfg) == cudaSuccess && n > 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN, KMAX>, &cfg) == cudaSuccess && n > 0;
   }
   cudaGetLastError();  // a refused query leaves no error behind
   if (n_cache < 64) {
@@ -791,15 +1023,40 @@ bool cluster_fits(int cluster, size_t smem) {
   return ok;
 }
 
-template <int BN>
+template <int BN, int KMAX>
 cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
                            const CUtensorMap& msb, const Params& p, int grid, int cluster,
                            size_t smem, cudaStream_t stream) {
-  const cudaError_t e = configure<BN>(smem, cluster);
+  const cudaError_t e = configure<BN, KMAX>(smem, cluster);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config<BN>(grid, cluster, smem, stream, attr);
-  return cudaLaunchKernelEx(&cfg, gemm_topk_kernel<BN>, ma, mb, msa, msb, p);
+  cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(grid, cluster, smem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gemm_topk_kernel<BN, KMAX>, ma, mb, msa, msb, p);
+}
+
+bool fits(const Plan& pl) {
+  const int c = pl.n_split * pl.k_split;
+  if (pl.bn == 128) {
+    if (pl.kmax == 8) return cluster_fits<128, 8>(c, pl.smem);
+    if (pl.kmax == 16) return cluster_fits<128, 16>(c, pl.smem);
+    return cluster_fits<128, 32>(c, pl.smem);
+  }
+  if (pl.kmax == 8) return cluster_fits<256, 8>(c, pl.smem);
+  if (pl.kmax == 16) return cluster_fits<256, 16>(c, pl.smem);
+  return cluster_fits<256, 32>(c, pl.smem);
+}
+
+cudaError_t launch(const Plan& pl, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
+                   const CUtensorMap& msb, const Params& p, int grid, cudaStream_t stream) {
+  const int c = pl.n_split * pl.k_split;
+  if (pl.bn == 128) {
+    if (pl.kmax == 8) return launch_variant<128, 8>(ma, mb, msa, msb, p, grid, c, pl.smem, stream);
+    if (pl.kmax == 16) return launch_variant<128, 16>(ma, mb, msa, msb, p, grid, c, pl.smem, stream);
+    return launch_variant<128, 32>(ma, mb, msa, msb, p, grid, c, pl.smem, stream);
+  }
+  if (pl.kmax == 8) return launch_variant<256, 8>(ma, mb, msa, msb, p, grid, c, pl.smem, stream);
+  if (pl.kmax == 16) return launch_variant<256, 16>(ma, mb, msa, msb, p, grid, c, pl.smem, stream);
+  return launch_variant<256, 32>(ma, mb, msa, msb, p, grid, c, pl.smem, stream);
 }
 
 }  // namespace
@@ -816,9 +1073,8 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   int cap = kMaxCluster;
   for (;;) {
     if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, &pl)) return NVFP4_ERR_UNSUPPORTED;
+    if (fits(pl)) break;
     const int c = pl.n_split * pl.k_split;
-    const bool fits = pl.bn == 128 ? cluster_fits<128>(c, pl.smem) : cluster_fits<256>(c, pl.smem);
-    if (fits) break;
     if (c <= 1 || cap <= 1) return NVFP4_ERR_UNSUPPORTED;
     cap = c / 2;
   }
@@ -859,15 +1115,15 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.stages = pl.stages;
   p.tma_sf = tma_sf ? 1 : 0;
   p.region_bytes = pl.region;
+  p.direct = pl.direct;
+  p.ro = pl.ro;
+  p.rst = pl.rst;
   p.large = pl.large;
   p.sel_warps = pl.sel_warps;
   p.cand_cap = pl.cand_cap;
   p.row_bytes = pl.row_bytes;
-  const int cluster = pl.n_split * pl.k_split;
-  const int grid = static_cast<int>((a.M + BM - 1) / BM) * cluster;
-  const cudaError_t e =
-      pl.bn == 128 ? launch_variant<128>(ma, mb, msa, msb, p, grid, cluster, pl.smem, stream)
-                   : launch_variant<256>(ma, mb, msa, msb, p, grid, cluster, pl.smem, stream);
+  const int grid = static_cast<int>((a.M + BM - 1) / BM) * pl.n_split * pl.k_split;
+  const cudaError_t e = launch(pl, ma, mb, msa, msb, p, grid, stream);
   if (e != cudaSuccess) {
     *err = e;
     return NVFP4_ERR_CUDA;

@@ -125,6 +125,8 @@ EDGE = [
     (33, 1000, 256, 100, 0),    # select path, ragged
     (200, 4096, 128, 1024, 0),  # largest k, largest N for the select path
     (9, 4000, 64, 1024, 1),
+    (300, 256, 512, 20, 1),     # split K, warp arg-max rounds (8 < k <= 32)
+    (64, 128, 7168, 8, 1),      # split K over many slices, butterfly top-8
 ]
 
 
@@ -137,6 +139,28 @@ def test_edge_shapes(nv, ws, M, N, K, k, epi):
     qa, sfa, gsa = quantized(xa)
     qb, sfb, gsb = quantized(xb)
     check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, epi, bias, k, what=f"edge {M}x{N}x{K} k={k}")
+
+
+# Many row tiles: two 128-column CTAs per tile, per-thread register lists of
+# 16 / 32 entries merged across the pair (checked on sampled rows).
+WIDE = [
+    (5000, 256, 256, 12, 1),
+    (5000, 200, 512, 24, 0),
+    (4900, 256, 768, 32, 1),
+]
+
+
+@pytest.mark.parametrize("M,N,K,k,epi", WIDE)
+def test_many_row_tiles(nv, ws, M, N, K, k, epi):
+    rng = np.random.default_rng(M + N + K)
+    xa = workloads.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    xb = workloads.bf16_bits((rng.standard_normal((N, K)) * 0.05).astype(np.float32))
+    bias = (rng.standard_normal(N) * 0.01).astype(np.float32) if epi == 1 else None
+    qa, sfa, gsa = quantized(xa)
+    qb, sfb, gsb = quantized(xb)
+    rows = sorted(set(range(0, 130)) | set(range(M - 70, M)) | set(rng.integers(0, M, 200).tolist()))
+    check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, epi, bias, k, rows=rows,
+               what=f"wide {M}x{N}x{K} k={k}")
 
 
 @pytest.mark.parametrize("k", [4, 40])
