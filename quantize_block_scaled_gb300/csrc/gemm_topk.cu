@@ -32,10 +32,10 @@
 //
 // Then one of two epilogues.
 //  Direct (no K split, k <= 32): the thread that owns TMEM lane r owns row
-//    r.  It walks its columns 32 at a time, skips every column whose logit
-//    cannot reach the current k-th best score (a bound on the logit derived
-//    once per threshold change, so most columns cost a multiply and a
-//    compare), scores the rest, and keeps a sorted register list.  With an N
+//    r.  It walks its columns 32 at a time: scores the whole chunk
+//    branch-free (independent columns give the exponential, log and square
+//    root instruction-level parallelism), then compares each score with the
+//    current k-th best and inserts into a sorted register list.  With an N
 //    split, each CTA pushes its per-row lists to the row's owner in the
 //    cluster (remote shared-memory stores), which merges them.
 //  Reduce (K split, or k > 32): each CTA pushes its FP32 partial sums to the
@@ -46,8 +46,8 @@
 //    shared memory otherwise (the indexer's top-512).
 //
 // The pages' WIP fused router kernel (TMA warp, MMA warp, four epilogue warps
-// with per-thread heaps) is prior art; the split, the scale-factor path, the
-// threshold filter and the selection schemes here are this library's own.
+// with per-thread heaps) is prior art; the split, the scale-factor path and
+// the selection schemes here are this library's own.
 //
 // Every wait on an mbarrier is bounded: after ~1 s of SM clock it records
 // NVFP4_DEVICE_TIMEOUT in the workspace, tells the CTA's other warps to stop,
@@ -79,7 +79,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;  // scale factors live after the (<= 256-column) accumulator
 constexpr uint32_t kSfChunk = 512;     // scales of 128 rows for one MMA (K = 64)
 constexpr uint32_t kCtrlBytes = 256;
-constexpr uint32_t kScratchStride = 33;  // direct epilogue: floats per thread of staged logits
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
 constexpr int kSmallCols = 8;        // reduce path, small rows: <= 8 columns per lane (N <= 256)
 
@@ -186,21 +185,6 @@ __device__ __forceinline__ float score_of(const Params& p, float z, int n) {
 }
 __device__ __forceinline__ float weight_of(const Params& p, float z) {
   return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) : z;
-}
-
-// Lowest logit that can still score above t (router: given the largest bias
-// bmax of the columns in play), minus a wide margin; -inf when every logit
-// can.  sqrt(softplus(z)) + b > t needs softplus(z) > (t - bmax)^2, i.e.
-// z > log(exp(y^2) - 1) with y = t - bmax.  The margin (1e-3 absolute +
-// 1e-3 relative, with y shrunk by 1e-4 first) dwarfs the ~1e-5 error of the
-// fast functions on both sides, so no column that scores above t is skipped.
-__device__ __forceinline__ float logit_floor(int epilogue, float t, float bmax) {
-  if (epilogue != NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) return t;
-  const float y = (t - bmax) * 0.9999f;
-  if (!(y > 0.0f)) return -__int_as_float(0x7F800000);
-  const float y2 = y * y;
-  const float g = y2 > 20.0f ? y2 : (y2 < 1e-3f ? __logf(y2) : __logf(__expf(y2) - 1.0f));
-  return g - 1e-3f * (1.0f + fabsf(g));
 }
 
 // Sorted (descending) insertion into a KMAX-entry register list; equal
@@ -386,9 +370,15 @@ __device__ void row_large(const Params& p, const RowCtx& c, int rr, int64_t grow
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
-    for (int i = lane; i < n_all; i += 32) {
-      const uint32_t u = keys[i];
-      if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    // Keys crowd into a few bins (scores share their top bits), so lanes with
+    // the same bin add their count once through the lowest such lane.
+    for (int base = 0; base < n_all; base += 32) {
+      const int i = base + static_cast<int>(lane);
+      const uint32_t u = i < n_all ? keys[i] : 0u;
+      const bool in = i < n_all && (u & pmask) == prefix;
+      const uint32_t bin = in ? (u >> shift) & 255u : 256u + lane;
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+      if (in && (__ffs(peers) - 1) == static_cast<int>(lane)) atomicAdd(&hist[bin], __popc(peers));
     }
     __syncwarp();
     uint32_t cnt[8];
@@ -705,42 +695,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       float tv[KMAX], tw[KMAX];
       int ti[KMAX];
       list_init<KMAX>(tv, ti, tw);
-      float bmax = -__int_as_float(0x7F800000);
-      if (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
-        for (int c = lane; c < ncols; c += 32) bmax = fmaxf(bmax, __ldg(p.bias + n0 + c));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, o));
-      }
+      const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
+      // This warp's copy of the bias of the CTA's columns (stage region is free now).
+      float* bias_s = reinterpret_cast<float*>(smem) + (warp - 2) * BN;
+      if (router)
+        for (int c = lane; c < ncols; c += 32) bias_s[c] = __ldg(p.bias + n0 + c);
+      __syncwarp();
+      const bool live = row < vr;
+      const bool full_list = p.k == KMAX;  // k-th score is simply the last slot
       float kth = -__int_as_float(0x7F800000);
-      float zfloor = -__int_as_float(0x7F800000);
-      float* scratch = reinterpret_cast<float*>(smem) + row * kScratchStride;
       if (acc_ready) {
         for (int c0 = 0; c0 < mma_n; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
           tmem_wait_ld();
-          uint32_t mask = 0;
+          // Logits, then activations for the whole chunk, branch-free (ILP across columns).
+          float w[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float z = __uint_as_float(v[j]) * gab;
-            scratch[j] = z;
-            if (c0 + j < ncols && z > zfloor) mask |= 1u << j;
+            w[j] = router ? router_weight(z) : z;
+            if (p.logits != nullptr && live && c0 + j < ncols)
+              p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
           }
-          if (row >= vr) mask = 0;
-          if (p.logits != nullptr && row < vr) {
-            for (int j = 0; j < 32 && c0 + j < ncols; ++j)
-              p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = scratch[j];
-          }
-          while (mask) {
-            const int j = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const float z = scratch[j];
-            const int n = n0 + c0 + j;
-            const float s = score_of(p, z, n);
-            if (s > kth) {
-              list_insert<KMAX>(tv, ti, tw, s, n, weight_of(p, z));
-              kth = list_kth<KMAX>(tv, p.k);
-              zfloor = logit_floor(p.epilogue, kth, bmax);
+          if (live) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (c0 + j < ncols) {
+                const float sc = router ? w[j] + bias_s[c0 + j] : w[j];
+                if (sc > kth) {
+                  list_insert<KMAX>(tv, ti, tw, sc, n0 + c0 + j, w[j]);
+                  kth = full_list ? tv[KMAX - 1] : list_kth<KMAX>(tv, p.k);
+                }
+              }
             }
           }
         }
@@ -901,6 +888,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
     pl.bn = 128;
   } else if (N <= 256 && m_tiles * 2 >= sms / 2) {
     pl.bn = 128;  // many row tiles: two 128-column halves give twice the CTAs
+  } else if ((k > 32 || N > 32 * kSmallCols) && N <= 128 * max_cluster && m_tiles * 16 <= sms) {
+    pl.bn = 128;  // long rows, few tiles: twice the CTAs, half the rows per CTA to select
   } else {
     pl.bn = 256;
   }
@@ -924,9 +913,9 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   pl.row_bytes = pl.large ? static_cast<uint32_t>((N * 4 + 15) & ~15) : 0u;
   const int nk_max = (kt + pl.k_split - 1) / pl.k_split;
   const uint32_t sb = pl.bn == 128 ? Layout<128>::kStage : Layout<256>::kStage;
-  // Stage region reuse after the main loop: the direct epilogue's staged
-  // logits, or the reduce epilogue's pushed partial sums.
-  const uint32_t reuse = pl.direct ? BM * kScratchStride * 4u
+  // Stage region reuse after the main loop: the direct epilogue's bias
+  // copies, or the reduce epilogue's pushed partial sums.
+  const uint32_t reuse = pl.direct ? 4u * static_cast<uint32_t>(pl.bn) * 4u
                                    : static_cast<uint32_t>(pl.k_split) * static_cast<uint32_t>(N) *
                                          static_cast<uint32_t>(pl.rst) * 4u;
   pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;

@@ -8,9 +8,11 @@
 // fence) writes gs to device memory; the quantize kernel then reads gs from
 // that buffer.  No host synchronisation anywhere.
 //
-// Memory access: 16-byte vector loads of 8 bf16, one 16-element block (two
-// vectors) per thread and iteration, 8-byte stores of the 8 packed code
-// bytes, grid-stride loops over a grid sized to the SM count.
+// Memory access: 16-byte vector loads of 8 bf16 (eight in flight per thread
+// in the amax pass, two 16-element blocks per thread in the quantize pass),
+// 8-byte stores of the packed code bytes, grid-stride loops over a grid
+// sized to the SM count.  The element quotients x / den are exact (one FMA
+// correction of x * (1/den)), so codes match the correctly rounded division.
 
 #include <cstdint>
 
@@ -43,7 +45,9 @@ __device__ __forceinline__ uint32_t fold16(uint32_t m2) { return max(m2 & 0xFFFF
 
 // ---------------------------------------------------------------- amax
 
-__global__ void __launch_bounds__(kThreads)
+constexpr int kAmaxUnroll = 8;  // 16-byte loads in flight per thread
+
+__global__ void __launch_bounds__(kThreads, 4)
     amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t vpr, int64_t ld,
                 float* __restrict__ gs_out, Workspace* __restrict__ ws) {
   uint32_t m2 = 0;
@@ -51,14 +55,15 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (ld == vpr * 8) {
-    for (; i + 3 * stride < total; i += 4 * stride) {
-      const uint4 a = ld_keep(x + i * 8);
-      const uint4 b = ld_keep(x + (i + stride) * 8);
-      const uint4 c = ld_keep(x + (i + 2 * stride) * 8);
-      const uint4 d = ld_keep(x + (i + 3 * stride) * 8);
-      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(absmax8(a), absmax8(b)), __vmaxu2(absmax8(c), absmax8(d))));
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    for (; i + (kAmaxUnroll - 1) * stride < total; i += kAmaxUnroll * stride) {
+      uint4 v[kAmaxUnroll];
+#pragma unroll
+      for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(xv + i + u * stride);
+#pragma unroll
+      for (int u = 0; u < kAmaxUnroll; ++u) m2 = __vmaxu2(m2, absmax8(v[u]));
     }
-    for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(ld_keep(x + i * 8)));
+    for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(__ldg(xv + i)));
   } else if (i < total) {
     int64_t r = i / vpr, c = i % vpr;
     const int64_t sr = stride / vpr, sc = stride % vpr;
@@ -135,86 +140,119 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float f0, float f1, float f2, flo
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Sign bits of 8 bf16 values, placed at the sign position of each nibble.
-__device__ __forceinline__ uint32_t sign_nibbles(uint4 v) {
-  return ((v.x >> 12) & 0x8u) | ((v.x >> 24) & 0x80u) | ((v.y >> 4) & 0x800u) |
-         ((v.y >> 16) & 0x8000u) | ((v.z << 4) & 0x80000u) | ((v.z >> 8) & 0x800000u) |
-         ((v.w << 12) & 0x8000000u) | (v.w & 0x80000000u);
+// Correctly rounded a / b from r = RN(1/b) by one FMA correction: q = RN(a r),
+// e = a - q b (exact, one FMA), result RN(q + e r).  This is Markstein's
+// division theorem (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r the
+// correctly rounded reciprocal and q within one ulp of a / b, the corrected
+// quotient is the correctly rounded one.  (Results in the subnormal range can
+// be off by an ulp; every such value encodes to a zero code and an E4M3 zero
+// here, so the outputs do not change.)
+__device__ __forceinline__ float div_rn(float a, float b, float r) {
+  const float q = __fmul_rn(a, r);
+  const float e = __fmaf_rn(-q, b, a);
+  return __fmaf_rn(e, r, q);
 }
 
-__device__ __forceinline__ float nudge(float v, int ulps) {
-  return __int_as_float(__float_as_int(v) + ulps);
+// The same for b > 0, keeping the sign of a zero a (the correction's
+// (+0) + (-0) would otherwise turn -0 / b into +0; a nonzero quotient
+// already carries a's sign, so the OR changes nothing else).
+__device__ __forceinline__ float div_rn_signed(float a, float b, float r) {
+  const float d = div_rn(a, b, r);
+  return __uint_as_float(__float_as_uint(d) | (__float_as_uint(a) & 0x80000000u));
 }
 
-// Codes of 8 values x / den, where the quotient is the correctly rounded
-// FP32 division.  Fast path: x * (1/den) is within 2 ulps of that quotient,
-// so if the codes of x*(1/den) moved 4 ulps down and 4 ulps up (in
-// magnitude) agree, the code of the exact quotient lies between them and
-// equals them.  Otherwise (a quotient next to an E2M1 rounding midpoint) the
-// 8 quotients are divided exactly.
-__device__ __forceinline__ uint32_t encode8(uint4 v, float inv, float den) {
-  const float x0 = lo_bf16(v.x), x1 = hi_bf16(v.x), x2 = lo_bf16(v.y), x3 = hi_bf16(v.y);
-  const float x4 = lo_bf16(v.z), x5 = hi_bf16(v.z), x6 = lo_bf16(v.w), x7 = hi_bf16(v.w);
-  const float q0 = __fmul_rn(x0, inv), q1 = __fmul_rn(x1, inv), q2 = __fmul_rn(x2, inv),
-              q3 = __fmul_rn(x3, inv), q4 = __fmul_rn(x4, inv), q5 = __fmul_rn(x5, inv),
-              q6 = __fmul_rn(x6, inv), q7 = __fmul_rn(x7, inv);
-  const uint32_t lo = cvt_e2m1x8(nudge(q0, -4), nudge(q1, -4), nudge(q2, -4), nudge(q3, -4),
-                                 nudge(q4, -4), nudge(q5, -4), nudge(q6, -4), nudge(q7, -4));
-  const uint32_t hi = cvt_e2m1x8(nudge(q0, 4), nudge(q1, 4), nudge(q2, 4), nudge(q3, 4),
-                                 nudge(q4, 4), nudge(q5, 4), nudge(q6, 4), nudge(q7, 4));
-  uint32_t codes = lo;
-  if (lo != hi) {
-    codes = cvt_e2m1x8(__fdiv_rn(x0, den), __fdiv_rn(x1, den), __fdiv_rn(x2, den),
-                       __fdiv_rn(x3, den), __fdiv_rn(x4, den), __fdiv_rn(x5, den),
-                       __fdiv_rn(x6, den), __fdiv_rn(x7, den));
-  }
-  // A negative value that rounds to zero keeps its sign bit.
-  return codes | sign_nibbles(v);
+// Codes of 8 values x / den (correctly rounded quotients; den == 0 passes
+// r = 0 and gives signed zeros).  The E2M1 conversion rounds to nearest
+// even, saturates, and keeps the sign of values that round to zero.
+__device__ __forceinline__ uint32_t encode8(uint4 v, float r, float den) {
+  return cvt_e2m1x8(div_rn_signed(lo_bf16(v.x), den, r), div_rn_signed(hi_bf16(v.x), den, r),
+                    div_rn_signed(lo_bf16(v.y), den, r), div_rn_signed(hi_bf16(v.y), den, r),
+                    div_rn_signed(lo_bf16(v.z), den, r), div_rn_signed(hi_bf16(v.z), den, r),
+                    div_rn_signed(lo_bf16(v.w), den, r), div_rn_signed(hi_bf16(v.w), den, r));
+}
+
+struct Scales {
+  float gs;      // global scale
+  float r_gs;    // RN(1 / gs)
+  float r_six;   // RN(1 / 6)
+};
+
+__device__ __forceinline__ Scales make_scales(const float* gs_ptr) {
+  Scales sc;
+  sc.gs = __ldg(gs_ptr);
+  sc.r_gs = __frcp_rn(sc.gs);
+  sc.r_six = __frcp_rn(6.0f);
+  return sc;
 }
 
 // Quantize one 16-element block held in two vectors.
-__device__ __forceinline__ void quantize_block(uint4 a, uint4 b, float gs, uint32_t& sbyte,
+__device__ __forceinline__ void quantize_block(uint4 a, uint4 b, const Scales& sc, uint32_t& sbyte,
                                                uint2& codes) {
   const uint32_t m = fold16(__vmaxu2(absmax8(a), absmax8(b)));
   const float bamax = __uint_as_float(m << 16);
-  const float s = __fdiv_rn(__fdiv_rn(bamax, 6.0f), gs);
+  const float s = div_rn(div_rn(bamax, 6.0f, sc.r_six), sc.gs, sc.r_gs);  // (bamax / 6) / gs
   sbyte = e4m3_encode(s);
-  const float den = __fmul_rn(e4m3_decode(sbyte), gs);
-  if (den == 0.0f) {
-    codes = make_uint2(sign_nibbles(a), sign_nibbles(b));
-  } else {
-    const float inv = __frcp_rn(den);
-    codes = make_uint2(encode8(a, inv, den), encode8(b, inv, den));
-  }
+  const float den = __fmul_rn(e4m3_decode(sbyte), sc.gs);
+  const float r = den == 0.0f ? 0.0f : __frcp_rn(den);
+  codes = make_uint2(encode8(a, r, den), encode8(b, r, den));
 }
 
 // ---------------------------------------------------------------- quantize
 
-__global__ void __launch_bounds__(kThreads)
+// Blocks are visited from the end of the tensor backwards: the amax pass that
+// ran just before leaves the tail of a tensor larger than L2 in L2, so this
+// pass finds that part there.  Loads and stores stream (evict first).
+__global__ void __launch_bounds__(kThreads, 4)
     quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t bpr, int64_t ld,
                     uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                     const float* __restrict__ gs_ptr) {
   const int64_t total = rows * bpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const float gs = __ldg(gs_ptr);
-  int64_t r = i / bpr, c = i % bpr;
-  const int64_t sr = stride / bpr, sc = stride % bpr;
-  while (r < rows) {
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t0 >= total) return;
+  const Scales sc = make_scales(gs_ptr);
+  if (ld == bpr * 16) {  // contiguous rows: one flat index
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    uint2* qv = reinterpret_cast<uint2*>(q);
+    int64_t b = total - 1 - t0;
+    for (; b - stride >= 0; b -= 2 * stride) {
+      const int64_t b2 = b - stride;
+      const uint4 a0 = __ldcs(xv + 2 * b), a1 = __ldcs(xv + 2 * b + 1);
+      const uint4 c0 = __ldcs(xv + 2 * b2), c1 = __ldcs(xv + 2 * b2 + 1);
+      uint32_t s0, s1;
+      uint2 k0, k1;
+      quantize_block(a0, a1, sc, s0, k0);
+      quantize_block(c0, c1, sc, s1, k1);
+      __stcs(qv + b, k0);
+      __stcs(qv + b2, k1);
+      sf[b] = static_cast<uint8_t>(s0);
+      sf[b2] = static_cast<uint8_t>(s1);
+    }
+    if (b >= 0) {
+      uint32_t s0;
+      uint2 k0;
+      quantize_block(__ldcs(xv + 2 * b), __ldcs(xv + 2 * b + 1), sc, s0, k0);
+      __stcs(qv + b, k0);
+      sf[b] = static_cast<uint8_t>(s0);
+    }
+    return;
+  }
+  const int64_t b0 = total - 1 - t0;
+  int64_t r = b0 / bpr, c = b0 % bpr;
+  const int64_t sr = stride / bpr, scol = stride % bpr;
+  while (r >= 0) {
     const uint16_t* src = x + r * ld + c * 16;
-    const uint4 a = ld_stream(src);
-    const uint4 b = ld_stream(src + 8);
     uint32_t sbyte;
     uint2 codes;
-    quantize_block(a, b, gs, sbyte, codes);
+    quantize_block(ld_stream(src), ld_stream(src + 8), sc, sbyte, codes);
     *reinterpret_cast<uint2*>(q + r * (bpr * 8) + c * 8) = codes;
     sf[r * bpr + c] = static_cast<uint8_t>(sbyte);
-    c += sc;
-    r += sr;
-    if (c >= bpr) {
-      c -= bpr;
-      ++r;
+    c -= scol;
+    r -= sr;
+    if (c < 0) {
+      c += bpr;
+      --r;
     }
   }
 }
@@ -245,25 +283,27 @@ __device__ __forceinline__ void split_gate_up(const uint32_t (&w)[16], uint32_t 
   }
 }
 
+// Same visiting order as quantize_kernel (from the end backwards, streaming).
 template <int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     deinterleave_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t inter,
                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                  const float* __restrict__ gs_ptr) {
   const int64_t cpr = inter / 16;  // 32-element input chunks per row
   const int64_t total = rows * cpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const float gs = __ldg(gs_ptr);
-  int64_t r = i / cpr, c = i % cpr;
-  const int64_t sr = stride / cpr, sc = stride % cpr;
-  while (r < rows) {
-    const uint16_t* src = x + r * (2 * inter) + c * 32;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t0 >= total) return;
+  const Scales sc = make_scales(gs_ptr);
+  const int64_t b0 = total - 1 - t0;
+  int64_t r = b0 / cpr, c = b0 % cpr;
+  const int64_t sr = stride / cpr, scol = stride % cpr;
+  while (r >= 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + r * (2 * inter) + c * 32);
     uint32_t w[16];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const uint4 t = ld_stream(src + 8 * v);
+      const uint4 t = __ldcs(src + v);
       w[4 * v] = t.x;
       w[4 * v + 1] = t.y;
       w[4 * v + 2] = t.z;
@@ -273,21 +313,21 @@ __global__ void __launch_bounds__(kThreads)
     split_gate_up<G>(w, g, u);
     uint32_t sg, su;
     uint2 cg, cu;
-    quantize_block(make_uint4(g[0], g[1], g[2], g[3]), make_uint4(g[4], g[5], g[6], g[7]), gs, sg,
+    quantize_block(make_uint4(g[0], g[1], g[2], g[3]), make_uint4(g[4], g[5], g[6], g[7]), sc, sg,
                    cg);
-    quantize_block(make_uint4(u[0], u[1], u[2], u[3]), make_uint4(u[4], u[5], u[6], u[7]), gs, su,
+    quantize_block(make_uint4(u[0], u[1], u[2], u[3]), make_uint4(u[4], u[5], u[6], u[7]), sc, su,
                    cu);
     uint8_t* qrow = q + r * inter;  // 2*inter codes -> inter bytes per row
-    *reinterpret_cast<uint2*>(qrow + c * 8) = cg;
-    *reinterpret_cast<uint2*>(qrow + inter / 2 + c * 8) = cu;
+    __stcs(reinterpret_cast<uint2*>(qrow + c * 8), cg);
+    __stcs(reinterpret_cast<uint2*>(qrow + inter / 2 + c * 8), cu);
     uint8_t* srow = sf + r * (inter / 8);
     srow[c] = static_cast<uint8_t>(sg);
     srow[inter / 16 + c] = static_cast<uint8_t>(su);
-    c += sc;
-    r += sr;
-    if (c >= cpr) {
-      c -= cpr;
-      ++r;
+    c -= scol;
+    r -= sr;
+    if (c < 0) {
+      c += cpr;
+      --r;
     }
   }
 }
@@ -304,7 +344,7 @@ int grid_for(int64_t work_items, int blocks_per_sm) {
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
                         Workspace* ws, cudaStream_t stream) {
   const int64_t vpr = cols / 8;
-  const int grid = grid_for(rows * vpr, 8);
+  const int grid = grid_for((rows * vpr + kAmaxUnroll - 1) / kAmaxUnroll, 4);
   amax_kernel<<<grid, kThreads, 0, stream>>>(x, rows, vpr, ld, gs, ws);
   return cudaGetLastError();
 }
@@ -313,7 +353,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
                             uint8_t* sf, const float* gs, cudaStream_t stream) {
   const int64_t bpr = cols / 16;
   if (rows * bpr == 0) return cudaSuccess;
-  const int grid = grid_for(rows * bpr, 8);
+  const int grid = grid_for((rows * bpr + 1) / 2, 4);
   quantize_kernel<<<grid, kThreads, 0, stream>>>(x, rows, bpr, ld, q, sf, gs);
   return cudaGetLastError();
 }
@@ -323,7 +363,7 @@ cudaError_t launch_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_
                                          cudaStream_t stream) {
   const int64_t items = rows * (inter / 16);
   if (items == 0) return cudaSuccess;
-  const int grid = grid_for(items, 8);
+  const int grid = grid_for(items, 4);
   switch (g) {
     case 1: deinterleave_quantize_kernel<1><<<grid, kThreads, 0, stream>>>(x, rows, inter, q, sf, gs); break;
     case 2: deinterleave_quantize_kernel<2><<<grid, kThreads, 0, stream>>>(x, rows, inter, q, sf, gs); break;

@@ -91,6 +91,14 @@ def test_quantize_edge_values(nv, ws):
     assert_quant_equal(gpu_quantize(nv, ws, z), oracle.quantize(z), "all zero")
 
 
+def test_quantize_signed_zero_inputs(nv, ws):
+    # -0.0 and +0.0 inputs next to normal values: codes 0x8 and 0x0
+    x = workloads.quantize_input(8, seed=31, cols=512)
+    x[:, ::7] = 0x8000
+    x[:, 3::11] = 0x0000
+    assert_quant_equal(gpu_quantize(nv, ws, x), oracle.quantize(x), "signed zeros")
+
+
 def test_quantize_midpoint_quotients(nv, ws):
     # Blocks whose quotients x/den sit exactly on E2M1 rounding midpoints
     # (gs = 1 from a 2688 entry, block max 6 * 2^e so den = 2^e).
