@@ -306,7 +306,11 @@ def load_traffic(kernel_file: str, workload: str):
 
 
 def flush_l2(buf):
-    buf.zero_()
+    """Evict L2: write one buffer larger than L2, then read another, so the
+    timed call starts with clean (not dirty) lines of unrelated data."""
+    half = buf.numel() // 2
+    buf[:half].zero_()
+    buf[half:].max()
 
 
 def time_op_flushed(fn, iters, flush):
@@ -466,7 +470,7 @@ def run_gpu(args, rank, world, local):
     status = nv.read_device_status(ws)
     detail = None
     if not args.quick and rank == 0:
-        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+        flush = torch.zeros(4 * L2_BYTES, dtype=torch.uint8, device="cuda")
         detail = secondary(nv, ws, pk, flush)
         del flush
     clocks = clk.summary(t0, t1)
@@ -533,8 +537,9 @@ def run_profile(kind: str, iters: int):
             nv.nvfp4_quantize(x, qa, sfa, gsa, ws)
             nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, bias, TOPK, *out, None, ws)
         fns = [f]
-    elif kind == "quantize":
-        x = torch.from_numpy(workloads.quantize_input(16384).view(np.int16)).cuda()
+    elif kind in ("quantize", "quantize2048"):
+        x = torch.from_numpy(workloads.quantize_input(16384 if kind == "quantize" else 2048)
+                             .view(np.int16)).cuda()
         q, sf, gs = nv.quantize(x, ws)
         fns = [lambda: nv.nvfp4_quantize(x, q, sf, gs, ws)]
     elif kind == "indexer":
@@ -566,7 +571,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--tokens", type=int, default=32, choices=(1, 32))
     ap.add_argument("--quick", action="store_true", help="skip the secondary per-config figures")
-    ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "indexer"),
+    ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "quantize2048", "indexer"),
                     help="run --warmup eager iterations of one workload in an NVTX range and exit")
     args = ap.parse_args()
     if args.profile:

@@ -123,7 +123,8 @@ struct Params {
   uint32_t region_bytes;  // pipeline ring, reused after the main loop (1 KB multiple)
   int direct;             // direct epilogue (k_split == 1, k <= 32)
   int ro;                 // rows of a tile owned by each CTA of the cluster
-  int rst;                // reduce path: row stride of the pushed partials (ro | 1)
+  int bulk;               // reduce path: rows arrive by bulk copy in a receive area beside the ring
+  uint32_t recv_bytes;    // reduce path, bulk: bytes of that receive area (at the start of rowmem)
   int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 256)
   int sel_warps;          // warps that own a key buffer in the large path
   int cand_cap;           // large path: power of two >= k
@@ -249,16 +250,17 @@ __device__ __forceinline__ void list_store(const Params& p, int64_t grow, const 
 // ---------------------------------------------------------------- reduce-path rows
 
 struct RowCtx {
-  const float* recv;  // pushed partials of this CTA's rows: [k_split][N][rst]
-  int rst;
+  const float* recv;  // partial sums of this CTA's rows: [k_split][ro][rs] (row-major)
+  int ro;             // rows owned per CTA
+  int rs;             // floats per received row (n_split * BN; column n at offset n)
   int k_split;
   float gab;
 };
 
 // Logit of owned row rr, column n: the K slices' partial sums in slice order.
-__device__ __forceinline__ float row_logit(const Params& p, const RowCtx& c, int rr, int n) {
+__device__ __forceinline__ float row_logit(const RowCtx& c, int rr, int n) {
   float acc = 0.0f;
-  for (int ks = 0; ks < c.k_split; ++ks) acc += c.recv[(static_cast<int64_t>(ks) * p.N + n) * c.rst + rr];
+  for (int ks = 0; ks < c.k_split; ++ks) acc += c.recv[(ks * c.ro + rr) * c.rs + n];
   return acc * c.gab;
 }
 
@@ -301,15 +303,33 @@ __device__ __forceinline__ void warp_top8(uint64_t (&v)[8]) {
 // k <= 32, N <= 256: columns lane + 32 i in registers.
 __device__ void row_small(const Params& p, const RowCtx& c, int rr, int64_t grow) {
   const uint32_t lane = lane_id();
+  const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
+  // Biases first (independent global loads), then the K slices summed with
+  // the 8 columns as the inner loop so the shared-memory loads overlap.
+  float b[kSmallCols], acc[kSmallCols];
+#pragma unroll
+  for (int i = 0; i < kSmallCols; ++i) {
+    const int n = static_cast<int>(lane) + 32 * i;
+    b[i] = (router && n < p.N) ? __ldg(p.bias + n) : 0.0f;
+    acc[i] = 0.0f;
+  }
+  for (int ks = 0; ks < c.k_split; ++ks) {
+    const float* rowp = c.recv + (ks * c.ro + rr) * c.rs;
+#pragma unroll
+    for (int i = 0; i < kSmallCols; ++i) {
+      const int n = static_cast<int>(lane) + 32 * i;
+      if (n < p.N) acc[i] += rowp[n];
+    }
+  }
   uint64_t e[kSmallCols];
 #pragma unroll
   for (int i = 0; i < kSmallCols; ++i) {
     const int n = static_cast<int>(lane) + 32 * i;
     e[i] = 0ull;
     if (n < p.N) {
-      const float z = row_logit(p, c, rr, n);
+      const float z = acc[i] * c.gab;
       if (p.logits != nullptr) p.logits[grow * p.N + n] = z;
-      e[i] = entry(score_of(p, z, n), n);
+      e[i] = entry(router ? router_weight(z) + b[i] : z, n);
     }
   }
   const int want = p.k < p.N ? p.k : p.N;
@@ -341,7 +361,7 @@ __device__ void row_small(const Params& p, const RowCtx& c, int rr, int64_t grow
       const int n = entry_col(mine);
       p.topk_idx[o] = n;
       p.topk_score[o] = entry_score(mine);
-      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(p, c, rr, n));
+      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(c, rr, n));
     } else {
       p.topk_idx[o] = -1;
       p.topk_score[o] = -__int_as_float(0x7F800000);
@@ -358,7 +378,7 @@ __device__ void row_large(const Params& p, const RowCtx& c, int rr, int64_t grow
   const uint32_t lane = lane_id();
   const int n_all = p.N;
   for (int n = lane; n < n_all; n += 32) {
-    const float z = row_logit(p, c, rr, n);
+    const float z = row_logit(c, rr, n);
     if (p.logits != nullptr) p.logits[grow * n_all + n] = z;
     keys[n] = float_key(score_of(p, z, n));
   }
@@ -460,7 +480,7 @@ __device__ void row_large(const Params& p, const RowCtx& c, int rr, int64_t grow
       const int n = entry_col(v);
       p.topk_idx[o] = n;
       p.topk_score[o] = entry_score(v);
-      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(p, c, rr, n));
+      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(c, rr, n));
     } else {
       p.topk_idx[o] = -1;
       p.topk_score[o] = -__int_as_float(0x7F800000);
@@ -519,8 +539,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(smem_addr(&bars[3 * kMaxStages + 2]), 1);  // rows received by bulk copy
     *abort = 0u;
     fence_mbar_init();
+    if (p.bulk) {
+      // Bytes this CTA will receive: each K slice's partials of its own rows,
+      // every column slice padded to 4 floats.
+      const int owned = max(0, min(p.ro, vr - rank * p.ro));
+      uint32_t per_row = 0;
+      for (int ni = 0; ni < p.n_split; ++ni) per_row += ((min(BN, p.N - ni * BN) + 3) & ~3) * 4;
+      mbar_arrive_expect_tx(smem_addr(&bars[3 * kMaxStages + 2]),
+                            per_row * static_cast<uint32_t>(owned * p.k_split));
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -536,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.bulk) cluster_sync();  // peers' receive barriers exist before any copy targets them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool acc_ready = false;  // epilogue warps: the accumulator is complete
@@ -774,35 +805,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ reduce epilogue
-    tc_fence_before();
-    cluster_sync();  // every main loop in the cluster is over: stage regions take pushes
-    tc_fence_after();
-    if (warp >= 2 && acc_ready) {  // warp-uniform: tcgen05.ld is warp-collective
-      const bool live = row < vr;
-      const int owner = live ? row / p.ro : 0;
-      const uint32_t base = mapa_shared(sbase, static_cast<uint32_t>(owner)) +
-                            static_cast<uint32_t>(live ? row - owner * p.ro : 0) * 4u;
-      for (int c0 = 0; c0 < mma_n; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
-        tmem_wait_ld();
-        if (live) {
+    const int rs = p.n_split * BN;  // floats per received row
+    if (p.bulk) {
+      // Stage this CTA's tile row-major (stride BN + 4 floats: 16-byte rows,
+      // conflict-free vector stores) in its own stage region, then send each
+      // row to its owner with one bulk copy counted on the owner's barrier.
+      if (warp >= 2) {
+        if (acc_ready && quarter * 32 < vr) {  // warp-uniform (tcgen05.ld is collective)
+          for (int c0 = 0; c0 < mma_n; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+            tmem_wait_ld();
+            if (row < vr) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (c0 + j < ncols) {
-              const int64_t slot = (static_cast<int64_t>(k_idx) * p.N + n0 + c0 + j) * p.rst;
-              st_cluster_f32(base + static_cast<uint32_t>(slot * 4), __uint_as_float(v[j]));
+              for (int q4 = 0; q4 < 8; ++q4)
+                st_shared_v4(sbase + static_cast<uint32_t>((row * (BN + 4) + c0 + 4 * q4) * 4),
+                             v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
             }
+          }
+          fence_proxy_async_smem();  // staged rows are read by the async (bulk copy) proxy
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        if (warp == 2 && acc_ready) {
+          const uint32_t bytes = static_cast<uint32_t>(((ncols + 3) & ~3) * 4);
+          const uint32_t recv_local = smem_addr(rowmem);
+          const uint32_t bar_local = smem_addr(&bars[3 * kMaxStages + 2]);
+          for (int r = lane; r < vr; r += 32) {
+            const int o = r / p.ro;
+            const int rr = r - o * p.ro;
+            bulk_copy_to_peer(
+                mapa_shared(recv_local, static_cast<uint32_t>(o)) +
+                    static_cast<uint32_t>(((k_idx * p.ro + rr) * rs + n0) * 4),
+                sbase + static_cast<uint32_t>(r * (BN + 4) * 4), bytes,
+                mapa_shared(bar_local, static_cast<uint32_t>(o)));
+          }
+          bulk_commit();
+          bulk_wait_read();
+        }
+      }
+      if (!warp_wait(smem_addr(&bars[3 * kMaxStages + 2]), 0, abort) && lane == 0)
+        record_timeout(p.status, abort);
+    } else {
+      // Receive area too large to sit beside the pipeline: it reuses the stage
+      // region, so every main loop must be over before anything is sent.
+      tc_fence_before();
+      cluster_sync();
+      tc_fence_after();
+      if (warp >= 2 && acc_ready) {  // warp-uniform: tcgen05.ld is warp-collective
+        const bool live = row < vr;
+        const int owner = live ? row / p.ro : 0;
+        const uint32_t base =
+            mapa_shared(sbase, static_cast<uint32_t>(owner)) +
+            static_cast<uint32_t>(((k_idx * p.ro + (live ? row - owner * p.ro : 0)) * rs + n0) * 4);
+        for (int c0 = 0; c0 < mma_n; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+          tmem_wait_ld();
+          if (live) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < ncols) st_cluster_f32(base + static_cast<uint32_t>((c0 + j) * 4), __uint_as_float(v[j]));
           }
         }
       }
+      tc_fence_before();
+      cluster_sync();  // all partial sums of this CTA's rows have arrived
+      tc_fence_after();
     }
-    tc_fence_before();
-    cluster_sync();  // all partial sums of this CTA's rows have arrived
-    tc_fence_after();
     RowCtx c;
-    c.recv = reinterpret_cast<const float*>(smem);
-    c.rst = p.rst;
+    c.recv = reinterpret_cast<const float*>(p.bulk ? rowmem : smem);
+    c.ro = p.ro;
+    c.rs = rs;
     c.k_split = p.k_split;
     c.gab = gab;
     const int r0 = rank * p.ro;
@@ -810,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!p.large) {
       for (int rr = warp; rr < owned; rr += kWarps) row_small(p, c, rr, m0 + r0 + rr);
     } else if (warp < p.sel_warps) {
-      uint8_t* mine = rowmem + warp * (p.row_bytes + 1024 + p.cand_cap * 8);
+      uint8_t* mine = rowmem + p.recv_bytes + warp * (p.row_bytes + 1024 + p.cand_cap * 8);
       uint32_t* keys = reinterpret_cast<uint32_t*>(mine);
       uint32_t* hist = reinterpret_cast<uint32_t*>(mine + p.row_bytes);
       uint64_t* cand = reinterpret_cast<uint64_t*>(mine + p.row_bytes + 1024);
@@ -870,7 +943,8 @@ struct Plan {
   int bn, kmax;
   int n_split, k_split;
   int stages;
-  int direct, ro, rst;
+  int direct, ro, bulk;
+  uint32_t recv_bytes;
   int large, sel_warps, cand_cap;
   uint32_t row_bytes;
   uint32_t region;
@@ -905,7 +979,6 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   const int csize = pl.n_split * pl.k_split;
   const int vr_max = static_cast<int>(M < BM ? M : BM);
   pl.ro = (vr_max + csize - 1) / csize;
-  pl.rst = pl.ro | 1;
   pl.direct = (pl.k_split == 1 && k <= 32) ? 1 : 0;
   pl.kmax = k <= 8 ? 8 : (k <= 16 ? 16 : 32);
   pl.large = (!pl.direct && (k > 32 || N > 32 * kSmallCols)) ? 1 : 0;
@@ -913,25 +986,36 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   pl.row_bytes = pl.large ? static_cast<uint32_t>((N * 4 + 15) & ~15) : 0u;
   const int nk_max = (kt + pl.k_split - 1) / pl.k_split;
   const uint32_t sb = pl.bn == 128 ? Layout<128>::kStage : Layout<256>::kStage;
-  // Stage region reuse after the main loop: the direct epilogue's bias
-  // copies, or the reduce epilogue's pushed partial sums.
-  const uint32_t reuse = pl.direct ? 4u * static_cast<uint32_t>(pl.bn) * 4u
-                                   : static_cast<uint32_t>(pl.k_split) * static_cast<uint32_t>(N) *
-                                         static_cast<uint32_t>(pl.rst) * 4u;
+  const uint32_t recv = static_cast<uint32_t>(pl.k_split) * static_cast<uint32_t>(pl.ro) *
+                        static_cast<uint32_t>(pl.n_split * pl.bn) * 4u;
+  const uint32_t staging = static_cast<uint32_t>(vr_max) * static_cast<uint32_t>(pl.bn + 4) * 4u;
   pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
   pl.sel_warps = pl.large ? kWarps : 0;
+  // After the main loop the stage region holds the direct epilogue's bias
+  // copies, or the reduce epilogue's staged tile (bulk) / received partials.
   auto total = [&]() {
+    const uint32_t reuse = pl.direct ? 4u * static_cast<uint32_t>(pl.bn) * 4u
+                                     : (pl.bulk ? staging : recv);
     uint32_t region = pl.stages * sb > reuse ? pl.stages * sb : reuse;
     region = (region + 1023u) & ~1023u;
     pl.region = region;
-    size_t extra = 0;
+    pl.recv_bytes = (!pl.direct && pl.bulk) ? recv : 0u;
+    size_t extra = pl.recv_bytes;
     if (pl.direct && pl.n_split > 1)
       extra = static_cast<size_t>(pl.n_split) * pl.ro * pl.kmax * 16;  // merged per-row lists
     if (pl.large)
-      extra = static_cast<size_t>(pl.sel_warps) *
-              (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8);
+      extra += static_cast<size_t>(pl.sel_warps) *
+               (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8);
     return 1024 + static_cast<size_t>(region) + kCtrlBytes + extra;
   };
+  pl.bulk = pl.direct ? 0 : 1;
+  while (pl.bulk && total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
+  while (pl.bulk && total() > static_cast<size_t>(smem_optin) && pl.sel_warps > 3) --pl.sel_warps;
+  if (pl.bulk && total() > static_cast<size_t>(smem_optin)) {  // receive in the stage region
+    pl.bulk = 0;
+    pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
+    pl.sel_warps = pl.large ? kWarps : 0;
+  }
   while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
   while (total() > static_cast<size_t>(smem_optin) && pl.sel_warps > 1) --pl.sel_warps;
   pl.smem = total();
@@ -1106,7 +1190,8 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.region_bytes = pl.region;
   p.direct = pl.direct;
   p.ro = pl.ro;
-  p.rst = pl.rst;
+  p.bulk = pl.bulk;
+  p.recv_bytes = pl.recv_bytes;
   p.large = pl.large;
   p.sel_warps = pl.sel_warps;
   p.cand_cap = pl.cand_cap;

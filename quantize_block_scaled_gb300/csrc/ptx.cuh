@@ -124,6 +124,27 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
+// Bulk copy of `bytes` (16-byte multiple) from this CTA's shared memory to a
+// cluster peer's shared memory; completion is counted, in bytes, on the
+// peer's mbarrier.  dst and bar are shared::cluster addresses (mapa).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until the bulk copies this thread committed have finished reading their source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // All threads of all CTAs of the cluster: release our shared-memory writes,
 // wait for everyone, acquire theirs.
 __device__ __forceinline__ void cluster_sync() {
