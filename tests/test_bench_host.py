@@ -1,0 +1,78 @@
+"""Host-side logic of bench.py that needs no GPU.
+
+* The replica aggregation (barrier, max over ranks, whole-job throughput) on
+  two gloo ranks on the CPU, as torchrun would launch them.
+* The clock-sample summary (throttle reasons, window selection).
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    r, w, local = bench.dist_setup(world)
+    assert (r, w, local) == (rank, world, rank)
+    bench.barrier(w)
+    secs = 1.0 + rank  # rank 1 is the slow one
+    slowest = bench.reduce_max(secs, w)
+    out[rank] = (slowest, bench.throughput(32, 100, slowest, w))
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for r in range(2):
+        slowest, value = out[r]
+        assert slowest == 2.0                      # max over ranks
+        assert value == pytest.approx(32 * 100 * 2 / 2.0)  # rows of all ranks / slowest time
+
+
+def test_single_process_is_identity():
+    assert bench.reduce_max(3.5, 1) == 3.5
+    assert bench.throughput(32, 10, 2.0, 1) == 160.0
+
+
+def test_clock_summary_window_and_reasons():
+    c = bench.ClockSampler(0)
+    c.samples = [
+        dict(t=1.0, sm=2070.0, sm_max=2070.0, reasons="0x0", hw="Not Active", hwt="Not Active",
+             swt="Not Active", pcap="Not Active"),
+        dict(t=2.0, sm=1980.0, sm_max=2070.0, reasons="0x4", hw="Not Active", hwt="Not Active",
+             swt="Not Active", pcap="Active"),
+        dict(t=9.0, sm=900.0, sm_max=2070.0, reasons="0x8", hw="Active", hwt="Not Active",
+             swt="Not Active", pcap="Not Active"),
+    ]
+    s = c.summary(0.5, 2.5)
+    assert s["window"] == "timed" and s["samples"] == 2
+    assert s["sm_mhz"] == 2025.0 and s["reasons"] == ["sw_power_cap"]
+    s = c.summary(3.0, 4.0)  # nothing inside: falls back to the whole run
+    assert s["window"] == "run" and "hw_slowdown" in s["reasons"]
+
+
+def test_algorithmic_bytes():
+    # one row of 7168: 14336 bytes read, 3584 + 448 written (+ 4 for gs)
+    assert bench.quantize_bytes(1, 7168) == 14336 + 3584 + 448 + 4
+    # router decode T=32: A and B codes + scales, gs, bias, top-8 outputs
+    assert bench.gemm_bytes(32, 256, 7168, 8) == (32 + 256) * 4032 + 8 + 1024 + 32 * 8 * 12
