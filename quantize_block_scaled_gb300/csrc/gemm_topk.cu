@@ -125,6 +125,7 @@ struct Params {
   int ro;                 // rows of a tile owned by each CTA of the cluster
   int bulk;               // reduce path: rows arrive by bulk copy in a receive area beside the ring
   uint32_t recv_bytes;    // reduce path, bulk: bytes of that receive area (at the start of rowmem)
+  uint32_t bias_off;      // reduce path: offset in rowmem of the staged biases (N floats)
   int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 256)
   int sel_warps;          // warps that own a key buffer in the large path
   int cand_cap;           // large path: power of two >= k
@@ -250,7 +251,8 @@ __device__ __forceinline__ void list_store(const Params& p, int64_t grow, const 
 // ---------------------------------------------------------------- reduce-path rows
 
 struct RowCtx {
-  const float* recv;  // partial sums of this CTA's rows: [k_split][ro][rs] (row-major)
+  float* recv;        // partial sums of this CTA's rows: [k_split][ro][rs] (row-major)
+  const float* bias;  // router epilogue: all N biases, staged in shared memory
   int ro;             // rows owned per CTA
   int rs;             // floats per received row (n_split * BN; column n at offset n)
   int k_split;
@@ -300,72 +302,153 @@ __device__ __forceinline__ void warp_top8(uint64_t (&v)[8]) {
   }
 }
 
-// k <= 32, N <= 256: columns lane + 32 i in registers.
-__device__ void row_small(const Params& p, const RowCtx& c, int rr, int64_t grow) {
+__device__ __forceinline__ void ce32(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b), lo = min(a, b);
+  a = hi;
+  b = lo;
+}
+
+// warp_top8 on 32-bit keys.
+__device__ __forceinline__ void warp_top8_u32(uint32_t (&v)[8]) {
+  ce32(v[0], v[1]); ce32(v[2], v[3]); ce32(v[4], v[5]); ce32(v[6], v[7]);
+  ce32(v[0], v[2]); ce32(v[1], v[3]); ce32(v[4], v[6]); ce32(v[5], v[7]);
+  ce32(v[1], v[2]); ce32(v[5], v[6]);
+  ce32(v[0], v[4]); ce32(v[1], v[5]); ce32(v[2], v[6]); ce32(v[3], v[7]);
+  ce32(v[2], v[4]); ce32(v[3], v[5]);
+  ce32(v[1], v[2]); ce32(v[3], v[4]); ce32(v[5], v[6]);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = max(v[i], w[7 - i]);
+    ce32(v[0], v[4]); ce32(v[1], v[5]); ce32(v[2], v[6]); ce32(v[3], v[7]);
+    ce32(v[0], v[2]); ce32(v[1], v[3]); ce32(v[4], v[6]); ce32(v[5], v[7]);
+    ce32(v[0], v[1]); ce32(v[2], v[3]); ce32(v[4], v[5]); ce32(v[6], v[7]);
+  }
+}
+
+// Reduce path with k <= 32 and N <= 256, where the K split is at least 2.
+// Step 1, every thread of the CTA: sum the K slices of each (owned row,
+// 4-column group) in slice order, apply the epilogue, and leave the score in
+// slice 0 and the unbiased weight in slice 1 of the receive area (each cell
+// is read and rewritten by the one thread that owns it).  Step 2, one warp
+// per row: columns lane + 32 i, top-k selection, outputs.
+__device__ void rows_small(const Params& p, const RowCtx& c, int owned, int64_t grow0) {
   const uint32_t lane = lane_id();
+  const int warp = static_cast<int>(threadIdx.x >> 5);
   const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
-  // Biases first (independent global loads), then the K slices summed with
-  // the 8 columns as the inner loop so the shared-memory loads overlap.
-  float b[kSmallCols], acc[kSmallCols];
-#pragma unroll
-  for (int i = 0; i < kSmallCols; ++i) {
-    const int n = static_cast<int>(lane) + 32 * i;
-    b[i] = (router && n < p.N) ? __ldg(p.bias + n) : 0.0f;
-    acc[i] = 0.0f;
-  }
-  for (int ks = 0; ks < c.k_split; ++ks) {
-    const float* rowp = c.recv + (ks * c.ro + rr) * c.rs;
-#pragma unroll
-    for (int i = 0; i < kSmallCols; ++i) {
-      const int n = static_cast<int>(lane) + 32 * i;
-      if (n < p.N) acc[i] += rowp[n];
+  const int slice = c.ro * c.rs;  // floats per K slice
+  const int groups = (p.N + 3) >> 2;
+  for (int it = static_cast<int>(threadIdx.x); it < owned * groups; it += kThreads) {
+    const int rr = it / groups;
+    const int n0 = 4 * (it - rr * groups);
+    float* cell = c.recv + rr * c.rs + n0;
+    float4 a = *reinterpret_cast<const float4*>(cell);
+#pragma unroll 8
+    for (int ks = 1; ks < c.k_split; ++ks) {
+      const float4 v = *reinterpret_cast<const float4*>(cell + ks * slice);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
     }
-  }
-  uint64_t e[kSmallCols];
+    float sv[4], wv[4];
 #pragma unroll
-  for (int i = 0; i < kSmallCols; ++i) {
-    const int n = static_cast<int>(lane) + 32 * i;
-    e[i] = 0ull;
-    if (n < p.N) {
-      const float z = acc[i] * c.gab;
-      if (p.logits != nullptr) p.logits[grow * p.N + n] = z;
-      e[i] = entry(router ? router_weight(z) + b[i] : z, n);
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + j;
+      const float z = (j == 0 ? a.x : j == 1 ? a.y : j == 2 ? a.z : a.w) * c.gab;
+      wv[j] = router ? router_weight(z) : z;
+      sv[j] = n < p.N ? (router ? wv[j] + c.bias[n] : z) : -__int_as_float(0x7F800000);
+      if (p.logits != nullptr && n < p.N) p.logits[(grow0 + rr) * p.N + n] = z;
     }
+    *reinterpret_cast<float4*>(cell) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+    *reinterpret_cast<float4*>(cell + slice) = make_float4(wv[0], wv[1], wv[2], wv[3]);
   }
+  __syncthreads();
   const int want = p.k < p.N ? p.k : p.N;
-  uint64_t mine = 0ull;
-  if (p.k <= 8) {
-    warp_top8(e);
+  for (int rr = warp; rr < owned; rr += kWarps) {
+    const float* S = c.recv + rr * c.rs;
+    const float* W = S + slice;
+    const int64_t grow = grow0 + rr;
+    uint64_t mine = 0ull;  // this lane's output slot: (score key, column) entry
+    float mine_w = 0.0f;
+    if (p.k <= 8) {
+      // Selection on 32-bit keys: the score key's top 24 bits and 255 - column.
+      // Exact ties still go to the lower column; scores closer than 2^-15
+      // relative may trade places at the boundary (a near-tie).
+      uint32_t e[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (static_cast<int>(lane) == i) mine = e[i];
-  } else {
-    for (int t = 0; t < want; ++t) {  // k rounds of a warp arg-max
-      uint64_t best = e[0];
-#pragma unroll
-      for (int i = 1; i < kSmallCols; ++i) best = e[i] > best ? e[i] : best;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
+      for (int i = 0; i < 8; ++i) {
+        const int n = static_cast<int>(lane) + 32 * i;
+        e[i] = n < p.N ? ((float_key(S[n]) & 0xFFFFFF00u) | (255u - static_cast<uint32_t>(n))) : 0u;
       }
+      warp_top8_u32(e);  // every lane now holds the same 8 picks
+      // pick lane & 7 through a select tree on its bits (a chain of equality
+      // selects is turned into an indexed local-memory load by the compiler)
+      const bool b0 = lane & 1u, b1 = lane & 2u, b2 = lane & 4u;
+      const uint32_t x0 = b0 ? e[1] : e[0], x1 = b0 ? e[3] : e[2];
+      const uint32_t x2 = b0 ? e[5] : e[4], x3 = b0 ? e[7] : e[6];
+      const uint32_t key = b2 ? (b1 ? x3 : x2) : (b1 ? x1 : x0);
+      // Exact score and weight of pick lane (lanes 0..7), then an exact
+      // bitonic sort of those eight entries across the lanes.
+      const int n = 255 - static_cast<int>(key & 0xFFu);
+      const bool has = lane < 8 && key != 0u;
+      mine = has ? entry(S[n], n) : 0ull;
+      mine_w = has ? W[n] : 0.0f;
 #pragma unroll
-      for (int i = 0; i < kSmallCols; ++i)
-        if (e[i] == best) e[i] = 0ull;
-      if (static_cast<int>(lane) == t) mine = best;
-    }
-  }
-  if (static_cast<int>(lane) < p.k) {
-    const int64_t o = grow * p.k + lane;
-    if (static_cast<int>(lane) < want) {
-      const int n = entry_col(mine);
-      p.topk_idx[o] = n;
-      p.topk_score[o] = entry_score(mine);
-      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(c, rr, n));
+      for (int size = 2; size <= 8; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+          const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, j);
+          const float other_w = __shfl_xor_sync(0xFFFFFFFFu, mine_w, j);
+          // descending overall: the lower lane of a pair keeps the larger entry
+          // in blocks sorted descending ((lane & size) == 0), the smaller otherwise
+          const bool lower = (lane & j) == 0;
+          const bool desc = (lane & size) == 0 || size == 8;
+          const bool take = desc == lower ? other > mine : other < mine;
+          if (take) {
+            mine = other;
+            mine_w = other_w;
+          }
+        }
+      }
     } else {
-      p.topk_idx[o] = -1;
-      p.topk_score[o] = -__int_as_float(0x7F800000);
-      if (p.topk_weight) p.topk_weight[o] = 0.0f;
+      uint64_t e[kSmallCols];
+#pragma unroll
+      for (int i = 0; i < kSmallCols; ++i) {
+        const int n = static_cast<int>(lane) + 32 * i;
+        e[i] = n < p.N ? entry(S[n], n) : 0ull;
+      }
+      for (int t = 0; t < want; ++t) {  // k rounds of a warp arg-max
+        uint64_t best = e[0];
+#pragma unroll
+        for (int i = 1; i < kSmallCols; ++i) best = e[i] > best ? e[i] : best;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+          best = other > best ? other : best;
+        }
+#pragma unroll
+        for (int i = 0; i < kSmallCols; ++i) e[i] = e[i] == best ? 0ull : e[i];
+        if (static_cast<int>(lane) == t) {
+          mine = best;
+          mine_w = W[entry_col(best)];
+        }
+      }
+    }
+    if (static_cast<int>(lane) < p.k) {
+      const int64_t o = grow * p.k + lane;
+      if (static_cast<int>(lane) < want) {
+        p.topk_idx[o] = entry_col(mine);
+        p.topk_score[o] = entry_score(mine);
+        if (p.topk_weight) p.topk_weight[o] = mine_w;
+      } else {
+        p.topk_idx[o] = -1;
+        p.topk_score[o] = -__int_as_float(0x7F800000);
+        if (p.topk_weight) p.topk_weight[o] = 0.0f;
+      }
     }
   }
 }
@@ -380,7 +463,7 @@ __device__ void row_large(const Params& p, const RowCtx& c, int rr, int64_t grow
   for (int n = lane; n < n_all; n += 32) {
     const float z = row_logit(c, rr, n);
     if (p.logits != nullptr) p.logits[grow * n_all + n] = z;
-    keys[n] = float_key(score_of(p, z, n));
+    keys[n] = float_key(p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) + c.bias[n] : z);
   }
   __syncwarp();
   const int want = p.k < n_all ? p.k : n_all;
@@ -542,6 +625,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&bars[3 * kMaxStages + 2]), 1);  // rows received by bulk copy
     *abort = 0u;
     fence_mbar_init();
+    if (p.tma_sf) {
+      // The first stages need no empty-slot wait: start their loads now,
+      // ahead of the TMEM allocation and the block barrier.
+      const int pre = min(S, nk);
+      const uint32_t tx = L::kA + L::kB + L::kSfaStage + L::kSfbStage;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = sbase + i * L::kStage;
+        mbar_arrive_expect_tx(full_bar(i), tx);
+        tma_load_2d(st, &tma_a, full_bar(i), (kt0 + i) * BKB, m0);
+        tma_load_2d(st + L::offB, &tma_b, full_bar(i), (kt0 + i) * BKB, n0);
+        tma_load_2d(st + L::offSfaStage, &tma_sfa, full_bar(i), (kt0 + i) * 16, m0);
+        tma_load_2d(st + L::offSfbStage, &tma_sfb, full_bar(i), (kt0 + i) * 16, n0);
+      }
+    }
     if (p.bulk) {
       // Bytes this CTA will receive: each K slice's partials of its own rows,
       // every column slice padded to 4 floats.
@@ -556,17 +653,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tma_a);
-    prefetch_tensormap(&tma_b);
-    if (p.tma_sf) {
-      prefetch_tensormap(&tma_sfa);
-      prefetch_tensormap(&tma_sfb);
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  if (p.bulk) cluster_sync();  // peers' receive barriers exist before any copy targets them
+  // Peers' receive barriers must exist before a copy targets them: arrive
+  // here, wait just before the first copy (the main loop runs in between).
+  if (p.bulk) cluster_arrive();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool acc_ready = false;  // epilogue warps: the accumulator is complete
@@ -578,8 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kk = lane & 3;
     const int rsub = lane >> 2;
     const uint32_t tx = L::kA + L::kB + (p.tma_sf ? L::kSfaStage + L::kSfbStage : 0u);
-    int last = -1;
-    for (int i = 0; i < nk; ++i) {
+    const int pre = p.tma_sf ? min(S, nk) : 0;  // stages already loaded during set-up
+    int last = pre - 1;
+    for (int i = pre; i < nk; ++i) {
       const int s = i % S;
       const uint32_t ph = (i / S) & 1;
       if (!warp_wait(empty_bar(s), ph ^ 1u, abort)) {
@@ -708,6 +800,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(sfready_bar(s));
       }
     }
+    if (!p.direct && p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
+      // The row phase reads every bias of the row: stage them while the MMAs run.
+      float* bias_s = reinterpret_cast<float*>(rowmem + p.bias_off);
+      for (int n = (warp - 2) * 32 + static_cast<int>(lane); n < p.N; n += 128) bias_s[n] = __ldg(p.bias + n);
+    }
     if (warp_wait(tfull_bar, 0, abort)) {
       acc_ready = true;
       tc_fence_after();
@@ -807,30 +904,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ reduce epilogue
     const int rs = p.n_split * BN;  // floats per received row
     if (p.bulk) {
+      cluster_wait();
       // Stage this CTA's tile row-major (stride BN + 4 floats: 16-byte rows,
       // conflict-free vector stores) in its own stage region, then send each
       // row to its owner with one bulk copy counted on the owner's barrier.
       if (warp >= 2) {
         if (acc_ready && quarter * 32 < vr) {  // warp-uniform (tcgen05.ld is collective)
-          for (int c0 = 0; c0 < mma_n; c0 += 32) {
-            uint32_t v[32];
+          for (int c0 = 0; c0 < mma_n; c0 += 64) {  // two 32-column loads in flight
+            const bool two = c0 + 32 < mma_n;       // then c0 + 64 <= BN
+            uint32_t v[32], u[32];
             tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+            if (two) tmem_ld_32x32b_x32(tmem + c0 + 32 + (static_cast<uint32_t>(quarter * 32) << 16), u);
             tmem_wait_ld();
             if (row < vr) {
+              const uint32_t dst = sbase + static_cast<uint32_t>((row * (BN + 4) + c0) * 4);
 #pragma unroll
               for (int q4 = 0; q4 < 8; ++q4)
-                st_shared_v4(sbase + static_cast<uint32_t>((row * (BN + 4) + c0 + 4 * q4) * 4),
-                             v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                st_shared_v4(dst + 16 * q4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+              if (two) {
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                  st_shared_v4(dst + 128 + 16 * q4, u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
+              }
             }
           }
           fence_proxy_async_smem();  // staged rows are read by the async (bulk copy) proxy
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
-        if (warp == 2 && acc_ready) {
+        if (acc_ready) {
           const uint32_t bytes = static_cast<uint32_t>(((ncols + 3) & ~3) * 4);
           const uint32_t recv_local = smem_addr(rowmem);
           const uint32_t bar_local = smem_addr(&bars[3 * kMaxStages + 2]);
-          for (int r = lane; r < vr; r += 32) {
+          for (int r = (warp - 2) + 4 * static_cast<int>(lane); r < vr; r += 128) {  // 4 warps share few rows
             const int o = r / p.ro;
             const int rr = r - o * p.ro;
             bulk_copy_to_peer(
@@ -872,8 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       cluster_sync();  // all partial sums of this CTA's rows have arrived
       tc_fence_after();
     }
+    __syncthreads();  // staged biases are visible to every warp of the row phase
     RowCtx c;
-    c.recv = reinterpret_cast<const float*>(p.bulk ? rowmem : smem);
+    c.recv = reinterpret_cast<float*>(p.bulk ? rowmem : smem);
+    c.bias = reinterpret_cast<const float*>(rowmem + p.bias_off);
     c.ro = p.ro;
     c.rs = rs;
     c.k_split = p.k_split;
@@ -881,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r0 = rank * p.ro;
     const int owned = min(p.ro, vr - r0);
     if (!p.large) {
-      for (int rr = warp; rr < owned; rr += kWarps) row_small(p, c, rr, m0 + r0 + rr);
+      rows_small(p, c, owned, m0 + r0);
     } else if (warp < p.sel_warps) {
       uint8_t* mine = rowmem + p.recv_bytes + warp * (p.row_bytes + 1024 + p.cand_cap * 8);
       uint32_t* keys = reinterpret_cast<uint32_t*>(mine);
@@ -944,7 +1051,7 @@ struct Plan {
   int n_split, k_split;
   int stages;
   int direct, ro, bulk;
-  uint32_t recv_bytes;
+  uint32_t recv_bytes, bias_off;
   int large, sel_warps, cand_cap;
   uint32_t row_bytes;
   uint32_t region;
@@ -1006,6 +1113,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
     if (pl.large)
       extra += static_cast<size_t>(pl.sel_warps) *
                (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8);
+    pl.bias_off = static_cast<uint32_t>(extra);
+    if (!pl.direct) extra += static_cast<size_t>((N * 4 + 15) & ~15);  // staged biases
     return 1024 + static_cast<size_t>(region) + kCtrlBytes + extra;
   };
   pl.bulk = pl.direct ? 0 : 1;
@@ -1192,6 +1301,7 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.ro = pl.ro;
   p.bulk = pl.bulk;
   p.recv_bytes = pl.recv_bytes;
+  p.bias_off = pl.bias_off;
   p.large = pl.large;
   p.sel_warps = pl.sel_warps;
   p.cand_cap = pl.cand_cap;
