@@ -153,6 +153,28 @@ int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
                     float* logits, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * nvfp4_quantize for callers that must not allocate device memory: an engine
+ * that gives all of HBM to its own arena up front, or a thread that may not
+ * call cudaMalloc/cudaFree because they can block on or synchronise the
+ * device.  The pages have no counterpart; it is the same two kernels as
+ * nvfp4_quantize with the same arguments and results, minus the workspace.
+ *
+ * Scratch: a 256-byte static device array inside the library (one per GPU
+ * that loads it, held until exit).  A call whose scratch need exceeds it
+ * returns NVFP4_ERR_WORKSPACE (today every shape needs exactly 256 bytes).
+ * Each call clears the words that must start at zero on `stream` before its
+ * kernels.  All calls on a device share the array: calls that can overlap on
+ * the GPU (different streams without ordering between them) race and give
+ * wrong results.  The first call on a device, with that device current,
+ * looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  Device status bits of these calls
+ * are not readable with nvfp4_read_device_status (the quantize kernels set
+ * none).  Allocates nothing.
+ */
+int nvfp4_quantize_noalloc(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
+                           uint8_t* q, uint8_t* sf, float* gs, cudaStream_t stream);
+
+/*
  * Diagnostic: synchronise `stream`, copy the workspace's device status bits
  * (NVFP4_DEVICE_*) to *status, and clear them.  Not for the hot path.
  */

@@ -73,13 +73,15 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_status_string.argtypes = [I]
         L.nvfp4_last_cuda_error.restype = I
         L.nvfp4_last_cuda_error.argtypes = []
+        L.nvfp4_quantize_noalloc.restype = I
+        L.nvfp4_quantize_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P]
         _lib = L
         return L
 
 
 EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
                     "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
-                    "nvfp4_status_string", "nvfp4_last_cuda_error")
+                    "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc")
 
 
 def _check(fn: str, status: int):
@@ -128,6 +130,15 @@ def nvfp4_quantize(x, q, sf, gs, ws, stream=None):
     _check("nvfp4_quantize", lib().nvfp4_quantize(
         _ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def nvfp4_quantize_noalloc(x, q, sf, gs, stream=None):
+    """nvfp4_quantize without a workspace: the library's static scratch is used
+    (for callers that cannot allocate device memory; overlapping calls race)."""
+    x = _bf16_bits(x)
+    rows, cols = x.shape
+    _check("nvfp4_quantize_noalloc", lib().nvfp4_quantize_noalloc(
+        _ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), _ptr(gs), _stream(stream)))
 
 
 def nvfp4_deinterleave_quantize(x, granularity, q, sf, gs, ws, stream=None):

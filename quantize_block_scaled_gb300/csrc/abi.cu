@@ -41,6 +41,8 @@ int sm_count() {
   return cache[dev];
 }
 
+void set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
 }  // namespace nvfp4
 
 extern "C" {

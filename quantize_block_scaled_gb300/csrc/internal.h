@@ -20,6 +20,8 @@ static_assert(sizeof(Workspace) == 256, "workspace layout");
 constexpr size_t kWorkspaceBytes = sizeof(Workspace);
 
 int sm_count();
+// Record a cudaError_t for nvfp4_last_cuda_error on this thread.
+void set_last_cuda_error(int e);
 
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
                         Workspace* ws, cudaStream_t stream);
