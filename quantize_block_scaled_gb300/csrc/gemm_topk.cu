@@ -174,17 +174,17 @@ __device__ __forceinline__ float entry_score(uint64_t e) {
 // sqrt(softplus(z)) with softplus(z) = max(z, 0) + log1p(exp(-|z|)).  For
 // u = exp(-|z|) < 2^-5 log1p(u) is taken from the first three terms of its
 // Mercator series u - u^2/2 + u^3/3 (truncation below u^4/4, relative 8e-6);
-// otherwise from the fast log of 1 + u.  Relative error ~1e-5, far inside the
-// 1e-3 the scores are held to.
+// otherwise from the fast log of 1 + u.  The square root is the hardware
+// approximation (no branch to a slow path, so columns interleave).  Relative
+// error ~1e-5, far inside the 1e-3 the scores are held to.
 __device__ __forceinline__ float router_weight(float z) {
   const float u = __expf(-fabsf(z));
   const float l = (u < 0.03125f) ? u * (1.0f - u * (0.5f - u * 0.333333343f)) : __logf(1.0f + u);
-  return sqrtf(fmaxf(z, 0.0f) + l);
+  float r;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(fmaxf(z, 0.0f) + l));
+  return r;
 }
 
-__device__ __forceinline__ float score_of(const Params& p, float z, int n) {
-  return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) + __ldg(p.bias + n) : z;
-}
 __device__ __forceinline__ float weight_of(const Params& p, float z) {
   return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) : z;
 }
@@ -266,15 +266,18 @@ __device__ __forceinline__ float row_logit(const RowCtx& c, int rr, int n) {
   return acc * c.gab;
 }
 
-__device__ __forceinline__ void ce_desc(uint64_t& a, uint64_t& b) {
-  const uint64_t hi = a > b ? a : b;
-  const uint64_t lo = a > b ? b : a;
+// Sorting networks on keys where a larger key is a better entry.
+template <typename T>
+__device__ __forceinline__ void ce_desc(T& a, T& b) {
+  const T hi = a > b ? a : b;
+  const T lo = a > b ? b : a;
   a = hi;
   b = lo;
 }
 
-// Sort 8 entries descending (Batcher's odd-even merge sort network, 19 comparators).
-__device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
+// Sort 8 keys descending (Batcher's odd-even merge sort network, 19 comparators).
+template <typename T>
+__device__ __forceinline__ void sort8_desc(T (&v)[8]) {
   ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
   ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
   ce_desc(v[1], v[2]); ce_desc(v[5], v[6]);
@@ -283,50 +286,66 @@ __device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
   ce_desc(v[1], v[2]); ce_desc(v[3], v[4]); ce_desc(v[5], v[6]);
 }
 
-// The 8 best entries of the whole warp, in every lane: each lane sorts its 8,
-// then 5 butterfly levels each keep the top 8 of two sorted lists (the
-// elementwise max against the partner's reversed list is bitonic and holds
-// them; a bitonic merge sorts it).
-__device__ __forceinline__ void warp_top8(uint64_t (&v)[8]) {
-  sort8_desc(v);
+// r := the 8 best of two descending lists r and g, descending.  The
+// elementwise max of r against g reversed is bitonic and holds them; three
+// half-cleaner levels sort it.
+template <typename T>
+__device__ __forceinline__ void merge_top8(T (&r)[8], const T (&g)[8]) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    uint64_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = v[i] > w[7 - i] ? v[i] : w[7 - i];
-    ce_desc(v[0], v[4]); ce_desc(v[1], v[5]); ce_desc(v[2], v[6]); ce_desc(v[3], v[7]);
-    ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
-    ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
-  }
+  for (int i = 0; i < 8; ++i) r[i] = r[i] > g[7 - i] ? r[i] : g[7 - i];
+  ce_desc(r[0], r[4]); ce_desc(r[1], r[5]); ce_desc(r[2], r[6]); ce_desc(r[3], r[7]);
+  ce_desc(r[0], r[2]); ce_desc(r[1], r[3]); ce_desc(r[4], r[6]); ce_desc(r[5], r[7]);
+  ce_desc(r[0], r[1]); ce_desc(r[2], r[3]); ce_desc(r[4], r[5]); ce_desc(r[6], r[7]);
 }
 
-__device__ __forceinline__ void ce32(uint32_t& a, uint32_t& b) {
-  const uint32_t hi = max(a, b), lo = min(a, b);
-  a = hi;
-  b = lo;
-}
-
-// warp_top8 on 32-bit keys.
+// The 8 best 32-bit keys of the whole warp, in every lane: each lane sorts
+// its 8, then 5 butterfly levels each keep the best 8 of two sorted lists.
 __device__ __forceinline__ void warp_top8_u32(uint32_t (&v)[8]) {
-  ce32(v[0], v[1]); ce32(v[2], v[3]); ce32(v[4], v[5]); ce32(v[6], v[7]);
-  ce32(v[0], v[2]); ce32(v[1], v[3]); ce32(v[4], v[6]); ce32(v[5], v[7]);
-  ce32(v[1], v[2]); ce32(v[5], v[6]);
-  ce32(v[0], v[4]); ce32(v[1], v[5]); ce32(v[2], v[6]); ce32(v[3], v[7]);
-  ce32(v[2], v[4]); ce32(v[3], v[5]);
-  ce32(v[1], v[2]); ce32(v[3], v[4]); ce32(v[5], v[6]);
+  sort8_desc(v);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = max(v[i], w[7 - i]);
-    ce32(v[0], v[4]); ce32(v[1], v[5]); ce32(v[2], v[6]); ce32(v[3], v[7]);
-    ce32(v[0], v[2]); ce32(v[1], v[3]); ce32(v[4], v[6]); ce32(v[5], v[7]);
-    ce32(v[0], v[1]); ce32(v[2], v[3]); ce32(v[4], v[5]); ce32(v[6], v[7]);
+    merge_top8(v, w);
   }
+}
+
+// Entries (64-bit keys) that carry a float payload through the networks.
+__device__ __forceinline__ void ce_pay(uint64_t& a, float& wa, uint64_t& b, float& wb) {
+  const bool swap = b > a;
+  const uint64_t hi = swap ? b : a, lo = swap ? a : b;
+  const float whi = swap ? wb : wa, wlo = swap ? wa : wb;
+  a = hi;
+  b = lo;
+  wa = whi;
+  wb = wlo;
+}
+__device__ __forceinline__ void sort8_pay(uint64_t (&v)[8], float (&w)[8]) {
+  ce_pay(v[0], w[0], v[1], w[1]); ce_pay(v[2], w[2], v[3], w[3]);
+  ce_pay(v[4], w[4], v[5], w[5]); ce_pay(v[6], w[6], v[7], w[7]);
+  ce_pay(v[0], w[0], v[2], w[2]); ce_pay(v[1], w[1], v[3], w[3]);
+  ce_pay(v[4], w[4], v[6], w[6]); ce_pay(v[5], w[5], v[7], w[7]);
+  ce_pay(v[1], w[1], v[2], w[2]); ce_pay(v[5], w[5], v[6], w[6]);
+  ce_pay(v[0], w[0], v[4], w[4]); ce_pay(v[1], w[1], v[5], w[5]);
+  ce_pay(v[2], w[2], v[6], w[6]); ce_pay(v[3], w[3], v[7], w[7]);
+  ce_pay(v[2], w[2], v[4], w[4]); ce_pay(v[3], w[3], v[5], w[5]);
+  ce_pay(v[1], w[1], v[2], w[2]); ce_pay(v[3], w[3], v[4], w[4]); ce_pay(v[5], w[5], v[6], w[6]);
+}
+__device__ __forceinline__ void merge_top8_pay(uint64_t (&r)[8], float (&rw)[8], const uint64_t (&g)[8],
+                                               const float (&gw)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool take = g[7 - i] > r[i];
+    r[i] = take ? g[7 - i] : r[i];
+    rw[i] = take ? gw[7 - i] : rw[i];
+  }
+  ce_pay(r[0], rw[0], r[4], rw[4]); ce_pay(r[1], rw[1], r[5], rw[5]);
+  ce_pay(r[2], rw[2], r[6], rw[6]); ce_pay(r[3], rw[3], r[7], rw[7]);
+  ce_pay(r[0], rw[0], r[2], rw[2]); ce_pay(r[1], rw[1], r[3], rw[3]);
+  ce_pay(r[4], rw[4], r[6], rw[6]); ce_pay(r[5], rw[5], r[7], rw[7]);
+  ce_pay(r[0], rw[0], r[1], rw[1]); ce_pay(r[2], rw[2], r[3], rw[3]);
+  ce_pay(r[4], rw[4], r[5], rw[5]); ce_pay(r[6], rw[6], r[7], rw[7]);
 }
 
 // Reduce path with k <= 32 and N <= 256, where the K split is at least 2.
@@ -830,30 +849,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = lane; c < ncols; c += 32) bias_s[c] = __ldg(p.bias + n0 + c);
       __syncwarp();
       const bool live = row < vr;
-      const bool full_list = p.k == KMAX;  // k-th score is simply the last slot
-      float kth = -__int_as_float(0x7F800000);
-      if (acc_ready) {
-        for (int c0 = 0; c0 < mma_n; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
-          tmem_wait_ld();
-          // Logits, then activations for the whole chunk, branch-free (ILP across columns).
-          float w[32];
+      if constexpr (KMAX == 8) {
+        // Branch-free: 32-bit keys (the score key's top 24 bits | 255 - local
+        // column), each 32-column chunk sorted in groups of 8 and merged into
+        // the running best 8.  The logits stay in shared memory (row stride
+        // BN + 4 floats) so the picks get their exact scores afterwards; keys
+        // closer than 2^-15 relative may trade places at the boundary (a
+        // near-tie), equal scores still go to the lower column.
+        float* zrow = reinterpret_cast<float*>(smem) + 4 * BN + row * (BN + 4);
+        uint32_t top[8];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float z = __uint_as_float(v[j]) * gab;
-            w[j] = router ? router_weight(z) : z;
-            if (p.logits != nullptr && live && c0 + j < ncols)
-              p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
-          }
-          if (live) {
+        for (int i = 0; i < 8; ++i) top[i] = 0u;
+        if (acc_ready) {
+          for (int c0 = 0; c0 < mma_n; c0 += 32) {
+            float b[32];  // the chunk's biases (one broadcast vector load per 4)
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 b4 = router ? *reinterpret_cast<const float4*>(bias_s + c0 + 4 * q4)
+                                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              b[4 * q4] = b4.x;
+              b[4 * q4 + 1] = b4.y;
+              b[4 * q4 + 2] = b4.z;
+              b[4 * q4 + 3] = b4.w;
+            }
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+            tmem_wait_ld();
+            uint32_t key[4][8];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (c0 + j < ncols) {
-                const float sc = router ? w[j] + bias_s[c0 + j] : w[j];
-                if (sc > kth) {
-                  list_insert<KMAX>(tv, ti, tw, sc, n0 + c0 + j, w[j]);
-                  kth = full_list ? tv[KMAX - 1] : list_kth<KMAX>(tv, p.k);
+              const float z = __uint_as_float(v[j]) * gab;
+              v[j] = __float_as_uint(z);
+              if (p.logits != nullptr && live && c0 + j < ncols)
+                p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
+              const float sc = router ? router_weight(z) + b[j] : z;
+              key[j >> 3][j & 7] = (live && c0 + j < ncols)
+                                       ? ((float_key(sc) & 0xFFFFFF00u) | (255u - static_cast<uint32_t>(c0 + j)))
+                                       : 0u;
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              sort8_desc(key[g]);
+              merge_top8(top, key[g]);
+            }
+            if (live) {
+              const uint32_t dst = smem_addr(zrow + c0);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                st_shared_v4(dst + 16 * q4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            }
+          }
+        }
+        // exact score and weight of each pick, then an exact sort (score
+        // descending, lower column first)
+        uint64_t e[8];
+        float ew[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = 255 - static_cast<int>(top[i] & 0xFFu);
+          const float z = top[i] != 0u ? zrow[c] : 0.0f;
+          const float w = router ? router_weight(z) : z;
+          const float sc = router ? w + bias_s[c] : z;
+          e[i] = top[i] != 0u ? entry(sc, n0 + c) : 0ull;
+          ew[i] = top[i] != 0u ? w : 0.0f;
+        }
+        sort8_pay(e, ew);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          tv[i] = e[i] != 0ull ? entry_score(e[i]) : -__int_as_float(0x7F800000);
+          ti[i] = e[i] != 0ull ? entry_col(e[i]) : -1;
+          tw[i] = ew[i];
+        }
+      } else {
+        const bool full_list = p.k == KMAX;  // k-th score is simply the last slot
+        float kth = -__int_as_float(0x7F800000);
+        if (acc_ready) {
+          for (int c0 = 0; c0 < mma_n; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+            tmem_wait_ld();
+            // Logits, then activations for the whole chunk, branch-free (ILP across columns).
+            float w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float z = __uint_as_float(v[j]) * gab;
+              w[j] = router ? router_weight(z) : z;
+              if (p.logits != nullptr && live && c0 + j < ncols)
+                p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
+            }
+            if (live) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (c0 + j < ncols) {
+                  const float sc = router ? w[j] + bias_s[c0 + j] : w[j];
+                  if (sc > kth) {
+                    list_insert<KMAX>(tv, ti, tw, sc, n0 + c0 + j, w[j]);
+                    kth = full_list ? tv[KMAX - 1] : list_kth<KMAX>(tv, p.k);
+                  }
                 }
               }
             }
@@ -880,7 +972,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r0 = rank * p.ro;
       const int owned = min(p.ro, vr - r0);
       const int t = static_cast<int>(threadIdx.x);
-      if (t < owned) {
+      if (KMAX == 8 && t < owned) {
+        // sorted lists of 8 entries, merged slice by slice (slices in column
+        // order; the entry order already puts the lower column first on ties)
+        const uint32_t* lists = reinterpret_cast<const uint32_t*>(rowmem);
+        uint64_t r[8], g[8];
+        float rw[8], gw[8];
+        for (int ni = 0; ni < p.n_split; ++ni) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 q = *reinterpret_cast<const uint4*>(lists + ((ni * p.ro + t) * 8 + i) * 4);
+            const int col = static_cast<int>(q.y);
+            g[i] = col >= 0 ? entry(__uint_as_float(q.x), col) : 0ull;
+            gw[i] = __uint_as_float(q.z);
+          }
+          if (ni == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              r[i] = g[i];
+              rw[i] = gw[i];
+            }
+          } else {
+            merge_top8_pay(r, rw, g, gw);
+          }
+        }
+        float tv[KMAX], tw[KMAX];
+        int ti[KMAX];
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+          tv[i] = r[i] != 0ull ? entry_score(r[i]) : -__int_as_float(0x7F800000);
+          ti[i] = r[i] != 0ull ? entry_col(r[i]) : -1;
+          tw[i] = r[i] != 0ull ? rw[i] : 0.0f;
+        }
+        list_store<KMAX>(p, m0 + r0 + t, tv, ti, tw);
+      } else if (t < owned) {
         float tv[KMAX], tw[KMAX];
         int ti[KMAX];
         list_init<KMAX>(tv, ti, tw);
@@ -1101,8 +1226,11 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   // After the main loop the stage region holds the direct epilogue's bias
   // copies, or the reduce epilogue's staged tile (bulk) / received partials.
   auto total = [&]() {
-    const uint32_t reuse = pl.direct ? 4u * static_cast<uint32_t>(pl.bn) * 4u
-                                     : (pl.bulk ? staging : recv);
+    // direct: four bias copies, and for k <= 8 the tile's logits (BM rows of BN + 4 floats)
+    const uint32_t reuse =
+        pl.direct ? 4u * static_cast<uint32_t>(pl.bn) * 4u +
+                        (pl.kmax == 8 ? static_cast<uint32_t>(BM) * static_cast<uint32_t>(pl.bn + 4) * 4u : 0u)
+                  : (pl.bulk ? staging : recv);
     uint32_t region = pl.stages * sb > reuse ? pl.stages * sb : reuse;
     region = (region + 1023u) & ~1023u;
     pl.region = region;
