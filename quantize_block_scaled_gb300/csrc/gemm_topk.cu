@@ -79,6 +79,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;  // scale factors live after the (<= 256-column) accumulator
 constexpr uint32_t kSfChunk = 512;     // scales of 128 rows for one MMA (K = 64)
 constexpr uint32_t kCtrlBytes = 256;
+// control block: 3 barriers per stage and 4 more, then the TMEM address at byte 128
+static_assert((3 * kMaxStages + 4) * 8 <= 128, "barriers precede the TMEM slot");
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
 constexpr int kSmallCols = 8;        // reduce path, small rows: <= 8 columns per lane (N <= 256)
 
@@ -615,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sfready_bar = [&](int s) { return smem_addr(&bars[2 * kMaxStages + s]); };
   const uint32_t tfull_bar = smem_addr(&bars[3 * kMaxStages]);
   const uint32_t drain_bar = smem_addr(&bars[3 * kMaxStages + 1]);
+  const uint32_t xdrain_bar = smem_addr(&bars[3 * kMaxStages + 3]);  // scale copies drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
   volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 132);
   uint8_t* rowmem = ctrl + kCtrlBytes;
@@ -641,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(xdrain_bar, kUnits);
     mbar_init(smem_addr(&bars[3 * kMaxStages + 2]), 1);  // rows received by bulk copy
     *abort = 0u;
     fence_mbar_init();
@@ -756,19 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (lane == 0) {
-        fence_proxy_async_smem();
         tc_fence_after();
         const uint32_t st = sbase + s * L::kStage;
         const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(st + L::offSfaMma + kk * kSfChunk, 0, 128, 0));
-#pragma unroll
-          for (int a = 0; a < L::kAtomsB; ++a)
-            tc_cp_32x128b_warpx4(
-                sf_col + 16 + kk * 4 * L::kAtomsB + a * 4,
-                smem_desc(st + L::offSfbMma + (kk * L::kAtomsB + a) * kSfChunk, 0, 128, 0));
-        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           tc_mma_nvf4(tmem, smem_desc(st + kk * 32, 16, 1024, 2),
@@ -816,8 +810,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfready_bar(s));
+        if (lane == 0) {
+          // This unit's scales into TMEM; the commit tells the MMA warp they
+          // are there (the copies of a stage run once the MMAs of its previous
+          // round have completed: full(s) of this round follows empty(s)).
+          fence_proxy_async_smem();  // scales written through the generic proxy (cp.async path)
+          tc_fence_after();
+          const uint32_t st = sbase + s * L::kStage;
+          const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
+          if (unit == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(st + L::offSfaMma + kk * kSfChunk, 0, 128, 0));
+          } else {
+            const int a = unit - 1;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4 * L::kAtomsB + a * 4,
+                                   smem_desc(st + L::offSfbMma + (kk * L::kAtomsB + a) * kSfChunk, 0, 128, 0));
+          }
+          tc_commit(sfready_bar(s));
+        }
+        __syncwarp();
       }
+      if (lane == 0) {  // every copy of this unit has completed before TMEM can be freed
+        uint32_t never = 0;
+        tc_commit(xdrain_bar);
+        if (!mbar_wait_bounded(xdrain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
+      }
+      __syncwarp();
     }
     if (!p.direct && p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
       // The row phase reads every bias of the row: stage them while the MMAs run.
