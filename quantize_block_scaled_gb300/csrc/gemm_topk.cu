@@ -640,11 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), p.tma_sf ? 1 : 1 + 32);  // + one cp.async arrival per producer lane
       mbar_init(empty_bar(s), 1);
-      mbar_init(sfready_bar(s), kUnits);
+      mbar_init(sfready_bar(s), 4);  // one tcgen05.commit per scale-layout warp
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
-    mbar_init(xdrain_bar, kUnits);
+    mbar_init(xdrain_bar, 4);
     mbar_init(smem_addr(&bars[3 * kMaxStages + 2]), 1);  // rows received by bulk copy
     *abort = 0u;
     fence_mbar_init();
@@ -782,64 +782,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ scale layout
-    const int unit = warp - 2;
-    if (unit < kUnits) {
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (i / S) & 1;
-        if (!warp_wait(full_bar(s), ph, abort)) {
-          if (lane == 0) record_timeout(p.status, abort);
-          break;
-        }
-        if (p.tma_sf) {
-          // Staged rows r0 + 32 r1 (r1 = 0..3) of one 128-row atom, 16 bytes
-          // (4 MMA words) each -> chunk kk gets the 16 bytes
-          // {word kk of rows r0, r0+32, r0+64, r0+96} at offset 16 * r0.
-          const uint32_t st = sbase + s * L::kStage;
-          const uint32_t src = unit == 0 ? st + L::offSfaStage : st + L::offSfbStage + (unit - 1) * 2048;
-          const uint32_t dst = unit == 0 ? st + L::offSfaMma : st + L::offSfbMma + (unit - 1) * kSfChunk;
-          const uint32_t chunk = unit == 0 ? kSfChunk : L::kAtomsB * kSfChunk;
-          uint32_t w0[4], w1[4], w2[4], w3[4];
-          ld_shared_v4(src + (0 * 32 + lane) * 16, w0);
-          ld_shared_v4(src + (1 * 32 + lane) * 16, w1);
-          ld_shared_v4(src + (2 * 32 + lane) * 16, w2);
-          ld_shared_v4(src + (3 * 32 + lane) * 16, w3);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            st_shared_v4(dst + kk * chunk + lane * 16, w0[kk], w1[kk], w2[kk], w3[kk]);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          // This unit's scales into TMEM; the commit tells the MMA warp they
-          // are there (the copies of a stage run once the MMAs of its previous
-          // round have completed: full(s) of this round follows empty(s)).
-          fence_proxy_async_smem();  // scales written through the generic proxy (cp.async path)
-          tc_fence_after();
-          const uint32_t st = sbase + s * L::kStage;
-          const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
-          if (unit == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(st + L::offSfaMma + kk * kSfChunk, 0, 128, 0));
-          } else {
-            const int a = unit - 1;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4 * L::kAtomsB + a * 4,
-                                   smem_desc(st + L::offSfbMma + (kk * L::kAtomsB + a) * kSfChunk, 0, 128, 0));
-          }
-          tc_commit(sfready_bar(s));
-        }
-        __syncwarp();
+    // Warp 2 + u owns MMA step kk = u of every 128-row scale atom (SFA, then
+    // the SFB atoms): it lays that chunk out for tcgen05.cp, copies it into
+    // TMEM and signals the stage with a tcgen05.commit.  Four warps share the
+    // copies because each tcgen05 instruction holds its issuing warp.
+    const int u = warp - 2;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S;
+      const uint32_t ph = (i / S) & 1;
+      if (!warp_wait(full_bar(s), ph, abort)) {
+        if (lane == 0) record_timeout(p.status, abort);
+        break;
       }
-      if (lane == 0) {  // every copy of this unit has completed before TMEM can be freed
-        uint32_t never = 0;
-        tc_commit(xdrain_bar);
-        if (!mbar_wait_bounded(xdrain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
+      const uint32_t st = sbase + s * L::kStage;
+      if (p.tma_sf) {
+        // Staged row r (16 bytes: MMA words 0..3) -> chunk u gets, at offset
+        // 16 * r0, word u of rows r0, r0 + 32, r0 + 64, r0 + 96.
+#pragma unroll
+        for (int a = 0; a < kUnits; ++a) {
+          const uint32_t src = a == 0 ? st + L::offSfaStage : st + L::offSfbStage + (a - 1) * 2048;
+          const uint32_t dst = a == 0 ? st + L::offSfaMma + u * kSfChunk
+                                      : st + L::offSfbMma + (u * L::kAtomsB + (a - 1)) * kSfChunk;
+          const uint32_t w0 = ld_shared_u32(src + (0 * 32 + lane) * 16 + u * 4);
+          const uint32_t w1 = ld_shared_u32(src + (1 * 32 + lane) * 16 + u * 4);
+          const uint32_t w2 = ld_shared_u32(src + (2 * 32 + lane) * 16 + u * 4);
+          const uint32_t w3 = ld_shared_u32(src + (3 * 32 + lane) * 16 + u * 4);
+          st_shared_v4(dst + lane * 16, w0, w1, w2, w3);
+        }
+        fence_proxy_async_smem();  // read by tcgen05.cp through the async proxy
+      }
+      __syncwarp();
+      if (lane == 0) {
+        // (the copies of a stage run once the MMAs of its previous round have
+        // completed: full(s) of this round follows empty(s))
+        fence_proxy_async_smem();  // scales written through the generic proxy (cp.async path)
+        tc_fence_after();
+        const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
+#pragma unroll
+        for (int a = 0; a < kUnits; ++a) {
+          if (a == 0)
+            tc_cp_32x128b_warpx4(sf_col + u * 4, smem_desc(st + L::offSfaMma + u * kSfChunk, 0, 128, 0));
+          else
+            tc_cp_32x128b_warpx4(sf_col + 16 + u * 4 * L::kAtomsB + (a - 1) * 4,
+                                 smem_desc(st + L::offSfbMma + (u * L::kAtomsB + (a - 1)) * kSfChunk, 0, 128, 0));
+        }
+        tc_commit(sfready_bar(s));
       }
       __syncwarp();
     }
+    if (lane == 0) {  // every copy of this warp has completed before TMEM can be freed
+      uint32_t never = 0;
+      tc_commit(xdrain_bar);
+      if (!mbar_wait_bounded(xdrain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
+    }
+    __syncwarp();
     if (!p.direct && p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
       // The row phase reads every bias of the row: stage them while the MMAs run.
       float* bias_s = reinterpret_cast<float*>(rowmem + p.bias_off);
