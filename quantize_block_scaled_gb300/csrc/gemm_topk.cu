@@ -128,8 +128,8 @@ struct Params {
   int bulk;               // reduce path: rows arrive by bulk copy in a receive area beside the ring
   uint32_t recv_bytes;    // reduce path, bulk: bytes of that receive area (at the start of rowmem)
   uint32_t bias_off;      // reduce path: offset in rowmem of the staged biases (N floats)
+  int rpc;                // rows per cluster tile (<= BM; smaller spreads few long rows over more clusters)
   int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 256)
-  int sel_warps;          // warps that own a key buffer in the large path
   int cand_cap;           // large path: power of two >= k
   uint32_t row_bytes;     // large path: bytes of one warp's key buffer (16-byte multiple)
 };
@@ -187,9 +187,6 @@ __device__ __forceinline__ float router_weight(float z) {
   return r;
 }
 
-__device__ __forceinline__ float weight_of(const Params& p, float z) {
-  return p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) : z;
-}
 
 // Sorted (descending) insertion into a KMAX-entry register list; equal
 // scores keep the earlier entry ahead.
@@ -474,124 +471,281 @@ __device__ void rows_small(const Params& p, const RowCtx& c, int owned, int64_t 
   }
 }
 
-// General row: keys of all N scores in shared memory, 4-pass radix select
-// of the k-th largest key, in-order compaction (keys above it, then the
-// lowest-column ties), bitonic sort of the picks, outputs.
-__device__ void row_large(const Params& p, const RowCtx& c, int rr, int64_t grow, uint32_t* keys,
-                          uint32_t* hist, uint64_t* cand) {
+// Warp inclusive prefix sum.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const uint32_t lane = lane_id();
-  const int n_all = p.N;
-  for (int n = lane; n < n_all; n += 32) {
-    const float z = row_logit(c, rr, n);
-    if (p.logits != nullptr) p.logits[grow * n_all + n] = z;
-    keys[n] = float_key(p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(z) + c.bias[n] : z);
-  }
-  __syncwarp();
-  const int want = p.k < n_all ? p.k : n_all;
-  uint32_t prefix = 0, pmask = 0;
-  int remaining = want;
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = lane; i < 256; i += 32) hist[i] = 0;
-    __syncwarp();
-    // Keys crowd into a few bins (scores share their top bits), so lanes with
-    // the same bin add their count once through the lowest such lane.
-    for (int base = 0; base < n_all; base += 32) {
-      const int i = base + static_cast<int>(lane);
-      const uint32_t u = i < n_all ? keys[i] : 0u;
-      const bool in = i < n_all && (u & pmask) == prefix;
-      const uint32_t bin = in ? (u >> shift) & 255u : 256u + lane;
-      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
-      if (in && (__ffs(peers) - 1) == static_cast<int>(lane)) atomicAdd(&hist[bin], __popc(peers));
-    }
-    __syncwarp();
-    uint32_t cnt[8];
-    uint32_t local = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // lane l owns digits 255-8l down to 248-8l
-      cnt[j] = hist[255 - 8 * lane - j];
-      local += cnt[j];
-    }
-    uint32_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= static_cast<uint32_t>(o)) incl += t;
-    }
-    const uint32_t excl = incl - local;
-    const bool owner = excl < static_cast<uint32_t>(remaining) && incl >= static_cast<uint32_t>(remaining);
-    uint32_t digit = 0, above = 0;
-    if (owner) {
-      uint32_t acc = excl;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (acc + cnt[j] >= static_cast<uint32_t>(remaining)) {
-          digit = 255 - 8 * lane - j;
-          above = acc;
-          break;
-        }
-        acc += cnt[j];
-      }
-    }
-    const uint32_t src = __ffs(__ballot_sync(0xFFFFFFFFu, owner)) - 1;
-    digit = __shfl_sync(0xFFFFFFFFu, digit, src);
-    above = __shfl_sync(0xFFFFFFFFu, above, src);
-    remaining -= static_cast<int>(above);
-    prefix |= digit << shift;
-    pmask |= 255u << shift;
-    __syncwarp();
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= static_cast<uint32_t>(o)) v += t;
   }
-  const uint32_t kth = prefix;
-  const int need_eq = remaining;
-  int out = 0, eq_seen = 0;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < n_all; base += 32) {
-    const int i = base + static_cast<int>(lane);
-    const uint32_t u = i < n_all ? keys[i] : 0u;
-    const bool gt = i < n_all && u > kth;
-    const bool eq = i < n_all && u == kth;
-    const uint32_t beq = __ballot_sync(0xFFFFFFFFu, eq);
-    const int eq_rank = eq_seen + __popc(beq & lt_mask);
-    const bool take = gt || (eq && eq_rank < need_eq);
-    const uint32_t btake = __ballot_sync(0xFFFFFFFFu, take);
-    if (take)
-      cand[out + __popc(btake & lt_mask)] =
-          (static_cast<uint64_t>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
-    out += __popc(btake);
-    eq_seen += __popc(beq);
-  }
-  for (int i = out + static_cast<int>(lane); i < p.cand_cap; i += 32) cand[i] = 0ull;
-  __syncwarp();
-  for (int size = 2; size <= p.cand_cap; size <<= 1) {  // bitonic sort, descending
+  return v;
+}
+
+// Sort 32 * P entries descending across the warp, entry e = lane * P + j in
+// v[j] (bitonic network: strides below P inside a lane, the rest by shuffles).
+template <int P>
+__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[P]) {
+  const uint32_t lane = lane_id();
+  constexpr int kN = 32 * P;
+#pragma unroll
+  for (int size = 2; size <= kN; size <<= 1) {
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = lane; t < p.cand_cap / 2; t += 32) {
-        const int lo = 2 * stride * (t / stride) + (t % stride);
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t a = cand[lo], b = cand[hi];
-        if ((a < b) == desc) {
-          cand[lo] = b;
-          cand[hi] = a;
+      if (stride < P) {
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          if ((j & stride) == 0) {
+            const int e = static_cast<int>(lane) * P + j;
+            const bool desc = (e & size) == 0;
+            const uint64_t x = v[j], y = v[j | stride];
+            const bool swap = desc ? (y > x) : (x > y);
+            v[j] = swap ? y : x;
+            v[j | stride] = swap ? x : y;
+          }
+        }
+      } else {
+        const int lx = stride / P;
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          const int e = static_cast<int>(lane) * P + j;
+          const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, v[j], lx);
+          const bool lower = (e & stride) == 0;
+          const bool desc = (e & size) == 0;
+          const bool keep_max = desc == lower;
+          v[j] = keep_max ? (other > v[j] ? other : v[j]) : (other < v[j] ? other : v[j]);
         }
       }
-      __syncwarp();
     }
   }
-  for (int t = lane; t < p.k; t += 32) {
-    const int64_t o = grow * p.k + t;
-    if (t < out) {
-      const uint64_t v = cand[t];
-      const int n = entry_col(v);
-      p.topk_idx[o] = n;
-      p.topk_score[o] = entry_score(v);
-      if (p.topk_weight) p.topk_weight[o] = weight_of(p, row_logit(c, rr, n));
-    } else {
-      p.topk_idx[o] = -1;
-      p.topk_score[o] = -__int_as_float(0x7F800000);
-      if (p.topk_weight) p.topk_weight[o] = 0.0f;
-    }
+}
+
+__device__ __forceinline__ void store_entry(const Params& p, const RowCtx& c, int rr, int64_t o, uint64_t e) {
+  const int n = entry_col(e);
+  const float sc = entry_score(e);
+  p.topk_idx[o] = n;
+  p.topk_score[o] = sc;
+  if (p.topk_weight)
+    p.topk_weight[o] = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(row_logit(c, rr, n)) : sc;
+}
+
+__device__ __forceinline__ void store_empty(const Params& p, int64_t o) {
+  p.topk_idx[o] = -1;
+  p.topk_score[o] = -__int_as_float(0x7F800000);
+  if (p.topk_weight) p.topk_weight[o] = 0.0f;
+}
+
+// Shared-memory slot of entry e of a run of 32 * P candidates that one warp
+// reads and writes as e = lane * P + j: each lane's P entries are
+// XOR-rotated by the lane so a warp's accesses spread over the banks.
+template <int P>
+__device__ __forceinline__ int run_slot(int e) {
+  const int local = e & (32 * P - 1);
+  return (e & ~(32 * P - 1)) | (local ^ ((local / P) & (P - 1)));
+}
+
+// Sort the run cand[base .. base + 32P) descending in place through registers.
+template <int P>
+__device__ void sort_run(uint64_t* cand, int base) {
+  const uint32_t lane = lane_id();
+  uint64_t v[P];
+#pragma unroll
+  for (int j = 0; j < P; ++j) v[j] = cand[run_slot<P>(base + static_cast<int>(lane) * P + j)];
+  warp_bitonic_desc<P>(v);
+#pragma unroll
+  for (int j = 0; j < P; ++j) cand[run_slot<P>(base + static_cast<int>(lane) * P + j)] = v[j];
+}
+
+// Entries of the sorted run cand[base .. base + len) that are greater than x.
+template <int P>
+__device__ __forceinline__ int count_above(const uint64_t* cand, int base, int len, uint64_t x) {
+  int lo = 0, hi = len;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cand[run_slot<P>(base + mid)] > x) lo = mid + 1; else hi = mid;
   }
-  __syncwarp();
+  return lo;
+}
+
+// Block-wide exclusive prefix sum of one value per thread; `tot` gets the
+// block total.  `red` holds kWarps words; two block barriers.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* tot) {
+  const uint32_t lane = lane_id();
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const uint32_t incl = warp_incl_scan(v);
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t t = red[w];
+    before += w < warp ? t : 0u;
+    all += t;
+  }
+  __syncthreads();  // red is reused by the next call
+  *tot = all;
+  return before + incl - v;
+}
+
+// Sort the W = cap / (32P) runs, then place every candidate by its rank
+// (its index in its run plus the entries of the other runs above it;
+// entries are distinct) and write the outputs.
+template <int P>
+__device__ void sort_runs_and_store(const Params& p, const RowCtx& c, int rr, int64_t grow, uint64_t* cand) {
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  constexpr int kLen = 32 * P;
+  const int runs = p.cand_cap / kLen;  // <= 4
+  if (warp < runs) sort_run<P>(cand, warp * kLen);
+  __syncthreads();
+  for (int e = static_cast<int>(threadIdx.x); e < p.cand_cap; e += kThreads) {
+    const uint64_t x = cand[run_slot<P>(e)];
+    if (x == 0ull) continue;  // padding
+    const int w = e / kLen;
+    int rank = e - w * kLen;
+    for (int o = 0; o < runs; ++o)
+      if (o != w) rank += count_above<P>(cand, o * kLen, kLen, x);
+    if (rank < p.k) store_entry(p, c, rr, grow * p.k + rank, x);
+  }
+}
+
+// General rows (k > 32 or N > 256), every thread of the CTA on one row at a
+// time: keys of all N scores in shared memory; the want-th largest key T by
+// a search over 2-bit digits (per digit, the counts of keys >= each of three
+// thresholds); the keys above T and the lowest-column keys equal to T in
+// column order (two block scans); runs of up to 256 candidates sorted by
+// up to four warps in registers, merged by rank; outputs.
+__device__ void rows_large(const Params& p, const RowCtx& c, int owned, int64_t grow0, uint32_t* keys,
+                           uint64_t* cand, uint32_t* red) {
+  const uint32_t lane = lane_id();
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int tid = static_cast<int>(threadIdx.x);
+  const int n_all = p.N;
+  const int n4 = (n_all + 3) >> 2;  // key quads (keys past N are 0, below every real key)
+  const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
+  const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
+  const uint32_t want = static_cast<uint32_t>(p.k < n_all ? p.k : n_all);
+  const int qp = (n4 + kThreads - 1) / kThreads;  // quads per thread, in column order
+  const int q_lo = min(n4, tid * qp), q_hi = min(n4, q_lo + qp);
+  for (int rr = 0; rr < owned; ++rr) {
+    const int64_t grow = grow0 + rr;
+    const float* rowp = c.recv + rr * c.rs;
+    for (int q = tid; q < n4; q += kThreads) {
+      float4 acc = *reinterpret_cast<const float4*>(rowp + 4 * q);
+      for (int ks = 1; ks < c.k_split; ++ks) {
+        const float4 t = *reinterpret_cast<const float4*>(rowp + ks * c.ro * c.rs + 4 * q);
+        acc.x += t.x;
+        acc.y += t.y;
+        acc.z += t.z;
+        acc.w += t.w;
+      }
+      uint32_t kq[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int n = 4 * q + j;
+        const float z = (j == 0 ? acc.x : j == 1 ? acc.y : j == 2 ? acc.z : acc.w) * c.gab;
+        if (p.logits != nullptr && n < n_all) p.logits[grow * n_all + n] = z;
+        kq[j] = n < n_all ? float_key(router ? router_weight(z) + c.bias[n] : z) : 0u;
+      }
+      reinterpret_cast<uint4*>(keys)[q] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+    }
+    __syncthreads();
+    // T: per 2-bit digit from the top, the largest d with at least `want`
+    // keys >= T | d << b (thresholds >= 1, so the zero keys never count).
+    uint32_t T = 0;
+#pragma unroll 1
+    for (int b = 30; b >= 0; b -= 2) {
+      const uint32_t t1 = T | (1u << b), t2 = T | (2u << b), t3 = T | (3u << b);
+      uint32_t c1 = 0, c2 = 0, c3 = 0;
+      for (int q = tid; q < n4; q += kThreads) {
+        const uint4 k4 = keys4[q];
+        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          c1 += kk[j] >= t1;
+          c2 += kk[j] >= t2;
+          c3 += kk[j] >= t3;
+        }
+      }
+      c1 = __reduce_add_sync(0xFFFFFFFFu, c1);
+      c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
+      c3 = __reduce_add_sync(0xFFFFFFFFu, c3);
+      uint32_t* slot = red + ((b >> 1) & 1) * (4 * kWarps);  // alternate buffers: one barrier per digit
+      if (lane == 0) {
+        slot[warp] = c1;
+        slot[kWarps + warp] = c2;
+        slot[2 * kWarps + warp] = c3;
+      }
+      __syncthreads();
+      uint32_t s1 = 0, s2 = 0, s3 = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        s1 += slot[w];
+        s2 += slot[kWarps + w];
+        s3 += slot[2 * kWarps + w];
+      }
+      T = s3 >= want ? t3 : s2 >= want ? t2 : s1 >= want ? t1 : T;
+    }
+    uint32_t* scan = red + 8 * kWarps;
+    // keys above T and equal to T among this thread's quads (column order)
+    uint32_t gt_cnt = 0, eq_cnt = 0;
+    for (int q = q_lo; q < q_hi; ++q) {
+      const uint4 k4 = keys4[q];
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gt_cnt += kk[j] > T;
+        eq_cnt += kk[j] == T && kk[j] != 0u;
+      }
+    }
+    uint32_t gt_total = 0, eq_total = 0;
+    block_excl_scan(gt_cnt, scan, &gt_total);
+    uint32_t eq_rank = block_excl_scan(eq_cnt, scan, &eq_total);
+    const uint32_t need_eq = want - gt_total;
+    uint32_t take_cnt = 0;
+    for (int q = q_lo; q < q_hi; ++q) {
+      const uint4 k4 = keys4[q];
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool eq = kk[j] == T && kk[j] != 0u;
+        take_cnt += kk[j] > T || (eq && eq_rank < need_eq);
+        eq_rank += eq;
+      }
+    }
+    eq_rank -= eq_cnt;
+    uint32_t out = 0;
+    uint32_t pos = block_excl_scan(take_cnt, scan, &out);
+    const int P = p.cand_cap <= 128 ? 1 : p.cand_cap / 128;  // 4 runs of 32P (2 runs for 64)
+    for (int q = q_lo; q < q_hi; ++q) {
+      const uint4 k4 = keys4[q];
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool eq = kk[j] == T && kk[j] != 0u;
+        if (kk[j] > T || (eq && eq_rank < need_eq)) {
+          const int n = 4 * q + j;
+          const int e = static_cast<int>(pos++);
+          const int slot_e = P == 1 ? e : P == 2 ? run_slot<2>(e) : P == 4 ? run_slot<4>(e) : run_slot<8>(e);
+          cand[slot_e] = (static_cast<uint64_t>(kk[j]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
+        }
+        eq_rank += eq;
+      }
+    }
+    for (int e = static_cast<int>(out) + tid; e < p.cand_cap; e += kThreads) {
+      const int slot_e = P == 1 ? e : P == 2 ? run_slot<2>(e) : P == 4 ? run_slot<4>(e) : run_slot<8>(e);
+      cand[slot_e] = 0ull;
+    }
+    for (int t = static_cast<int>(out) + tid; t < p.k; t += kThreads)  // slots past N
+      store_empty(p, grow * p.k + t);
+    __syncthreads();
+    switch (P) {
+      case 1: sort_runs_and_store<1>(p, c, rr, grow, cand); break;
+      case 2: sort_runs_and_store<2>(p, c, rr, grow, cand); break;
+      case 4: sort_runs_and_store<4>(p, c, rr, grow, cand); break;
+      default: sort_runs_and_store<8>(p, c, rr, grow, cand); break;
+    }
+    __syncthreads();  // keys and candidates are rewritten for the next row
+  }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -627,9 +781,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int mt = blockIdx.x / csize;
   const int n_idx = rank % p.n_split;
   const int k_idx = rank / p.n_split;
-  const int m0 = mt * BM;
+  const int m0 = mt * p.rpc;
   const int n0 = n_idx * BN;
-  const int vr = min(BM, p.M - m0);  // valid rows of this tile
+  const int vr = min(p.rpc, p.M - m0);  // valid rows of this tile
   const int kt0 = k_idx * p.num_k_tiles / p.k_split;
   const int nk = (k_idx + 1) * p.num_k_tiles / p.k_split - kt0;
   const int ncols = min(BN, p.N - n0);
@@ -1131,13 +1285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int owned = min(p.ro, vr - r0);
     if (!p.large) {
       rows_small(p, c, owned, m0 + r0);
-    } else if (warp < p.sel_warps) {
-      uint8_t* mine = rowmem + p.recv_bytes + warp * (p.row_bytes + 1024 + p.cand_cap * 8);
-      uint32_t* keys = reinterpret_cast<uint32_t*>(mine);
-      uint32_t* hist = reinterpret_cast<uint32_t*>(mine + p.row_bytes);
-      uint64_t* cand = reinterpret_cast<uint64_t*>(mine + p.row_bytes + 1024);
-      for (int rr = warp; rr < owned; rr += p.sel_warps)
-        row_large(p, c, rr, m0 + r0 + rr, keys, hist, cand);
+    } else {
+      uint8_t* mine = rowmem + p.recv_bytes;
+      rows_large(p, c, owned, m0 + r0, reinterpret_cast<uint32_t*>(mine),
+                 reinterpret_cast<uint64_t*>(mine + p.row_bytes),
+                 reinterpret_cast<uint32_t*>(mine + p.row_bytes + p.cand_cap * 8));
     }
   }
 
@@ -1194,7 +1346,8 @@ struct Plan {
   int stages;
   int direct, ro, bulk;
   uint32_t recv_bytes, bias_off;
-  int large, sel_warps, cand_cap;
+  int rpc;
+  int large, cand_cap;
   uint32_t row_bytes;
   uint32_t region;
   size_t smem;
@@ -1203,9 +1356,10 @@ struct Plan {
 // Pick the split, epilogue and shared-memory layout of one problem; false if
 // it cannot be laid out.
 bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, int max_cluster,
-               Plan* out) {
+               int rpc, Plan* out) {
   Plan pl{};
-  const int64_t m_tiles = (M + BM - 1) / BM;
+  pl.rpc = rpc;
+  const int64_t m_tiles = (M + rpc - 1) / rpc;
   const int kt = static_cast<int>((K / 2 + BKB - 1) / BKB);
   if (N <= 128) {
     pl.bn = 128;
@@ -1226,12 +1380,12 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
     pl.k_split = ks < 1 ? 1 : ks;
   }
   const int csize = pl.n_split * pl.k_split;
-  const int vr_max = static_cast<int>(M < BM ? M : BM);
+  const int vr_max = static_cast<int>(M < rpc ? M : rpc);
   pl.ro = (vr_max + csize - 1) / csize;
   pl.direct = (pl.k_split == 1 && k <= 32) ? 1 : 0;
   pl.kmax = k <= 8 ? 8 : (k <= 16 ? 16 : 32);
   pl.large = (!pl.direct && (k > 32 || N > 32 * kSmallCols)) ? 1 : 0;
-  pl.cand_cap = pl.large ? next_pow2(k) : 0;
+  pl.cand_cap = pl.large ? (k <= 64 ? 64 : next_pow2(k)) : 0;  // 2 .. 32 per lane of the sort
   pl.row_bytes = pl.large ? static_cast<uint32_t>((N * 4 + 15) & ~15) : 0u;
   const int nk_max = (kt + pl.k_split - 1) / pl.k_split;
   const uint32_t sb = pl.bn == 128 ? Layout<128>::kStage : Layout<256>::kStage;
@@ -1239,7 +1393,6 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
                         static_cast<uint32_t>(pl.n_split * pl.bn) * 4u;
   const uint32_t staging = static_cast<uint32_t>(vr_max) * static_cast<uint32_t>(pl.bn + 4) * 4u;
   pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
-  pl.sel_warps = pl.large ? kWarps : 0;
   // After the main loop the stage region holds the direct epilogue's bias
   // copies, or the reduce epilogue's staged tile (bulk) / received partials.
   auto total = [&]() {
@@ -1256,22 +1409,18 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
     if (pl.direct && pl.n_split > 1)
       extra = static_cast<size_t>(pl.n_split) * pl.ro * pl.kmax * 16;  // merged per-row lists
     if (pl.large)
-      extra += static_cast<size_t>(pl.sel_warps) *
-               (pl.row_bytes + 1024 + static_cast<size_t>(pl.cand_cap) * 8);
+      extra += pl.row_bytes + static_cast<size_t>(pl.cand_cap) * 8 + 256;  // keys, candidates, block scratch
     pl.bias_off = static_cast<uint32_t>(extra);
     if (!pl.direct) extra += static_cast<size_t>((N * 4 + 15) & ~15);  // staged biases
     return 1024 + static_cast<size_t>(region) + kCtrlBytes + extra;
   };
   pl.bulk = pl.direct ? 0 : 1;
   while (pl.bulk && total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
-  while (pl.bulk && total() > static_cast<size_t>(smem_optin) && pl.sel_warps > 3) --pl.sel_warps;
   if (pl.bulk && total() > static_cast<size_t>(smem_optin)) {  // receive in the stage region
     pl.bulk = 0;
     pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
-    pl.sel_warps = pl.large ? kWarps : 0;
-  }
+    }
   while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
-  while (total() > static_cast<size_t>(smem_optin) && pl.sel_warps > 1) --pl.sel_warps;
   pl.smem = total();
   if (pl.smem > static_cast<size_t>(smem_optin)) return false;
   *out = pl;
@@ -1320,24 +1469,24 @@ cudaError_t configure(size_t smem, int cluster) {
 // Whether clusters of this size and shared-memory footprint can be resident
 // at all (answers cached per device and configuration).
 template <int BN, int KMAX>
-bool cluster_fits(int cluster, size_t smem) {
-  if (cluster <= 1) return true;
+int active_clusters(int cluster, size_t smem) {
+  if (cluster <= 1) return sm_count();  // one CTA per SM
   static std::mutex mu;
   static int cache_dev[64], cache_cluster[64];
   static size_t cache_smem[64];
-  static bool cache_ok[64];
+  static int cache_ok[64];
   static int n_cache = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_cache; ++i)
     if (cache_dev[i] == dev && cache_cluster[i] == cluster && cache_smem[i] == smem) return cache_ok[i];
-  bool ok = false;
+  int ok = 0;
   if (configure<BN, KMAX>(smem, cluster) == cudaSuccess) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(cluster, cluster, smem, nullptr, attr);
     int n = 0;
-    ok = cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN, KMAX>, &cfg) == cudaSuccess && n > 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN, KMAX>, &cfg) == cudaSuccess && n > 0) ok = n;
   }
   cudaGetLastError();  // a refused query leaves no error behind
   if (n_cache < 64) {
@@ -1361,16 +1510,17 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const C
   return cudaLaunchKernelEx(&cfg, gemm_topk_kernel<BN, KMAX>, ma, mb, msa, msb, p);
 }
 
-bool fits(const Plan& pl) {
+// Clusters of this plan that can be resident at once (0: none fits).
+int active(const Plan& pl) {
   const int c = pl.n_split * pl.k_split;
   if (pl.bn == 128) {
-    if (pl.kmax == 8) return cluster_fits<128, 8>(c, pl.smem);
-    if (pl.kmax == 16) return cluster_fits<128, 16>(c, pl.smem);
-    return cluster_fits<128, 32>(c, pl.smem);
+    if (pl.kmax == 8) return active_clusters<128, 8>(c, pl.smem);
+    if (pl.kmax == 16) return active_clusters<128, 16>(c, pl.smem);
+    return active_clusters<128, 32>(c, pl.smem);
   }
-  if (pl.kmax == 8) return cluster_fits<256, 8>(c, pl.smem);
-  if (pl.kmax == 16) return cluster_fits<256, 16>(c, pl.smem);
-  return cluster_fits<256, 32>(c, pl.smem);
+  if (pl.kmax == 8) return active_clusters<256, 8>(c, pl.smem);
+  if (pl.kmax == 16) return active_clusters<256, 16>(c, pl.smem);
+  return active_clusters<256, 32>(c, pl.smem);
 }
 
 cudaError_t launch(const Plan& pl, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
@@ -1399,11 +1549,21 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   Plan pl;
   int cap = kMaxCluster;
   for (;;) {
-    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, &pl)) return NVFP4_ERR_UNSUPPORTED;
-    if (fits(pl)) break;
+    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, BM, &pl)) return NVFP4_ERR_UNSUPPORTED;
+    if (active(pl) > 0) break;
     const int c = pl.n_split * pl.k_split;
     if (c <= 1 || cap <= 1) return NVFP4_ERR_UNSUPPORTED;
     cap = c / 2;
+  }
+  if (pl.large) {
+    // Row selection dominates: spread the rows over every cluster that can
+    // be resident (fewer rows per tile, so fewer rows per owning CTA).
+    const int n_active = active(pl);
+    const int64_t rpc = n_active > 0 ? (a.M + n_active - 1) / n_active : BM;
+    Plan spread;
+    if (rpc < BM && make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, static_cast<int>(rpc), &spread) &&
+        spread.n_split == pl.n_split && spread.k_split == pl.k_split && active(spread) > 0)
+      pl = spread;
   }
 
   const bool tma_sf = (a.K % 256) == 0;
@@ -1447,11 +1607,11 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.bulk = pl.bulk;
   p.recv_bytes = pl.recv_bytes;
   p.bias_off = pl.bias_off;
+  p.rpc = pl.rpc;
   p.large = pl.large;
-  p.sel_warps = pl.sel_warps;
   p.cand_cap = pl.cand_cap;
   p.row_bytes = pl.row_bytes;
-  const int grid = static_cast<int>((a.M + BM - 1) / BM) * pl.n_split * pl.k_split;
+  const int grid = static_cast<int>((a.M + pl.rpc - 1) / pl.rpc) * pl.n_split * pl.k_split;
   const cudaError_t e = launch(pl, ma, mb, msa, msb, p, grid, stream);
   if (e != cudaSuccess) {
     *err = e;
