@@ -36,7 +36,6 @@ import workloads  # noqa: E402
 L2_BYTES = 126 * 1024 * 1024
 HIDDEN, EXPERTS, TOPK, INTER, GRAN = workloads.HIDDEN, workloads.EXPERTS, workloads.ROUTER_TOPK, \
     workloads.MOE_INTER, 8
-KERNELS_PER_STEP = 5
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense NVFP4 / BF16 tensor ratio on GB300
 
 
@@ -400,6 +399,12 @@ def run_gpu(args, rank, world, local):
     chunk = 16
     n_sets = int(np.ceil(n_sets / chunk) * chunk)
     sets = RouterSets(nv, T, n_sets, ws)
+    # kernels one step launches (counted by the library itself)
+    torch.cuda.synchronize()
+    before = nv.kernel_launches()
+    sets.step(nv, ws, 0)
+    kernels_per_step = nv.kernel_launches() - before
+    torch.cuda.synchronize()
 
     graphs, singles = capture_chunks(lambda i: sets.step(nv, ws, i), n_sets, chunk)
     with ClockSampler(local) as clk:
@@ -474,7 +479,7 @@ def run_gpu(args, rank, world, local):
         detail = secondary(nv, ws, pk, flush)
         del flush
     clocks = clk.summary(t0, t1)
-    return dict(value=value, secs=secs_max, roofline=roofline, e2e=e2e, op_us={k: round(v * 1e6, 3)
+    return dict(value=value, secs=secs_max, kernels_per_step=kernels_per_step, roofline=roofline, e2e=e2e, op_us={k: round(v * 1e6, 3)
                 for k, v in op_times.items()}, clocks=clocks, detail=detail, n_sets=n_sets,
                 footprint=sets.footprint(), device_status=status)
 
@@ -616,7 +621,7 @@ def main():
                 ms_per_step=round(res["secs"] / args.steps * 1e3, 5), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="nvfp4-e2m1/f32", data="synthetic",
                 config=config, roofline=res["roofline"], cpu_baseline=cpu, e2e=res["e2e"],
-                gpu_launches=KERNELS_PER_STEP * args.steps, clocks=res["clocks"],
+                gpu_launches=res["kernels_per_step"] * args.steps, clocks=res["clocks"],
                 op_us=res["op_us"], device_status=res["device_status"], detail=res["detail"])
     print(json.dumps(line), flush=True)
 

@@ -186,6 +186,10 @@ const char* nvfp4_status_string(int status);
 /* The cudaError_t of the last call that returned NVFP4_ERR_CUDA on this thread. */
 int nvfp4_last_cuda_error(void);
 
+/* Diagnostic: kernels this library has launched in this process (all threads;
+ * a launch recorded into a CUDA graph counts once, at capture). */
+uint64_t nvfp4_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

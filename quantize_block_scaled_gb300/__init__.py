@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_status_string.argtypes = [I]
         L.nvfp4_last_cuda_error.restype = I
         L.nvfp4_last_cuda_error.argtypes = []
+        L.nvfp4_kernel_launches.restype = ctypes.c_uint64
+        L.nvfp4_kernel_launches.argtypes = []
         L.nvfp4_quantize_noalloc.restype = I
         L.nvfp4_quantize_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P]
         _lib = L
@@ -81,7 +83,8 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
                     "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
-                    "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc")
+                    "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc",
+                    "nvfp4_kernel_launches")
 
 
 def _check(fn: str, status: int):
@@ -130,6 +133,11 @@ def nvfp4_quantize(x, q, sf, gs, ws, stream=None):
     _check("nvfp4_quantize", lib().nvfp4_quantize(
         _ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process (graph captures count once)."""
+    return int(lib().nvfp4_kernel_launches())
 
 
 def nvfp4_quantize_noalloc(x, q, sf, gs, stream=None):

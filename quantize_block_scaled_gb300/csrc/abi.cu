@@ -2,6 +2,7 @@
 // caller's stream.  Nothing here allocates or synchronises (except the
 // diagnostic nvfp4_read_device_status).
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -10,6 +11,7 @@
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
 
 int cuda_failure(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -43,6 +45,8 @@ int sm_count() {
 
 void set_last_cuda_error(int e) { g_last_cuda_error = e; }
 
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace nvfp4
 
 extern "C" {
@@ -67,7 +71,10 @@ int nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, 
   const int st = check_workspace(ws, ws_bytes);
   if (st != NVFP4_OK) return st;
   auto* w = static_cast<nvfp4::Workspace*>(ws);
-  cudaError_t e = nvfp4::launch_amax(x, rows, cols, ld_x, gs, w, stream);
+  cudaError_t e = cudaSuccess;
+  if (nvfp4::launch_quantize_onepass(x, rows, cols, ld_x, q, sf, gs, w, stream, &e))
+    return e == cudaSuccess ? NVFP4_OK : cuda_failure(e);
+  e = nvfp4::launch_amax(x, rows, cols, ld_x, gs, w, stream);
   if (e != cudaSuccess) return cuda_failure(e);
   e = nvfp4::launch_quantize(x, rows, cols, ld_x, q, sf, gs, stream);
   if (e != cudaSuccess) return cuda_failure(e);
@@ -88,7 +95,10 @@ int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, 
   const int st = check_workspace(ws, ws_bytes);
   if (st != NVFP4_OK) return st;
   auto* w = static_cast<nvfp4::Workspace*>(ws);
-  cudaError_t e = nvfp4::launch_amax(x, rows, 2 * inter, 2 * inter, gs, w, stream);
+  cudaError_t e = cudaSuccess;
+  if (nvfp4::launch_deinterleave_onepass(x, rows, inter, granularity, q, sf, gs, w, stream, &e))
+    return e == cudaSuccess ? NVFP4_OK : cuda_failure(e);
+  e = nvfp4::launch_amax(x, rows, 2 * inter, 2 * inter, gs, w, stream);
   if (e != cudaSuccess) return cuda_failure(e);
   e = nvfp4::launch_deinterleave_quantize(x, rows, inter, granularity, q, sf, gs, stream);
   if (e != cudaSuccess) return cuda_failure(e);
@@ -169,5 +179,7 @@ const char* nvfp4_status_string(int status) {
 }
 
 int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t nvfp4_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

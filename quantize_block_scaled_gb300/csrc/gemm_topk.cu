@@ -1507,6 +1507,7 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const C
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(grid, cluster, smem, stream, attr);
+  count_launch();
   return cudaLaunchKernelEx(&cfg, gemm_topk_kernel<BN, KMAX>, ma, mb, msa, msb, p);
 }
 

@@ -12,9 +12,10 @@ namespace nvfp4 {
 // calls.
 struct Workspace {
   uint32_t amax_bits;  // running max of |x| as FP32 bits (valid for x >= 0)
-  uint32_t done;       // blocks of the amax kernel that have finished
+  uint32_t done;       // blocks of the amax kernel that have finished (one-pass kernel: arrived)
+  uint32_t depart;     // one-pass quantize kernel: blocks that have finished
   uint32_t status;     // NVFP4_DEVICE_* bits; cleared by nvfp4_read_device_status
-  uint32_t reserved[61];
+  uint32_t reserved[60];
 };
 static_assert(sizeof(Workspace) == 256, "workspace layout");
 constexpr size_t kWorkspaceBytes = sizeof(Workspace);
@@ -22,6 +23,17 @@ constexpr size_t kWorkspaceBytes = sizeof(Workspace);
 int sm_count();
 // Record a cudaError_t for nvfp4_last_cuda_error on this thread.
 void set_last_cuda_error(int e);
+// Count one kernel launch issued by the library (nvfp4_kernel_launches).
+void count_launch();
+
+// One-pass quantize (single cooperative launch) for inputs that fit in the
+// SMs' shared memory.  Returns false, having launched nothing, when the input
+// is empty or too large; otherwise *err is the launch status.
+bool launch_quantize_onepass(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,
+                             uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream, cudaError_t* err);
+bool launch_deinterleave_onepass(const uint16_t* x, int64_t rows, int64_t inter, int g, uint8_t* q,
+                                 uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream,
+                                 cudaError_t* err);
 
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
                         Workspace* ws, cudaStream_t stream);

@@ -9,8 +9,8 @@
 // owns its inputs and outputs; only the scratch moves into the library.
 //
 // The scratch is the same 256-byte block the workspace path uses: the
-// grid-wide amax slot and the block counter of the amax kernel (both must be
-// zero when the amax kernel starts) and the device status word.  It lives in
+// grid-wide amax slot and the block counters of the amax and one-pass kernels
+// (zero when a kernel starts) and the device status word.  It lives in
 // one file-scope array per device, so every call on a device shares it and
 // calls that run at the same time on the GPU (two streams, no ordering)
 // race on it.
@@ -72,12 +72,14 @@ extern "C" int nvfp4_quantize_noalloc(const uint16_t* x, int64_t rows, int64_t c
     nvfp4::set_last_cuda_error(rc);
     return NVFP4_ERR_CUDA;
   }
-  // The amax slot and the block counter (the first two words) must start at
-  // zero; the kernels leave them zeroed, but a call that never finished could
-  // have left anything behind, so they are cleared on the caller's stream.
-  static_assert(offsetof(nvfp4::Workspace, amax_bits) == 0 && offsetof(nvfp4::Workspace, done) == 4,
+  // The amax slot and the two block counters (the first three words) must
+  // start at zero; the kernels leave them zeroed, but a call that never
+  // finished could have left anything behind, so they are cleared on the
+  // caller's stream.
+  static_assert(offsetof(nvfp4::Workspace, amax_bits) == 0 && offsetof(nvfp4::Workspace, done) == 4 &&
+                    offsetof(nvfp4::Workspace, depart) == 8,
                 "cleared words");
-  const cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), stream);
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, 3 * sizeof(uint32_t), stream);
   if (e != cudaSuccess) {
     nvfp4::set_last_cuda_error(static_cast<int>(e));
     return NVFP4_ERR_CUDA;

@@ -17,6 +17,8 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "nvfp4.h"
+#include "ptx.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -332,6 +334,227 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
 }
 
+// ---------------------------------------------------------------- one pass
+
+// For inputs that fit in the shared memory of the SMs (up to ~30 MB on a
+// GB300): one cooperative launch, one CTA per SM.  Each CTA bulk-copies its
+// slice of units (16-element blocks, or 32-element gate/up chunks for the
+// deinterleave variant) into shared memory, reduces its |x| maximum into the
+// workspace, meets the other CTAs at a grid barrier (an arrival counter; the
+// launch guarantees the CTAs are co-resident; the wait is bounded), derives
+// gs from the complete maximum exactly as the amax kernel does, and
+// quantizes its slice from shared memory.  x is read from HBM once.  The
+// last CTA to finish re-zeroes the workspace counters.
+constexpr int kOnePassThreads = 256;
+constexpr uint32_t kOnePassMaxBytes = 200 * 1024;  // input bytes one CTA holds
+constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s of SM clock
+
+// kCluster: the grid is one thread-block cluster (<= 16 CTAs, small inputs);
+// the maxima meet in distributed shared memory behind cluster barriers
+// instead of the workspace counter.
+template <int G, bool kCluster>  // G = 0: plain quantize (unit = 16 elements); else deinterleave granularity (unit = 32)
+__global__ void __launch_bounds__(kOnePassThreads, 1)
+    quantize_onepass_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t upr, int64_t ld,
+                            int64_t units_per_cta, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                            float* __restrict__ gs_out, Workspace* __restrict__ ws) {
+  constexpr int kUnitElems = G == 0 ? 16 : 32;
+  constexpr uint32_t kUnitBytes = kUnitElems * 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t red[kOnePassThreads / 32];
+  __shared__ float gs_sh;
+  const int64_t total = rows * upr;
+  const int64_t u0 = static_cast<int64_t>(blockIdx.x) * units_per_cta;
+  const int64_t u1 = u0 + units_per_cta < total ? u0 + units_per_cta : total;
+  const int64_t n_units = u1 > u0 ? u1 - u0 : 0;
+  const uint32_t bar_a = ptx::smem_addr(&bar);
+  const uint32_t dst0 = ptx::smem_addr(smem);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_a, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(bar_a, static_cast<uint32_t>(n_units * kUnitBytes));
+    // one copy per row segment (rows may be strided), at most 64 KB each
+    const int64_t row_units = ld == upr * kUnitElems ? total : upr;  // contiguous rows: one segment
+    for (int64_t u = u0; u < u1;) {
+      const int64_t seg_end0 = (u / row_units + 1) * row_units;
+      const int64_t seg_end = seg_end0 < u1 ? seg_end0 : u1;
+      const int64_t r = u / upr, c = u % upr;
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(x + r * ld + c * kUnitElems);
+      int64_t left = (seg_end - u) * kUnitBytes;
+      uint32_t dst = dst0 + static_cast<uint32_t>((u - u0) * kUnitBytes);
+      while (left > 0) {
+        const uint32_t n = left < 65536 ? static_cast<uint32_t>(left) : 65536u;
+        ptx::bulk_load(dst, src, n, bar_a);
+        src += n;
+        dst += n;
+        left -= n;
+      }
+      u = seg_end;
+    }
+  }
+  __syncthreads();  // the barrier is initialised before anyone waits on it
+  uint32_t never = 0;
+  if (!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL) && threadIdx.x == 0)
+    atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+  // local max of |x| over the slice
+  const uint4* sv = reinterpret_cast<const uint4*>(smem);
+  const int64_t n_vec = n_units * (kUnitBytes / 16);
+  uint32_t m2 = 0;
+  for (int64_t i = threadIdx.x; i < n_vec; i += kOnePassThreads) m2 = __vmaxu2(m2, absmax8(sv[i]));
+  uint32_t m = fold16(m2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if constexpr (kCluster) {
+    __shared__ float cta_max;
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kOnePassThreads / 32; ++w) m = max(m, red[w]);
+      cta_max = __uint_as_float(m << 16);
+    }
+    ptx::cluster_sync();
+    if (threadIdx.x == 0) {
+      float mx = 0.0f;
+      for (uint32_t r = 0; r < gridDim.x; ++r) mx = fmaxf(mx, ptx::ld_cluster_f32(ptx::mapa_shared(ptx::smem_addr(&cta_max), r)));
+      const float gs = __fdiv_rn(fmaxf(mx, kAmaxFloor), kGsDivisor);
+      gs_sh = gs;
+      if (blockIdx.x == 0) gs_out[0] = gs;
+    }
+    ptx::cluster_sync();  // no CTA leaves while a peer may still read its maximum
+  } else if (threadIdx.x == 0) {
+    for (int w = 1; w < kOnePassThreads / 32; ++w) m = max(m, red[w]);
+    atomicMax(&ws->amax_bits, m << 16);
+    __threadfence();
+    atomicAdd(&ws->done, 1u);
+    // grid barrier: every CTA's maximum is in before gs is derived
+    volatile uint32_t* arrived = &ws->done;
+    const long long t0 = clock64();
+    bool late = false;
+    while (*arrived < gridDim.x) {
+      if (clock64() - t0 > kBarrierCycles) {
+        late = true;
+        break;
+      }
+    }
+    if (late) atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+    __threadfence();
+    const uint32_t bits = atomicAdd(&ws->amax_bits, 0u);
+    const float gs = __fdiv_rn(fmaxf(__uint_as_float(bits), kAmaxFloor), kGsDivisor);
+    gs_sh = gs;
+    if (blockIdx.x == 0) gs_out[0] = gs;
+  }
+  __syncthreads();
+  Scales sc;
+  sc.gs = gs_sh;
+  sc.r_gs = __frcp_rn(sc.gs);
+  sc.r_six = __frcp_rn(6.0f);
+  for (int64_t i = threadIdx.x; i < n_units; i += kOnePassThreads) {
+    const int64_t u = u0 + i;
+    if constexpr (G == 0) {
+      uint32_t sbyte;
+      uint2 codes;
+      quantize_block(sv[2 * i], sv[2 * i + 1], sc, sbyte, codes);
+      __stcs(reinterpret_cast<uint2*>(q) + u, codes);  // flat block index: [rows, cols/16]
+      sf[u] = static_cast<uint8_t>(sbyte);
+    } else {
+      const int64_t inter = upr * 16;
+      const int64_t r = u / upr, c = u % upr;
+      uint32_t w[16];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 t = sv[4 * i + v];
+        w[4 * v] = t.x;
+        w[4 * v + 1] = t.y;
+        w[4 * v + 2] = t.z;
+        w[4 * v + 3] = t.w;
+      }
+      uint32_t g[8], up[8];
+      split_gate_up<G>(w, g, up);
+      uint32_t sg, su;
+      uint2 cg, cu;
+      quantize_block(make_uint4(g[0], g[1], g[2], g[3]), make_uint4(g[4], g[5], g[6], g[7]), sc, sg, cg);
+      quantize_block(make_uint4(up[0], up[1], up[2], up[3]), make_uint4(up[4], up[5], up[6], up[7]), sc, su,
+                     cu);
+      uint8_t* qrow = q + r * inter;
+      __stcs(reinterpret_cast<uint2*>(qrow + c * 8), cg);
+      __stcs(reinterpret_cast<uint2*>(qrow + inter / 2 + c * 8), cu);
+      uint8_t* srow = sf + r * (inter / 8);
+      srow[c] = static_cast<uint8_t>(sg);
+      srow[inter / 16 + c] = static_cast<uint8_t>(su);
+    }
+  }
+  if constexpr (kCluster) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Every CTA read the maximum before departing; the last one resets.
+    if (atomicAdd(&ws->depart, 1u) == gridDim.x - 1) {
+      atomicExch(&ws->amax_bits, 0u);
+      atomicExch(&ws->done, 0u);
+      atomicExch(&ws->depart, 0u);
+    }
+  }
+}
+
+// Launch the one-pass kernel if the input fits in the SMs' shared memory;
+// false (nothing launched, no error left behind) otherwise.  Up to 512 KB a
+// single cluster of up to 16 CTAs, beyond that a cooperative grid of one
+// CTA per SM.
+constexpr int64_t kClusterMaxBytes = 512 * 1024;
+
+template <int G>
+bool launch_onepass(const uint16_t* x, int64_t rows, int64_t upr, int64_t ld, uint8_t* q, uint8_t* sf,
+                    float* gs, Workspace* ws, cudaStream_t stream, cudaError_t* err) {
+  constexpr int64_t kUnitBytes = (G == 0 ? 16 : 32) * 2;
+  const int64_t total = rows * upr;
+  if (total == 0) return false;
+  const int sms = sm_count();
+  const int64_t max_units = kOnePassMaxBytes / kUnitBytes;
+  if (total > max_units * sms) return false;
+  const bool cluster = total * kUnitBytes <= kClusterMaxBytes;
+  // at least 8 KB per CTA; one cluster of <= 16 CTAs, or at most one CTA per SM
+  const int64_t min_units = 8192 / kUnitBytes;
+  int64_t grid = (total + min_units - 1) / min_units;
+  const int64_t cap = cluster ? 16 : sms;
+  if (grid > cap) grid = cap;
+  const int64_t per = (total + grid - 1) / grid;
+  grid = (total + per - 1) / per;
+  const size_t smem = static_cast<size_t>(per * kUnitBytes);
+  auto kernel = cluster ? quantize_onepass_kernel<G, true> : quantize_onepass_kernel<G, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kOnePassMaxBytes)) != cudaSuccess ||
+      (cluster && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kOnePassThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (cluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(grid);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cluster) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return false;
+    }
+  }
+  count_launch();
+  *err = cudaLaunchKernelEx(&cfg, kernel, x, rows, upr, ld, per, q, sf, gs, ws);
+  return true;
+}
+
 int grid_for(int64_t work_items, int blocks_per_sm) {
   const int64_t need = (work_items + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
@@ -341,10 +564,30 @@ int grid_for(int64_t work_items, int blocks_per_sm) {
 
 }  // namespace
 
+bool launch_quantize_onepass(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,
+                             uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream, cudaError_t* err) {
+  return launch_onepass<0>(x, rows, cols / 16, ld, q, sf, gs, ws, stream, err);
+}
+
+bool launch_deinterleave_onepass(const uint16_t* x, int64_t rows, int64_t inter, int g, uint8_t* q,
+                                 uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream,
+                                 cudaError_t* err) {
+  const int64_t cpr = inter / 16;  // 32-element input chunks per row
+  switch (g) {
+    case 1: return launch_onepass<1>(x, rows, cpr, 2 * inter, q, sf, gs, ws, stream, err);
+    case 2: return launch_onepass<2>(x, rows, cpr, 2 * inter, q, sf, gs, ws, stream, err);
+    case 4: return launch_onepass<4>(x, rows, cpr, 2 * inter, q, sf, gs, ws, stream, err);
+    case 8: return launch_onepass<8>(x, rows, cpr, 2 * inter, q, sf, gs, ws, stream, err);
+    case 16: return launch_onepass<16>(x, rows, cpr, 2 * inter, q, sf, gs, ws, stream, err);
+    default: return false;
+  }
+}
+
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
                         Workspace* ws, cudaStream_t stream) {
   const int64_t vpr = cols / 8;
   const int grid = grid_for((rows * vpr + kAmaxUnroll - 1) / kAmaxUnroll, 4);
+  count_launch();
   amax_kernel<<<grid, kThreads, 0, stream>>>(x, rows, vpr, ld, gs, ws);
   return cudaGetLastError();
 }
@@ -354,6 +597,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
   const int64_t bpr = cols / 16;
   if (rows * bpr == 0) return cudaSuccess;
   const int grid = grid_for((rows * bpr + 1) / 2, 4);
+  count_launch();
   quantize_kernel<<<grid, kThreads, 0, stream>>>(x, rows, bpr, ld, q, sf, gs);
   return cudaGetLastError();
 }
@@ -364,6 +608,7 @@ cudaError_t launch_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_
   const int64_t items = rows * (inter / 16);
   if (items == 0) return cudaSuccess;
   const int grid = grid_for(items, 4);
+  count_launch();
   switch (g) {
     case 1: deinterleave_quantize_kernel<1><<<grid, kThreads, 0, stream>>>(x, rows, inter, q, sf, gs); break;
     case 2: deinterleave_quantize_kernel<2><<<grid, kThreads, 0, stream>>>(x, rows, inter, q, sf, gs); break;

@@ -1,6 +1,8 @@
 """GPU parity of nvfp4_quantize / nvfp4_deinterleave_quantize with the oracle.
 
-Bit-exact: packed codes, E4M3 scale bytes and the FP32 global scale.
+Bit-exact: packed codes, E4M3 scale bytes and the FP32 global scale.  The
+sizes cover all three kernel paths: one cluster (up to 512 KB of input), one
+cooperative grid (up to ~30 MB), and the amax + quantize kernel pair beyond.
 Inputs are the seeded workloads (N(0,1) with 0.1% x100 outliers, the
 Student-t prefill activations with +-U(500,2000) outliers) plus edge cases.
 """
@@ -78,6 +80,13 @@ def test_quantize_strided_rows(nv, ws):
     assert_quant_equal(gpu_quantize(nv, ws, x, ld=1040), oracle.quantize(x), "ld 1040")
 
 
+def test_quantize_strided_two_pass(nv, ws):
+    # 2200 x 7168 bf16 = 31.5 MB: beyond what the one-pass kernel holds on chip
+    # (about 30 MB), so the amax + quantize kernels run, on strided rows.
+    x = workloads.quantize_input(2200, seed=8)
+    assert_quant_equal(gpu_quantize(nv, ws, x, ld=7184), oracle.quantize(x), "two-pass ld 7184")
+
+
 def test_quantize_edge_values(nv, ws):
     f = np.zeros((4, 64), np.float32)
     f[1, :] = -1e-30                      # all tiny negatives: one far-below-max block
@@ -153,6 +162,13 @@ def test_deinterleave_quantize_large(nv, ws, g):
     x = workloads.swiglu_interleaved(2048)
     assert_quant_equal(gpu_deinterleave(nv, ws, x, g), oracle.deinterleave_quantize(x, g),
                        f"deinterleave T=2048 g={g}")
+
+
+def test_deinterleave_quantize_two_pass(nv, ws):
+    # 4096 x 4096 bf16 = 33.5 MB: the amax + deinterleave kernels, not the one-pass kernel
+    x = workloads.swiglu_interleaved(4096, seed=11)
+    assert_quant_equal(gpu_deinterleave(nv, ws, x, 1), oracle.deinterleave_quantize(x, 1),
+                       "deinterleave T=4096 g=1")
 
 
 def test_deinterleave_small_width(nv, ws):
