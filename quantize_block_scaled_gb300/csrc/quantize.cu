@@ -105,23 +105,21 @@ __global__ void __launch_bounds__(kThreads, 4)
 
 // ---------------------------------------------------------------- block codec
 
-// E4M3 (FN) code of s >= 0: round to nearest even, saturating at 448.
+// E4M3 (FN) code of s >= 0: round to nearest even, saturating at 448 (the
+// hardware conversion, branch-free; subnormal codes are steps of 2^-9).
 __device__ __forceinline__ uint32_t e4m3_encode(float s) {
-  if (!(s < 448.0f)) return 0x7Eu;
-  if (s < 0.015625f) {  // below 2^-6: subnormal grid, step 2^-9 (code = step count)
-    return static_cast<uint32_t>(__float2int_rn(__fmul_rn(s, 512.0f)));
-  }
-  const uint32_t b = __float_as_uint(s);
-  const uint32_t r = b + 0x7FFFFu + ((b >> 20) & 1u);  // round the mantissa to 3 bits
-  const uint32_t code = (r >> 20) - (120u << 3);        // rebias exponent 127 -> 7
-  return min(code, 0x7Eu);
+  uint16_t pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(s));
+  return pair & 0xFFu;  // the second operand lands in the low byte
 }
 
-// Value of a non-negative E4M3 code.
+// Value of a non-negative E4M3 code (exact through FP16).
 __device__ __forceinline__ float e4m3_decode(uint32_t c) {
-  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
-  if (e == 0) return __fmul_rn(static_cast<float>(m), 0.001953125f);  // m * 2^-9
-  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c)));
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(static_cast<uint16_t>(h2 & 0xFFFFu)));
+  return f;
 }
 
 // Four E2M1 bytes (8 codes, element 0 in the low nibble) of 8 floats.

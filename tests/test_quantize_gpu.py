@@ -100,6 +100,18 @@ def test_quantize_edge_values(nv, ws):
     assert_quant_equal(gpu_quantize(nv, ws, z), oracle.quantize(z), "all zero")
 
 
+def test_quantize_wide_scale_range(nv, ws):
+    # Block maxima spread over 2^-30 .. 2^21, so the E4M3 scales run through
+    # zero, the subnormal steps of 2^-9, every normal binade and saturation.
+    rng = np.random.default_rng(12)
+    rows, cols = 96, 1024
+    f = rng.standard_normal((rows, cols)).astype(np.float32)
+    e = rng.integers(-30, 21, size=(rows, cols // 16)).astype(np.float32)
+    f *= np.repeat(np.exp2(e), 16, axis=1)
+    x = workloads.bf16_bits(f)
+    assert_quant_equal(gpu_quantize(nv, ws, x), oracle.quantize(x), "wide scale range")
+
+
 def test_quantize_signed_zero_inputs(nv, ws):
     # -0.0 and +0.0 inputs next to normal values: codes 0x8 and 0x0
     x = workloads.quantize_input(8, seed=31, cols=512)
