@@ -28,10 +28,32 @@ constexpr float kGsDivisor = 2688.0f;  // 6 (E2M1 max) * 448 (E4M3 max)
 constexpr float kAmaxFloor = 1e-8f;
 
 // First pass (amax): ordinary loads, so a tensor that fits in L2 is still
-// there for the second pass.  Second pass: streaming loads (last use).
+// there for the second pass; for a larger tensor the tail that the second
+// pass (which runs backwards) reads first is loaded with an L2 evict-last
+// policy and the rest with evict-first, so the tail survives in L2.
+// Second pass: streaming loads (last use).
 __device__ __forceinline__ uint4 ld_keep(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
+__device__ __forceinline__ uint64_t l2_policy_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld_policy(const uint4* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+// Bytes of a large tensor's tail the amax pass marks to keep in L2 (of 126 MB).
+constexpr int64_t kL2KeepBytes = 96ll << 20;
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
@@ -58,14 +80,30 @@ __global__ void __launch_bounds__(kThreads, 4)
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (ld == vpr * 8) {
     const uint4* xv = reinterpret_cast<const uint4*>(x);
-    for (; i + (kAmaxUnroll - 1) * stride < total; i += kAmaxUnroll * stride) {
-      uint4 v[kAmaxUnroll];
+    const int64_t keep_from = total * 16 > 2 * kL2KeepBytes ? total - kL2KeepBytes / 16 : total;
+    if (keep_from < total) {  // larger than L2: keep the tail, stream the head
+      const uint64_t pol_first = l2_policy_first(), pol_last = l2_policy_last();
+      for (; i + (kAmaxUnroll - 1) * stride < total; i += kAmaxUnroll * stride) {
+        uint4 v[kAmaxUnroll];
 #pragma unroll
-      for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(xv + i + u * stride);
+        for (int u = 0; u < kAmaxUnroll; ++u) {
+          const int64_t j = i + u * stride;
+          v[u] = ld_policy(xv + j, j >= keep_from ? pol_last : pol_first);
+        }
 #pragma unroll
-      for (int u = 0; u < kAmaxUnroll; ++u) m2 = __vmaxu2(m2, absmax8(v[u]));
+        for (int u = 0; u < kAmaxUnroll; ++u) m2 = __vmaxu2(m2, absmax8(v[u]));
+      }
+      for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(ld_policy(xv + i, i >= keep_from ? pol_last : pol_first)));
+    } else {
+      for (; i + (kAmaxUnroll - 1) * stride < total; i += kAmaxUnroll * stride) {
+        uint4 v[kAmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(xv + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u) m2 = __vmaxu2(m2, absmax8(v[u]));
+      }
+      for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(__ldg(xv + i)));
     }
-    for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(__ldg(xv + i)));
   } else if (i < total) {
     int64_t r = i / vpr, c = i % vpr;
     const int64_t sr = stride / vpr, sc = stride % vpr;
