@@ -210,6 +210,10 @@ class RouterSets:
         self.idx, self.score, self.weight = e(T, TOPK, dt=torch.int32), e(T, TOPK, dt=torch.float32), \
             e(T, TOPK, dt=torch.float32)
         self.qh, self.sfh, self.gsh = e(T, INTER), e(T, INTER // 8), e(1, dt=torch.float32)
+        # The SwiGLU-output quantize does not depend on the router: it runs on a
+        # second stream (with its own workspace) beside quantize -> GEMM.
+        self.side = torch.cuda.Stream()
+        self.ws2 = nv.workspace()
         torch.cuda.synchronize()
 
     def footprint(self):
@@ -231,9 +235,14 @@ class RouterSets:
         nv.nvfp4_deinterleave_quantize(self.h[i], GRAN, self.qh[i], self.sfh[i], self.gsh[i], ws)
 
     def step(self, nv, ws, i):
+        import torch
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)  # fork after this step's inputs are in place
+        with torch.cuda.stream(self.side):
+            self.op_deinterleave(nv, self.ws2, i)
         self.op_quantize(nv, ws, i)
         self.op_gemm(nv, ws, i)
-        self.op_deinterleave(nv, ws, i)
+        main.wait_stream(self.side)  # join
 
 
 def capture_chunks(fn, n_sets, chunk):

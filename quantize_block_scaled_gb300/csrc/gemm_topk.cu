@@ -802,20 +802,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&bars[3 * kMaxStages + 2]), 1);  // rows received by bulk copy
     *abort = 0u;
     fence_mbar_init();
-    if (p.tma_sf) {
-      // The first stages need no empty-slot wait: start their loads now,
-      // ahead of the TMEM allocation and the block barrier.
-      const int pre = min(S, nk);
-      const uint32_t tx = L::kA + L::kB + L::kSfaStage + L::kSfbStage;
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t st = sbase + i * L::kStage;
-        mbar_arrive_expect_tx(full_bar(i), tx);
-        tma_load_2d(st, &tma_a, full_bar(i), (kt0 + i) * BKB, m0);
-        tma_load_2d(st + L::offB, &tma_b, full_bar(i), (kt0 + i) * BKB, n0);
-        tma_load_2d(st + L::offSfaStage, &tma_sfa, full_bar(i), (kt0 + i) * 16, m0);
-        tma_load_2d(st + L::offSfbStage, &tma_sfb, full_bar(i), (kt0 + i) * 16, n0);
-      }
-    }
     if (p.bulk) {
       // Bytes this CTA will receive: each K slice's partials of its own rows,
       // every column slice padded to 4 floats.
@@ -829,6 +815,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
+  }
+  pdl_wait();  // the previous kernel's outputs (our A operand, scales, ...) are complete
+  if (threadIdx.x == 0) {
+    if (p.tma_sf) {
+      // The first stages need no empty-slot wait: start their loads now,
+      // ahead of the block barrier.
+      const int pre = min(S, nk);
+      const uint32_t tx = L::kA + L::kB + L::kSfaStage + L::kSfbStage;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = sbase + i * L::kStage;
+        mbar_arrive_expect_tx(full_bar(i), tx);
+        tma_load_2d(st, &tma_a, full_bar(i), (kt0 + i) * BKB, m0);
+        tma_load_2d(st + L::offB, &tma_b, full_bar(i), (kt0 + i) * BKB, n0);
+        tma_load_2d(st + L::offSfaStage, &tma_sfa, full_bar(i), (kt0 + i) * 16, m0);
+        tma_load_2d(st + L::offSfbStage, &tma_sfb, full_bar(i), (kt0 + i) * 16, n0);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1439,8 +1442,12 @@ cudaLaunchConfig_t launch_config(int grid, int cluster, size_t smem, cudaStream_
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // set-up (barriers, TMEM) may overlap the previous kernel; every thread
+  // waits for it (pdl_wait) before touching global memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -1483,7 +1490,7 @@ int active_clusters(int cluster, size_t smem) {
     if (cache_dev[i] == dev && cache_cluster[i] == cluster && cache_smem[i] == smem) return cache_ok[i];
   int ok = 0;
   if (configure<BN, KMAX>(smem, cluster) == cudaSuccess) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(cluster, cluster, smem, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN, KMAX>, &cfg) == cudaSuccess && n > 0) ok = n;
@@ -1505,7 +1512,7 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const C
                            size_t smem, cudaStream_t stream) {
   const cudaError_t e = configure<BN, KMAX>(smem, cluster);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(grid, cluster, smem, stream, attr);
   count_launch();
   return cudaLaunchKernelEx(&cfg, gemm_topk_kernel<BN, KMAX>, ma, mb, msa, msb, p);

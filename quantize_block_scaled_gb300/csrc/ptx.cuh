@@ -59,6 +59,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel in the stream ends;
+// wait() returns once that kernel has completed and its writes are visible
+// (at once when there is no such predecessor).  launch_dependents() lets the
+// next kernel start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- async copies
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`

@@ -74,6 +74,7 @@ constexpr int kAmaxUnroll = 8;  // 16-byte loads in flight per thread
 __global__ void __launch_bounds__(kThreads, 4)
     amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t vpr, int64_t ld,
                 float* __restrict__ gs_out, Workspace* __restrict__ ws) {
+  ptx::pdl_launch_dependents();  // a dependent kernel may set up while this one runs
   uint32_t m2 = 0;
   const int64_t total = rows * vpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t bpr, int64_t ld,
                     uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                     const float* __restrict__ gs_ptr) {
+  ptx::pdl_launch_dependents();
   const int64_t total = rows * bpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     deinterleave_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t inter,
                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                  const float* __restrict__ gs_ptr) {
+  ptx::pdl_launch_dependents();
   const int64_t cpr = inter / 16;  // 32-element input chunks per row
   const int64_t total = rows * cpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -393,6 +396,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
     quantize_onepass_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t upr, int64_t ld,
                             int64_t units_per_cta, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                             float* __restrict__ gs_out, Workspace* __restrict__ ws) {
+  ptx::pdl_launch_dependents();
   constexpr int kUnitElems = G == 0 ? 16 : 32;
   constexpr uint32_t kUnitBytes = kUnitElems * 2;
   extern __shared__ __align__(128) uint8_t smem[];
