@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   const int64_t n_units = u1 > u0 ? u1 - u0 : 0;
   const uint32_t bar_a = ptx::smem_addr(&bar);
   const uint32_t dst0 = ptx::smem_addr(smem);
+  ptx::pdl_wait();  // launched early after the previous kernel: its writes are complete now
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_a, 1);
     ptx::fence_mbar_init();
@@ -571,18 +572,22 @@ bool launch_onepass(const uint16_t* x, int64_t rows, int64_t upr, int64_t ld, ui
   cfg.blockDim = dim3(kOnePassThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (cluster) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(grid);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the small cluster may start while the previous kernel finishes (the
+    // kernel waits for it before touching global memory)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
   } else {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
   }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster ? 2 : 1;
   if (cluster) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
