@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 // gs from the complete maximum exactly as the amax kernel does, and
 // quantizes its slice from shared memory.  x is read from HBM once.  The
 // last CTA to finish re-zeroes the workspace counters.
-constexpr int kOnePassThreads = 256;
+constexpr int kOnePassThreads = 512;
 constexpr uint32_t kOnePassMaxBytes = 200 * 1024;  // input bytes one CTA holds
 constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s of SM clock
 
