@@ -66,6 +66,7 @@ def _load():
             "orc_gemm_logits": (None, [P, P, F, P, P, F, I64, I64, I64, I64, P]),
             "orc_epilogue": (None, [P, I64, I64, ctypes.c_int, P, P, P]),
             "orc_topk": (None, [P, P, I64, I64, ctypes.c_int, P, P, P]),
+            "orc_normalize_topk_weights": (None, [P, P, I64, ctypes.c_int]),
             "orc_gemm_topk_rows": (None, [P, P, F, P, P, F, I64, I64, ctypes.c_int, P,
                                           ctypes.c_int, I64, I64, P, P, P]),
         }
@@ -204,6 +205,15 @@ def topk(score: np.ndarray, k: int, weight=None):
     return idx, val, wout
 
 
+def normalize_topk_weights(idx: np.ndarray, weight: np.ndarray) -> np.ndarray:
+    """Router gating normalisation (epilogue 2): each row's selected weights over their sum."""
+    idx = _c(idx, np.int32)
+    w = _c(weight, np.float32).copy()
+    rows, k = idx.shape
+    _load().orc_normalize_topk_weights(_ptr(idx), _ptr(w), rows, int(k))
+    return w
+
+
 def gemm_topk(qa, sfa, gsa, qb, sfb, gsb, kind: int, bias, k: int,
               row_begin: int = 0, row_end: int | None = None, threads: int = 1):
     """GEMM + epilogue + top-k over rows [row_begin, row_end); optional row-parallel threads."""
@@ -213,7 +223,7 @@ def gemm_topk(qa, sfa, gsa, qb, sfb, gsb, kind: int, bias, k: int,
     row_end = M if row_end is None else row_end
     rows = row_end - row_begin
     bias_c = None if bias is None else _c(bias, np.float32)
-    if kind == 1 and bias_c is None:
+    if kind in (1, 2) and bias_c is None:
         bias_c = np.zeros(N, np.float32)
     idx = np.zeros((rows, k), np.int32)
     val = np.zeros((rows, k), np.float32)

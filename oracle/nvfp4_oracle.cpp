@@ -24,7 +24,10 @@
 //   GEMM scaling         page "commit 107d62d / single_shot_inference.py",
 //                        global-scale commit ((A*SFA)@(B*SFB), then gsa*gsb)
 //   router epilogue      same commit (sqrt(softplus(logit*gsa*gsb))) and
-//                        CORRECTNESS_BACKLOG.md section 5 (+ e_bias, top-k)
+//                        CORRECTNESS_BACKLOG.md section 5 (+ e_bias, top-k);
+//                        the V4-Pro router variant (384 experts, top-6) is
+//                        in the compare view's model notes; its gating-weight
+//                        normalisation is not spelled out (reading below)
 //   deinterleave         page "commit 0d1cd1e", fused_deinterleave commit;
 //                        docs/PERFORMANCE_AUDIT.md P1 (granularity 8)
 //
@@ -34,7 +37,8 @@
 // E2M1 round-to-nearest-even with saturation to 6, sign bit kept (a
 // negative value that rounds to zero encodes as 0x8); a block whose scale
 // byte is zero encodes every element as a signed zero; the even element of a
-// pair goes to the low nibble; softplus(z) = z for z > 20.
+// pair goes to the low nibble; softplus(z) = z for z > 20; normalised
+// router weights (epilogue 2) are the selected weights over their sum.
 //
 // Floating point: every FP32 step is one IEEE single operation (compile with
 // -ffp-contract=off and without fast-math); the GEMM accumulates in double.
@@ -301,6 +305,22 @@ void orc_topk(const float* score, const float* weight, int64_t rows, int64_t N, 
   }
 }
 
+// Gating-weight normalisation of a router's top-k (epilogue 2): each row's
+// selected weights divided by their sum, so they add up to one (the pages
+// name the router variants but give no formula; this is the reading taken).
+// Sum and quotients in double, stored as float; empty slots (index -1) stay
+// 0 and do not count.
+void orc_normalize_topk_weights(const int32_t* idx, float* weight, int64_t rows, int k) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double sum = 0.0;
+    for (int t = 0; t < k; ++t)
+      if (idx[r * k + t] >= 0) sum += weight[r * k + t];
+    if (sum <= 0.0) continue;
+    for (int t = 0; t < k; ++t)
+      if (idx[r * k + t] >= 0) weight[r * k + t] = static_cast<float>(weight[r * k + t] / sum);
+  }
+}
+
 // The whole GEMM + epilogue + top-k for rows [row_begin, row_end).
 void orc_gemm_topk_rows(const uint8_t* qa, const uint8_t* sfa, float gsa,
                         const uint8_t* qb, const uint8_t* sfb, float gsb,
@@ -312,8 +332,9 @@ void orc_gemm_topk_rows(const uint8_t* qa, const uint8_t* sfa, float gsa,
   std::vector<float> score(static_cast<size_t>(rows * N));
   std::vector<float> weight(static_cast<size_t>(rows * N));
   orc_gemm_logits(qa, sfa, gsa, qb, sfb, gsb, N, K, row_begin, row_end, logits.data());
-  orc_epilogue(logits.data(), rows, N, epilogue, bias, score.data(), weight.data());
+  orc_epilogue(logits.data(), rows, N, epilogue == 2 ? 1 : epilogue, bias, score.data(), weight.data());
   orc_topk(score.data(), weight.data(), rows, N, k, idx_out, score_out, weight_out);
+  if (epilogue == 2 && weight_out) orc_normalize_topk_weights(idx_out, weight_out, rows, k);
 }
 
 }  // extern "C"

@@ -15,6 +15,7 @@ import torch
 
 import oracle
 from conftest import read_golden
+import workloads
 from workloads import bf16_bits, bf16_to_f32
 
 E2M1_TABLE = {int(c, 2): float(v) for c, v in read_golden("e2m1_table.txt")}
@@ -348,3 +349,30 @@ def test_gemm_topk_composes_steps():
         np.testing.assert_array_equal(wt[r], weight[r, ref])
     idx2, _, _ = oracle.gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, d["bias"], d["k"], threads=3)
     np.testing.assert_array_equal(idx, idx2)
+
+
+def test_router_weight_normalisation():
+    # Epilogue 2: the selected weights of a row divided by their sum.  Worked
+    # by hand: weights 1, 3, 4 (plus an empty slot) -> 1/8, 3/8, 4/8, 0.
+    idx = np.array([[5, 2, 9, -1]], np.int32)
+    w = np.array([[1.0, 3.0, 4.0, 0.0]], np.float32)
+    out = oracle.normalize_topk_weights(idx, w)
+    assert out.tolist() == [[0.125, 0.375, 0.5, 0.0]]
+    # a row of one: weight 1; an all-empty row stays as it is
+    idx = np.array([[7, -1], [-1, -1]], np.int32)
+    w = np.array([[0.3, 0.0], [0.0, 0.0]], np.float32)
+    assert oracle.normalize_topk_weights(idx, w).tolist() == [[1.0, 0.0], [0.0, 0.0]]
+
+
+def test_gemm_topk_epilogue2_is_epilogue1_then_normalised():
+    rng = np.random.default_rng(77)
+    xa = workloads.bf16_bits(rng.standard_normal((3, 128)).astype(np.float32))
+    xb = workloads.bf16_bits((rng.standard_normal((40, 128)) * 0.05).astype(np.float32))
+    bias = (rng.standard_normal(40) * 0.01).astype(np.float32)
+    qa, sfa, gsa = oracle.quantize(xa)
+    qb, sfb, gsb = oracle.quantize(xb)
+    i1, s1, w1 = oracle.gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, bias, 6)
+    i2, s2, w2 = oracle.gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 2, bias, 6)
+    assert np.array_equal(i1, i2) and np.array_equal(s1, s2)
+    np.testing.assert_allclose(w2, w1 / w1.sum(axis=1, keepdims=True), rtol=1e-6)
+    np.testing.assert_allclose(w2.sum(axis=1), 1.0, rtol=1e-6)
