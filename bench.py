@@ -391,6 +391,24 @@ def secondary(nv, ws, pk, flush):
     by = gemm_bytes(M, N, K, k, bias=False) - M * k * 4
     out["indexer_M64_N2048_k512"] = dict(us=round(ti * 1e6, 2), hbm_frac=round(by / ti / hbm, 4),
                                          rows_per_s=round(M / ti, 1))
+    # router variant: 384 experts, top-6, normalised gating weights (decode, T = 32)
+    rng = np.random.default_rng(384)
+    E, kv = 384, 6
+    xv = torch.from_numpy(workloads.bf16_bits(rng.standard_normal((32, HIDDEN), np.float32))
+                          .view(np.int16)).cuda()
+    wv = torch.from_numpy(workloads.bf16_bits(rng.standard_normal((E, HIDDEN), np.float32) * np.float32(0.02))
+                          .view(np.int16)).cuda()
+    bv = torch.from_numpy((rng.standard_normal(E) * 0.01).astype(np.float32)).cuda()
+    qa, sfa, gsa = nv.quantize(xv, ws)
+    qb, sfb, gsb = nv.quantize(wv, ws)
+    idx = torch.empty(32, kv, dtype=torch.int32, device="cuda")
+    sc = torch.empty(32, kv, dtype=torch.float32, device="cuda")
+    wt = torch.empty(32, kv, dtype=torch.float32, device="cuda")
+    tv = time_op_flushed(lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, nv.EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM,
+                                                   bv, kv, idx, sc, wt, None, ws), 30, flush)
+    by = gemm_bytes(32, E, HIDDEN, kv)
+    out["router_E384_k6_norm_decode_T32"] = dict(us=round(tv * 1e6, 2), hbm_frac=round(by / tv / hbm, 4),
+                                                 rows_per_s=round(32 / tv, 1))
     torch.cuda.synchronize()
     return out
 

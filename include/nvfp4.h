@@ -59,7 +59,10 @@ typedef enum nvfp4_epilogue {
   /* score = logit (indexer-shaped scoring) */
   NVFP4_EPILOGUE_IDENTITY = 0,
   /* weight = sqrt(softplus(logit)), score = weight + bias[n] (router-shaped) */
-  NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS = 1
+  NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS = 1,
+  /* as 1, and each row's k output weights are divided by their sum (the
+   * router variant with normalised gating weights; k <= 32) */
+  NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM = 2
 } nvfp4_epilogue;
 
 /* Device-side status bits a kernel may record in the workspace. */
@@ -129,6 +132,10 @@ int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, 
  *   epilogue IDENTITY:           weight = score = logit
  *   epilogue SQRT_SOFTPLUS_BIAS: weight = sqrt(softplus(logit)),
  *                                score  = weight + bias[n]
+ *   epilogue SQRT_SOFTPLUS_BIAS_NORM: as above, then the k selected weights
+ *                                of a row are divided by their sum (the
+ *                                pages name this router variant without a
+ *                                formula; this is the reading taken)
  *   per row m: the k largest scores, in descending order; equal scores are
  *   ordered by lower n.
  *
@@ -138,7 +145,8 @@ int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, 
  * M >= 0 (M == 0 launches nothing; qa, sfa and the outputs may then be NULL),
  * N >= 1, K a positive multiple of 64.  1 <= k <= 1024; for k > 32
  * the N scores of a row must fit on chip (N <= 4096).
- * bias: N floats, required for SQRT_SOFTPLUS_BIAS, ignored for IDENTITY.
+ * bias: N floats, required for the SQRT_SOFTPLUS epilogues, ignored for
+ * IDENTITY.  SQRT_SOFTPLUS_BIAS_NORM takes k <= 32.
  * Outputs, each [M, k] row-major: topk_idx (int32), topk_score (float),
  * topk_weight (float, may be NULL).  Slots beyond N hold idx -1,
  * score -inf, weight 0.

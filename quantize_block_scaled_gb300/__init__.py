@@ -29,6 +29,7 @@ LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
 
 EPILOGUE_IDENTITY = 0
 EPILOGUE_SQRT_SOFTPLUS_BIAS = 1
+EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM = 2
 DEVICE_TIMEOUT = 0x1
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or alignment",

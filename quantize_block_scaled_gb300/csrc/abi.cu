@@ -116,12 +116,14 @@ int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa, con
     return NVFP4_ERR_INVALID;
   if (M < 0 || N < 1 || K < 1 || M > kInt32Max || N > kInt32Max || K > kInt32Max)
     return NVFP4_ERR_INVALID;
-  if (epilogue != NVFP4_EPILOGUE_IDENTITY && epilogue != NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS)
+  if (epilogue != NVFP4_EPILOGUE_IDENTITY && epilogue != NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS &&
+      epilogue != NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM)
     return NVFP4_ERR_INVALID;
-  if (epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS && bias == nullptr) return NVFP4_ERR_INVALID;
+  if (epilogue != NVFP4_EPILOGUE_IDENTITY && bias == nullptr) return NVFP4_ERR_INVALID;
   if (k < 1 || k > 1024) return NVFP4_ERR_INVALID;
   if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
   if (k > 32 && N > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM && k > 32) return NVFP4_ERR_UNSUPPORTED;
   if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sfa, 4) || !aligned(sfb, 4) ||
       !aligned(gsa, 4) || !aligned(gsb, 4) || !aligned(topk_idx, 4) || !aligned(topk_score, 4) ||
       (topk_weight != nullptr && !aligned(topk_weight, 4)) || (logits != nullptr && !aligned(logits, 4)) ||

@@ -82,7 +82,7 @@ constexpr uint32_t kCtrlBytes = 256;
 // control block: 3 barriers per stage and 4 more, then the TMEM address at byte 128
 static_assert((3 * kMaxStages + 4) * 8 <= 128, "barriers precede the TMEM slot");
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
-constexpr int kSmallCols = 8;        // reduce path, small rows: <= 8 columns per lane (N <= 256)
+constexpr int kSmallCols = 16;       // reduce path, small rows: <= 16 columns per lane (N <= 512)
 
 template <int BN>
 struct Layout {
@@ -129,7 +129,7 @@ struct Params {
   uint32_t recv_bytes;    // reduce path, bulk: bytes of that receive area (at the start of rowmem)
   uint32_t bias_off;      // reduce path: offset in rowmem of the staged biases (N floats)
   int rpc;                // rows per cluster tile (<= BM; smaller spreads few long rows over more clusters)
-  int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 256)
+  int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 512)
   int cand_cap;           // large path: power of two >= k
   uint32_t row_bytes;     // large path: bytes of one warp's key buffer (16-byte multiple)
 };
@@ -237,14 +237,34 @@ template <int KMAX>
 __device__ __forceinline__ void list_store(const Params& p, int64_t grow, const float (&tv)[KMAX],
                                            const int (&ti)[KMAX], const float (&tw)[KMAX]) {
   const int64_t o = grow * p.k;
+  // normalised router weights: over the sum of the selected ones, in slot order
+  float sum = 0.0f;
+  if (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM) {
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i)
+      if (i < p.k && ti[i] >= 0) sum += tw[i];
+  }
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) {
     if (i < p.k) {  // empty slots hold -1 / -inf / 0 already
       p.topk_idx[o + i] = ti[i];
       p.topk_score[o + i] = tv[i];
-      if (p.topk_weight) p.topk_weight[o + i] = tw[i];
+      if (p.topk_weight) p.topk_weight[o + i] = sum > 0.0f && ti[i] >= 0 ? tw[i] / sum : tw[i];
     }
   }
+}
+
+// Normalised router weights for rows whose weights are already in global
+// memory (k <= 32, one warp, after a block barrier).
+__device__ __forceinline__ void normalize_row_weights(const Params& p, int64_t grow) {
+  const uint32_t lane = lane_id();
+  const int64_t o = grow * p.k + lane;
+  const bool has = static_cast<int>(lane) < p.k && p.topk_idx[o] >= 0;
+  const float w = has ? p.topk_weight[o] : 0.0f;
+  float sum = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+  if (has && sum > 0.0f) p.topk_weight[o] = w / sum;
 }
 
 // ---------------------------------------------------------------- reduce-path rows
@@ -347,7 +367,7 @@ __device__ __forceinline__ void merge_top8_pay(uint64_t (&r)[8], float (&rw)[8],
   ce_pay(r[4], rw[4], r[5], rw[5]); ce_pay(r[6], rw[6], r[7], rw[7]);
 }
 
-// Reduce path with k <= 32 and N <= 256, where the K split is at least 2.
+// Reduce path with k <= 32 and N <= 512, where the K split is at least 2.
 // Step 1, every thread of the CTA: sum the K slices of each (owned row,
 // 4-column group) in slice order, apply the epilogue, and leave the score in
 // slice 0 and the unbiased weight in slice 1 of the receive area (each cell
@@ -356,7 +376,7 @@ __device__ __forceinline__ void merge_top8_pay(uint64_t (&r)[8], float (&rw)[8],
 __device__ void rows_small(const Params& p, const RowCtx& c, int owned, int64_t grow0) {
   const uint32_t lane = lane_id();
   const int warp = static_cast<int>(threadIdx.x >> 5);
-  const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
+  const bool router = p.epilogue != NVFP4_EPILOGUE_IDENTITY;
   const int slice = c.ro * c.rs;  // floats per K slice
   const int groups = (p.N + 3) >> 2;
   for (int it = static_cast<int>(threadIdx.x); it < owned * groups; it += kThreads) {
@@ -393,14 +413,25 @@ __device__ void rows_small(const Params& p, const RowCtx& c, int owned, int64_t 
     uint64_t mine = 0ull;  // this lane's output slot: (score key, column) entry
     float mine_w = 0.0f;
     if (p.k <= 8) {
-      // Selection on 32-bit keys: the score key's top 24 bits and 255 - column.
-      // Exact ties still go to the lower column; scores closer than 2^-15
+      // Selection on 32-bit keys: the score key's top 23 bits and 511 - column.
+      // Exact ties still go to the lower column; scores closer than 2^-14
       // relative may trade places at the boundary (a near-tie).
       uint32_t e[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int n = static_cast<int>(lane) + 32 * i;
-        e[i] = n < p.N ? ((float_key(S[n]) & 0xFFFFFF00u) | (255u - static_cast<uint32_t>(n))) : 0u;
+        e[i] = n < p.N ? ((float_key(S[n]) & 0xFFFFFE00u) | (511u - static_cast<uint32_t>(n))) : 0u;
+      }
+      if (p.N > 256) {  // warp-uniform: columns lane + 256 + 32 i too; keep the lane's best 8
+        uint32_t f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int n = static_cast<int>(lane) + 256 + 32 * i;
+          f[i] = n < p.N ? ((float_key(S[n]) & 0xFFFFFE00u) | (511u - static_cast<uint32_t>(n))) : 0u;
+        }
+        sort8_desc(e);
+        sort8_desc(f);
+        merge_top8(e, f);
       }
       warp_top8_u32(e);  // every lane now holds the same 8 picks
       // pick lane & 7 through a select tree on its bits (a chain of equality
@@ -411,7 +442,7 @@ __device__ void rows_small(const Params& p, const RowCtx& c, int owned, int64_t 
       const uint32_t key = b2 ? (b1 ? x3 : x2) : (b1 ? x1 : x0);
       // Exact score and weight of pick lane (lanes 0..7), then an exact
       // bitonic sort of those eight entries across the lanes.
-      const int n = 255 - static_cast<int>(key & 0xFFu);
+      const int n = 511 - static_cast<int>(key & 0x1FFu);
       const bool has = lane < 8 && key != 0u;
       mine = has ? entry(S[n], n) : 0ull;
       mine_w = has ? W[n] : 0.0f;
@@ -455,6 +486,12 @@ __device__ void rows_small(const Params& p, const RowCtx& c, int owned, int64_t 
           mine_w = W[entry_col(best)];
         }
       }
+    }
+    if (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM) {  // warp-uniform
+      float sum = static_cast<int>(lane) < want ? mine_w : 0.0f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+      if (sum > 0.0f) mine_w = mine_w / sum;
     }
     if (static_cast<int>(lane) < p.k) {
       const int64_t o = grow * p.k + lane;
@@ -526,7 +563,7 @@ __device__ __forceinline__ void store_entry(const Params& p, const RowCtx& c, in
   p.topk_idx[o] = n;
   p.topk_score[o] = sc;
   if (p.topk_weight)
-    p.topk_weight[o] = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS ? router_weight(row_logit(c, rr, n)) : sc;
+    p.topk_weight[o] = p.epilogue != NVFP4_EPILOGUE_IDENTITY ? router_weight(row_logit(c, rr, n)) : sc;
 }
 
 __device__ __forceinline__ void store_empty(const Params& p, int64_t o) {
@@ -608,7 +645,7 @@ __device__ void sort_runs_and_store(const Params& p, const RowCtx& c, int rr, in
   }
 }
 
-// General rows (k > 32 or N > 256), every thread of the CTA on one row at a
+// General rows (k > 32 or N > 512), every thread of the CTA on one row at a
 // time: keys of all N scores in shared memory; the want-th largest key T by
 // a search over 2-bit digits (per digit, the counts of keys >= each of three
 // thresholds); the keys above T and the lowest-column keys equal to T in
@@ -621,7 +658,7 @@ __device__ void rows_large(const Params& p, const RowCtx& c, int owned, int64_t 
   const int tid = static_cast<int>(threadIdx.x);
   const int n_all = p.N;
   const int n4 = (n_all + 3) >> 2;  // key quads (keys past N are 0, below every real key)
-  const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
+  const bool router = p.epilogue != NVFP4_EPILOGUE_IDENTITY;
   const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
   const uint32_t want = static_cast<uint32_t>(p.k < n_all ? p.k : n_all);
   const int qp = (n4 + kThreads - 1) / kThreads;  // quads per thread, in column order
@@ -745,6 +782,8 @@ __device__ void rows_large(const Params& p, const RowCtx& c, int owned, int64_t 
       default: sort_runs_and_store<8>(p, c, rr, grow, cand); break;
     }
     __syncthreads();  // keys and candidates are rewritten for the next row
+    if (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM && p.topk_weight && warp == 0)
+      normalize_row_weights(p, grow);  // k <= 32 (the outputs are visible after the barrier)
   }
 }
 
@@ -993,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(xdrain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
     }
     __syncwarp();
-    if (!p.direct && p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS) {
+    if (!p.direct && p.epilogue != NVFP4_EPILOGUE_IDENTITY) {
       // The row phase reads every bias of the row: stage them while the MMAs run.
       float* bias_s = reinterpret_cast<float*>(rowmem + p.bias_off);
       for (int n = (warp - 2) * 32 + static_cast<int>(lane); n < p.N; n += 128) bias_s[n] = __ldg(p.bias + n);
@@ -1016,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float tv[KMAX], tw[KMAX];
       int ti[KMAX];
       list_init<KMAX>(tv, ti, tw);
-      const bool router = p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS;
+      const bool router = p.epilogue != NVFP4_EPILOGUE_IDENTITY;
       // This warp's copy of the bias of the CTA's columns (stage region is free now).
       float* bias_s = reinterpret_cast<float*>(smem) + (warp - 2) * BN;
       if (router)

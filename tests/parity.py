@@ -30,8 +30,13 @@ def assert_close(got, ref, what=""):
                              f"gpu {got[tuple(i)]!r} oracle {ref[tuple(i)]!r}")
 
 
-def assert_topk(gpu_idx, gpu_score, gpu_weight, ref_score_rows, ref_weight_rows, k, what=""):
-    """Check GPU top-k of each row against the oracle's full score rows."""
+def assert_topk(gpu_idx, gpu_score, gpu_weight, ref_score_rows, ref_weight_rows, k, what="",
+                normalized=False):
+    """Check GPU top-k of each row against the oracle's full score rows.
+
+    normalized: the weights are the router's normalised gating weights, so
+    the reference is the oracle's weights of the GPU's picks over their sum.
+    """
     gpu_idx = np.asarray(gpu_idx)
     gpu_score = np.asarray(gpu_score)
     rows, N = ref_score_rows.shape
@@ -54,7 +59,8 @@ def assert_topk(gpu_idx, gpu_score, gpu_weight, ref_score_rows, ref_weight_rows,
         if gpu_weight is not None and ref_weight_rows is not None:
             W = ref_weight_rows[r].astype(np.float64)
             gw = np.asarray(gpu_weight)[r][:take].astype(np.float64)
-            assert (np.abs(gw - W[gi]) <= tol(W[gi])).all(), f"{what} row {r}: weight mismatch"
+            ref_w = W[gi] / W[gi].sum() if normalized else W[gi]
+            assert (np.abs(gw - ref_w) <= tol(ref_w)).all(), f"{what} row {r}: weight mismatch"
         # order: non-increasing, ties by increasing index
         assert (np.diff(gs) <= 0).all(), f"{what} row {r}: scores not descending"
         same = np.diff(gs) == 0

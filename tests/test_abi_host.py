@@ -89,8 +89,10 @@ def _gemm(L, M=4, N=64, K=512, epilogue=1, bias=FAKE, k=6, qa=FAKE, sfa=FAKE, ws
 def test_gemm_validation(L):
     assert _gemm(L, k=0) == 1
     assert _gemm(L, k=1025) == 1
-    assert _gemm(L, epilogue=2) == 1
-    assert _gemm(L, epilogue=1, bias=0) == 1       # router epilogue needs a bias
+    assert _gemm(L, epilogue=3) == 1
+    assert _gemm(L, epilogue=1, bias=0) == 1       # router epilogues need a bias
+    assert _gemm(L, epilogue=2, bias=0) == 1
+    assert _gemm(L, epilogue=2, k=40) == 2         # normalised weights: k <= 32
     assert _gemm(L, M=-1) == 1
     assert _gemm(L, N=0) == 1
     assert _gemm(L, K=480) == 2                    # K must be a multiple of 64

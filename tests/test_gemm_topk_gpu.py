@@ -50,7 +50,7 @@ def run_gpu(nv, ws, qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, logits=True):
 def oracle_rows(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, rows):
     """Oracle logits / scores / weights for a list of row indices."""
     lg = np.concatenate([oracle.gemm_logits(qa, sfa, gsa, qb, sfb, gsb, r, r + 1) for r in rows])
-    score, weight = oracle.epilogue(lg, epilogue, bias)
+    score, weight = oracle.epilogue(lg, 1 if epilogue == 2 else epilogue, bias)
     return lg, score, weight
 
 
@@ -60,7 +60,7 @@ def check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, rows=None,
     idx, score, weight, lg = run_gpu(nv, ws, qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k)
     rlg, rscore, rweight = oracle_rows(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, rows)
     assert_close(lg[rows], rlg, f"{what} logits")
-    assert_topk(idx[rows], score[rows], weight[rows], rscore, rweight, k, what)
+    assert_topk(idx[rows], score[rows], weight[rows], rscore, rweight, k, what, normalized=epilogue == 2)
     assert nv.read_device_status(ws) == 0
     return idx, score
 
@@ -161,6 +161,31 @@ def test_many_row_tiles(nv, ws, M, N, K, k, epi):
     rows = sorted(set(range(0, 130)) | set(range(M - 70, M)) | set(rng.integers(0, M, 200).tolist()))
     check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, epi, bias, k, rows=rows,
                what=f"wide {M}x{N}x{K} k={k}")
+
+
+# Router variant with normalised gating weights (epilogue 2): 384 experts,
+# top-6, on the decode and prefill paths, plus wider rows and k > 8.
+VARIANTS = [
+    # M, N, K, k
+    (1, 384, 7168, 6),       # decode: K split, 16 columns per lane
+    (32, 384, 7168, 6),
+    (2048, 384, 1024, 6),    # direct epilogue, two 256-column CTAs per tile
+    (64, 400, 512, 20),      # K split, arg-max rounds over 16 columns per lane
+    (40, 640, 256, 6),       # N > 512: block-wide selection
+]
+
+
+@pytest.mark.parametrize("M,N,K,k", VARIANTS)
+def test_router_variant_normalised(nv, ws, M, N, K, k):
+    rng = np.random.default_rng(M * 3 + N + K)
+    xa = workloads.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    xb = workloads.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    bias = (rng.standard_normal(N) * 0.01).astype(np.float32)
+    qa, sfa, gsa = quantized(xa)
+    qb, sfb, gsb = quantized(xb)
+    rows = None if M <= 64 else sorted(set(range(0, 96)) | set(range(M - 32, M)))
+    idx, _ = check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, 2, bias, k, rows=rows,
+                        what=f"variant {M}x{N}x{K} k={k}")
 
 
 @pytest.mark.parametrize("k", [4, 40])
