@@ -67,6 +67,8 @@ def _load():
             "orc_epilogue": (None, [P, I64, I64, ctypes.c_int, P, P, P]),
             "orc_topk": (None, [P, P, I64, I64, ctypes.c_int, P, P, P]),
             "orc_normalize_topk_weights": (None, [P, P, I64, ctypes.c_int]),
+            "orc_rmsnorm": (None, [P, I64, I64, I64, P, F, P]),
+            "orc_rmsnorm_quantize": (None, [P, I64, I64, I64, P, F, P, P, P]),
             "orc_gemm_topk_rows": (None, [P, P, F, P, P, F, I64, I64, ctypes.c_int, P,
                                           ctypes.c_int, I64, I64, P, P, P]),
         }
@@ -203,6 +205,28 @@ def topk(score: np.ndarray, k: int, weight=None):
     wout = np.zeros((rows, k), np.float32)
     _load().orc_topk(_ptr(score), _ptr(w), rows, N, int(k), _ptr(idx), _ptr(val), _ptr(wout))
     return idx, val, wout
+
+
+def rmsnorm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """bf16 bits of RMSNorm(x) * weight (x, weight: bf16 bits), the oracle's op order."""
+    x = _c(x, np.uint16)
+    w = _c(weight, np.uint16)
+    rows, cols = x.shape
+    out = np.zeros((rows, cols), np.uint16)
+    _load().orc_rmsnorm(_ptr(x), rows, cols, cols, _ptr(w), float(eps), _ptr(out))
+    return out
+
+
+def rmsnorm_quantize(x: np.ndarray, weight: np.ndarray, eps: float):
+    """RMSNorm to bf16, then NVFP4 quantize: (codes, scales, gs)."""
+    x = _c(x, np.uint16)
+    w = _c(weight, np.uint16)
+    rows, cols = x.shape
+    q = np.zeros((rows, cols // 2), np.uint8)
+    sf = np.zeros((rows, cols // 16), np.uint8)
+    gs = np.zeros(1, np.float32)
+    _load().orc_rmsnorm_quantize(_ptr(x), rows, cols, cols, _ptr(w), float(eps), _ptr(q), _ptr(sf), _ptr(gs))
+    return q, sf, gs[0]
 
 
 def normalize_topk_weights(idx: np.ndarray, weight: np.ndarray) -> np.ndarray:

@@ -191,6 +191,64 @@ void orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
   orc_quantize_rows(x, cols, ld, gs, 0, rows, q, sf);
 }
 
+// bf16 bits of a float, rounded to nearest even (finite inputs).
+uint16_t bf16_round(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof(u));
+  const uint32_t rounded = u + 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(rounded >> 16);
+}
+
+// RMSNorm of each row to bf16, as the producer of the quantize input (page
+// "compare ... v-official-encoding-path": fused RMSNorm + NVFP4 quantize,
+// PERFORMANCE_AUDIT.md P4; the norm is input * inv_rms * weight[c]).  The
+// pages fix neither epsilon nor the summation order; the readings taken:
+//   sum of squares: each 16-element block accumulated in order with fused
+//     multiply-adds from 0; the block sums combined pairwise, level by level
+//     (entry j of the next level is p[2j] + p[2j+1], or p[2j] alone at an
+//     odd end) down to one value;
+//   inv_rms = 1 / sqrt(sum / cols + eps), each step one FP32 operation;
+//   y = (x * inv_rms) * weight[c] in FP32, rounded to bf16 (the model's
+//     hidden-state type), which is what gets quantized.
+void orc_rmsnorm(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const uint16_t* weight,
+                 float eps, uint16_t* out) {
+  const int64_t nb = cols / 16;
+  std::vector<float> level(static_cast<size_t>(nb));
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * ld;
+    for (int64_t b = 0; b < nb; ++b) {
+      float acc = 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        const float v = bf16_value(xr[b * 16 + i]);
+        acc = std::fma(v, v, acc);
+      }
+      level[b] = acc;
+    }
+    int64_t n = nb;
+    while (n > 1) {
+      const int64_t half = (n + 1) / 2;
+      for (int64_t j = 0; j < half; ++j)
+        level[j] = (2 * j + 1 < n) ? level[2 * j] + level[2 * j + 1] : level[2 * j];
+      n = half;
+    }
+    const float sum = nb > 0 ? level[0] : 0.0f;
+    const float mean = sum / static_cast<float>(cols);
+    const float inv_rms = 1.0f / std::sqrt(mean + eps);
+    for (int64_t c = 0; c < cols; ++c) {
+      const float y = (bf16_value(xr[c]) * inv_rms) * bf16_value(weight[c]);
+      out[r * cols + c] = bf16_round(y);
+    }
+  }
+}
+
+// RMSNorm, then quantize the [rows, cols] bf16 result as a whole.
+void orc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                          const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs_out) {
+  std::vector<uint16_t> tmp(static_cast<size_t>(rows * cols));
+  orc_rmsnorm(x, rows, cols, ld, weight, eps, tmp.data());
+  orc_quantize(tmp.data(), rows, cols, cols, q, sf, gs_out);
+}
+
 // Deinterleave one [rows, 2I] matrix whose gate/up columns alternate in
 // groups of g: output column j < I is gate column j, taken from input column
 // 2g*floor(j/g) + (j mod g); output column I + j is up column j, taken from

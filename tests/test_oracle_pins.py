@@ -376,3 +376,51 @@ def test_gemm_topk_epilogue2_is_epilogue1_then_normalised():
     assert np.array_equal(i1, i2) and np.array_equal(s1, s2)
     np.testing.assert_allclose(w2, w1 / w1.sum(axis=1, keepdims=True), rtol=1e-6)
     np.testing.assert_allclose(w2.sum(axis=1), 1.0, rtol=1e-6)
+
+
+# ---- RMSNorm producer of the quantize input (fused RMSNorm + quantize)
+
+def _bf16(vals):
+    return bf16_bits(np.asarray(vals, np.float32))
+
+
+def test_rmsnorm_worked_row():
+    # x = [3, 4, 0 x 14], weight 1, eps 0: sum 25, mean 25/16, rms 1.25,
+    # y = [2.4, 3.2, 0 ...] -> bf16 2.40625, 3.203125 (round to nearest even)
+    x = _bf16([[3.0, 4.0] + [0.0] * 14])
+    w = _bf16(np.ones(16))
+    y = bf16_to_f32(oracle.rmsnorm(x, w, 0.0))
+    assert y[0, 0] == 2.40625 and y[0, 1] == 3.203125 and (y[0, 2:] == 0).all()
+
+
+def test_rmsnorm_constant_row_and_weight_scaling():
+    # a constant row normalises to ~1 (eps 1e-6 makes it 0.99999988 -> bf16 1.0);
+    # a weight of 2 (a power of two) doubles every output exactly
+    x = _bf16(np.full((2, 64), 2.0))
+    y1 = bf16_to_f32(oracle.rmsnorm(x, _bf16(np.ones(64)), 1e-6))
+    y2 = bf16_to_f32(oracle.rmsnorm(x, _bf16(np.full(64, 2.0)), 1e-6))
+    assert (y1 == 1.0).all() and (y2 == 2.0).all()
+
+
+def test_rmsnorm_matches_double_precision_textbook():
+    # against sqrt(mean(x^2) + eps) in double on wide-range rows: within one
+    # bf16 rounding of the exact value (relative 2^-8), every element
+    rng = np.random.default_rng(31)
+    f = (rng.standard_normal((6, 7168)) * np.exp2(rng.integers(-8, 8, (6, 1)))).astype(np.float32)
+    x = bf16_bits(f)
+    wf = (1.0 + 0.2 * rng.standard_normal(7168)).astype(np.float32)
+    w = bf16_bits(wf)
+    xd = bf16_to_f32(x).astype(np.float64)
+    wd = bf16_to_f32(w).astype(np.float64)
+    ref = xd / np.sqrt((xd ** 2).mean(axis=1, keepdims=True) + 1e-6) * wd
+    y = bf16_to_f32(oracle.rmsnorm(x, w, 1e-6)).astype(np.float64)
+    assert (np.abs(y - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30).all()
+
+
+def test_rmsnorm_quantize_is_rmsnorm_then_quantize():
+    rng = np.random.default_rng(32)
+    x = bf16_bits(rng.standard_normal((5, 256)).astype(np.float32))
+    w = bf16_bits((1.0 + 0.1 * rng.standard_normal(256)).astype(np.float32))
+    q, sf, gs = oracle.rmsnorm_quantize(x, w, 1e-6)
+    rq, rsf, rgs = oracle.quantize(oracle.rmsnorm(x, w, 1e-6))
+    assert np.array_equal(q, rq) and np.array_equal(sf, rsf) and gs == rgs
