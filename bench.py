@@ -358,6 +358,17 @@ def secondary(nv, ws, pk, flush):
     sweep["deinterleave_T2048_g8"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1),
                                           hbm_frac=round(b / t / hbm, 3))
     del hh, q, sf, gs
+    # NEXT-2: RMSNorm fused into the quantize (the norm output never reaches HBM)
+    rng = np.random.default_rng(7)
+    wn = torch.from_numpy(workloads.bf16_bits((1.0 + 0.1 * rng.standard_normal(HIDDEN)).astype(np.float32))
+                          .view(np.int16)).cuda()
+    for T in (32, 2048):
+        x = torch.from_numpy(workloads.quantize_input(T).view(np.int16)).cuda()
+        q, sf, gs = nv.rmsnorm_quantize(x, wn, 1e-6, ws)
+        t = time_op_flushed(lambda: nv.nvfp4_rmsnorm_quantize(x, wn, 1e-6, q, sf, gs, ws), 30, flush)
+        b = quantize_bytes(T, HIDDEN) + HIDDEN * 2
+        sweep[f"rmsnorm_T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3))
+        del x, q, sf, gs
     out["quantize"] = sweep
     # router prefill T = 8192 (Student-t activations with outliers)
     d = workloads.router_prefill()

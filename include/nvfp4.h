@@ -9,6 +9,8 @@
  *                                global scale, E4M3 block scales, E2M1 codes
  *   nvfp4_deinterleave_quantize  the same for an interleaved SwiGLU gate/up
  *                                output, deinterleaved to [gate | up] first
+ *   nvfp4_rmsnorm_quantize       the same for RMSNorm(x) * weight, the
+ *                                norm fused in
  *   nvfp4_gemm_topk              block-scaled FP4 GEMM with a fused scoring
  *                                epilogue and per-row top-k
  *
@@ -118,6 +120,28 @@ int nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
 int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, int granularity,
                                 uint8_t* q, uint8_t* sf, float* gs,
                                 void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * RMSNorm fused into the activation quantize (the compare view's
+ * PERFORMANCE_AUDIT.md P4, "fuse RMSNorm into the next NVFP4 quantize";
+ * the norm is input * inv_rms * weight[c], as in the model notes' kv_norm):
+ *
+ *   per row: sum of squares in a fixed order (16-element blocks accumulated
+ *            with fused multiply-adds, block sums combined pairwise level by
+ *            level), inv_rms = 1 / sqrt(sum / cols + eps)          (FP32)
+ *   y[r, c] = bf16((x[r, c] * inv_rms) * weight[c])   (round to nearest even)
+ *   then exactly nvfp4_quantize of the bf16 matrix y, which never reaches
+ *   memory.
+ *
+ * x      : bf16 [rows, cols], row stride ld_x elements (16-byte aligned,
+ *          ld_x a multiple of 8).  weight: bf16 [cols], 16-byte aligned.
+ * cols   : multiple of 16, at most 16384.  eps >= 0 (finite).
+ * q, sf, gs: as for nvfp4_quantize.  One launch when the rows fit in the
+ *          SMs' shared memory (about 30 MB), else two row-parallel passes.
+ */
+int nvfp4_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
+                           const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Block-scaled FP4 GEMM + fused epilogue + per-row top-k.  Sources: the

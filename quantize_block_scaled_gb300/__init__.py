@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_status_string.argtypes = [I]
         L.nvfp4_last_cuda_error.restype = I
         L.nvfp4_last_cuda_error.argtypes = []
+        L.nvfp4_rmsnorm_quantize.restype = I
+        L.nvfp4_rmsnorm_quantize.argtypes = [P, I64, I64, I64, P, ctypes.c_float, P, P, P, P, SZ, P]
         L.nvfp4_kernel_launches.restype = ctypes.c_uint64
         L.nvfp4_kernel_launches.argtypes = []
         L.nvfp4_quantize_noalloc.restype = I
@@ -85,7 +87,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
                     "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
                     "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc",
-                    "nvfp4_kernel_launches")
+                    "nvfp4_kernel_launches", "nvfp4_rmsnorm_quantize")
 
 
 def _check(fn: str, status: int):
@@ -134,6 +136,25 @@ def nvfp4_quantize(x, q, sf, gs, ws, stream=None):
     _check("nvfp4_quantize", lib().nvfp4_quantize(
         _ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def nvfp4_rmsnorm_quantize(x, weight, eps, q, sf, gs, ws, stream=None):
+    x = _bf16_bits(x)
+    weight = _bf16_bits(weight)
+    rows, cols = x.shape
+    _check("nvfp4_rmsnorm_quantize", lib().nvfp4_rmsnorm_quantize(
+        _ptr(x), rows, cols, x.stride(0), _ptr(weight), float(eps), _ptr(q), _ptr(sf), _ptr(gs), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def rmsnorm_quantize(x, weight, eps, ws, stream=None):
+    """Allocating convenience: (q, sf, gs) of RMSNorm(x) * weight."""
+    rows, cols = x.shape
+    q = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=x.device)
+    gs = torch.empty(1, dtype=torch.float32, device=x.device)
+    nvfp4_rmsnorm_quantize(x, weight, eps, q, sf, gs, ws, stream)
+    return q, sf, gs
 
 
 def kernel_launches() -> int:

@@ -81,6 +81,22 @@ int nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, 
   return NVFP4_OK;
 }
 
+int nvfp4_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
+                           const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs, void* ws,
+                           size_t ws_bytes, cudaStream_t stream) {
+  if (gs == nullptr || weight == nullptr || (rows != 0 && (x == nullptr || q == nullptr || sf == nullptr)))
+    return NVFP4_ERR_INVALID;
+  if (rows < 0 || cols <= 0 || ld_x < cols || !(eps >= 0.0f) || eps > 3.4e38f) return NVFP4_ERR_INVALID;
+  if (cols % 16 != 0 || cols > 16384 || ld_x % 8 != 0 || !aligned(x, 16) || !aligned(weight, 16) ||
+      !aligned(q, 8) || !aligned(gs, 4))
+    return NVFP4_ERR_UNSUPPORTED;
+  const int st = check_workspace(ws, ws_bytes);
+  if (st != NVFP4_OK) return st;
+  const cudaError_t e = nvfp4::launch_rmsnorm_quantize(x, rows, cols, ld_x, weight, eps, q, sf, gs,
+                                                       static_cast<nvfp4::Workspace*>(ws), stream);
+  return e == cudaSuccess ? NVFP4_OK : cuda_failure(e);
+}
+
 int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, int granularity,
                                 uint8_t* q, uint8_t* sf, float* gs, void* ws, size_t ws_bytes,
                                 cudaStream_t stream) {

@@ -35,6 +35,12 @@ bool launch_deinterleave_onepass(const uint16_t* x, int64_t rows, int64_t inter,
                                  uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream,
                                  cudaError_t* err);
 
+// RMSNorm (bf16 out) fused into the quantize: one pass when the rows fit on
+// chip, else two row-parallel passes.
+cudaError_t launch_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                    const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs,
+                                    Workspace* ws, cudaStream_t stream);
+
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
                         Workspace* ws, cudaStream_t stream);
 

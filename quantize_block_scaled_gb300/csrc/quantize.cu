@@ -16,6 +16,8 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 #include "internal.h"
 #include "nvfp4.h"
 #include "ptx.cuh"
@@ -600,6 +602,350 @@ bool launch_onepass(const uint16_t* x, int64_t rows, int64_t upr, int64_t ld, ui
   return true;
 }
 
+// ---------------------------------------------------------------- RMSNorm + quantize
+
+// The quantize input produced by an RMSNorm: y = bf16((x * inv_rms) * w[c])
+// with inv_rms = 1 / sqrt(sum(x^2) / cols + eps), fused so that y never
+// reaches HBM (the compare view's PERFORMANCE_AUDIT.md P4).  The sum of
+// squares follows one fixed order: each 16-element block accumulated with
+// fused multiply-adds in element order, the block sums then combined
+// pairwise level by level (entry j of a level is the sum of entries 2j and
+// 2j + 1 of the level below, or entry 2j alone at an odd end).
+constexpr int kRmsMaxBlocks = 1024;  // 16-element blocks per row (cols <= 16384)
+
+__device__ __forceinline__ float sq_block(uint4 a, uint4 b) {
+  float acc = 0.0f;
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lo = lo_bf16(w[i]), hi = hi_bf16(w[i]);
+    acc = __fmaf_rn(lo, lo, acc);
+    acc = __fmaf_rn(hi, hi, acc);
+  }
+  return acc;
+}
+
+// inv_rms of one bf16 row (global or shared memory), one warp; p is this
+// warp's scratch of at least cols / 16 floats.
+__device__ float warp_inv_rms(const uint16_t* xr, int nb, int64_t cols, float eps, float* p) {
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  for (int b = lane; b < nb; b += 32) {
+    const uint4* v = reinterpret_cast<const uint4*>(xr + b * 16);
+    p[b] = sq_block(v[0], v[1]);
+  }
+  __syncwarp();
+  for (int n = nb; n > 1; n = (n + 1) / 2) {
+    const int half = (n + 1) / 2;
+    float s[kRmsMaxBlocks / 64];  // outputs of this lane at this level (read all, then write)
+#pragma unroll
+    for (int t = 0; t < kRmsMaxBlocks / 64; ++t) {
+      const int j = lane + 32 * t;
+      s[t] = j < half ? (2 * j + 1 < n ? __fadd_rn(p[2 * j], p[2 * j + 1]) : p[2 * j]) : 0.0f;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < kRmsMaxBlocks / 64; ++t) {
+      const int j = lane + 32 * t;
+      if (j < half) p[j] = s[t];
+    }
+    __syncwarp();
+  }
+  const float sum = nb > 0 ? p[0] : 0.0f;
+  __syncwarp();  // the caller reuses p for its next row
+  const float mean = __fdiv_rn(sum, static_cast<float>(cols));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+// bf16 bits of (x * inv) * w, round to nearest even, for the two halves of a word.
+__device__ __forceinline__ uint32_t rms_word(uint32_t xw, uint32_t ww, float inv) {
+  const float ylo = __fmul_rn(__fmul_rn(lo_bf16(xw), inv), lo_bf16(ww));
+  const float yhi = __fmul_rn(__fmul_rn(hi_bf16(xw), inv), hi_bf16(ww));
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(ylo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(yhi))) << 16);
+}
+
+__device__ __forceinline__ uint4 rms_vec(uint4 x, uint4 w, float inv) {
+  return make_uint4(rms_word(x.x, w.x, inv), rms_word(x.y, w.y, inv), rms_word(x.z, w.z, inv),
+                    rms_word(x.w, w.w, inv));
+}
+
+constexpr int kRmsThreads = 256;  // 8 warps, one row per warp at a time
+
+// Pass 1 (inputs larger than the SMs' shared memory): y's maximum |.|, then
+// gs by the last block, exactly as the amax kernel does.
+__global__ void __launch_bounds__(kRmsThreads)
+    rmsnorm_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                        const uint16_t* __restrict__ wt, float eps, float* __restrict__ gs_out,
+                        Workspace* __restrict__ ws) {
+  ptx::pdl_launch_dependents();
+  extern __shared__ __align__(16) float rms_scratch[];
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int nb = static_cast<int>(cols / 16);
+  float* p = rms_scratch + warp * nb;
+  uint32_t m2 = 0;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
+  for (int64_t r = gw; r < rows; r += nw) {
+    const uint16_t* xr = x + r * ld;
+    const float inv = warp_inv_rms(xr, nb, cols, eps, p);
+    for (int b = lane; b < nb; b += 32) {
+      const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
+      const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
+      m2 = __vmaxu2(m2, absmax8(rms_vec(xv[0], __ldg(wv), inv)));
+      m2 = __vmaxu2(m2, absmax8(rms_vec(xv[1], __ldg(wv + 1), inv)));
+    }
+  }
+  uint32_t m = fold16(m2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ uint32_t warp_max[kRmsThreads / 32];
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRmsThreads / 32; ++w) m = max(m, warp_max[w]);
+    atomicMax(&ws->amax_bits, m << 16);
+    __threadfence();
+    const uint32_t ticket = atomicAdd(&ws->done, 1u);
+    if (ticket == gridDim.x - 1) {
+      const uint32_t bits = atomicAdd(&ws->amax_bits, 0u);
+      gs_out[0] = __fdiv_rn(fmaxf(__uint_as_float(bits), kAmaxFloor), kGsDivisor);
+      ws->amax_bits = 0;
+      ws->done = 0;
+    }
+  }
+}
+
+// Pass 2: recompute each row's inv_rms (same order, same value) and quantize y.
+__global__ void __launch_bounds__(kRmsThreads)
+    rmsnorm_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                            const uint16_t* __restrict__ wt, float eps, uint8_t* __restrict__ q,
+                            uint8_t* __restrict__ sf, const float* __restrict__ gs_ptr) {
+  ptx::pdl_launch_dependents();
+  extern __shared__ __align__(16) float rms_scratch[];
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int nb = static_cast<int>(cols / 16);
+  float* p = rms_scratch + warp * nb;
+  const Scales sc = make_scales(gs_ptr);
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
+  for (int64_t r = gw; r < rows; r += nw) {
+    const uint16_t* xr = x + r * ld;
+    const float inv = warp_inv_rms(xr, nb, cols, eps, p);
+    for (int b = lane; b < nb; b += 32) {
+      const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
+      const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
+      uint32_t sbyte;
+      uint2 codes;
+      quantize_block(rms_vec(xv[0], __ldg(wv), inv), rms_vec(xv[1], __ldg(wv + 1), inv), sc, sbyte, codes);
+      const int64_t blk = r * nb + b;
+      __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
+      sf[blk] = static_cast<uint8_t>(sbyte);
+    }
+  }
+}
+
+// One pass for inputs that fit in the SMs' shared memory: each CTA holds
+// whole rows; every warp normalises its rows in place (y replaces x), the
+// CTAs exchange maxima as in quantize_onepass_kernel (one cluster, or a
+// cooperative grid meeting at the workspace counter), then each CTA
+// quantizes its rows from shared memory.
+template <bool kCluster>
+__global__ void __launch_bounds__(kOnePassThreads, 1)
+    rmsnorm_quantize_onepass_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                                    const uint16_t* __restrict__ wt, float eps, int64_t rows_per_cta,
+                                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                    float* __restrict__ gs_out, Workspace* __restrict__ ws) {
+  ptx::pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t red[kOnePassThreads / 32];
+  __shared__ float gs_sh;
+  constexpr int kWarpsOp = kOnePassThreads / 32;
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int nb = static_cast<int>(cols / 16);
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
+  const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
+  const int64_t n_rows = r1 > r0 ? r1 - r0 : 0;
+  const uint32_t row_bytes = static_cast<uint32_t>(cols * 2);
+  uint16_t* data = reinterpret_cast<uint16_t*>(smem);
+  float* scratch = reinterpret_cast<float*>(smem + rows_per_cta * row_bytes) + warp * nb;
+  const uint32_t bar_a = ptx::smem_addr(&bar);
+  ptx::pdl_wait();
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_a, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(bar_a, static_cast<uint32_t>(n_rows) * row_bytes);
+    for (int64_t r = r0; r < r1; ++r)  // one copy per row (rows may be strided)
+      ptx::bulk_load(ptx::smem_addr(data) + static_cast<uint32_t>((r - r0) * row_bytes), x + r * ld, row_bytes,
+                     bar_a);
+  }
+  __syncthreads();
+  uint32_t never = 0;
+  if (!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL) && threadIdx.x == 0)
+    atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+  uint32_t m2 = 0;
+  for (int64_t rr = warp; rr < n_rows; rr += kWarpsOp) {
+    uint16_t* yr = data + rr * cols;
+    const float inv = warp_inv_rms(yr, nb, cols, eps, scratch);
+    for (int b = lane; b < nb; b += 32) {
+      uint4* v = reinterpret_cast<uint4*>(yr + b * 16);
+      const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
+      const uint4 y0 = rms_vec(v[0], __ldg(wv), inv), y1 = rms_vec(v[1], __ldg(wv + 1), inv);
+      v[0] = y0;  // y replaces x: only this lane touches this block
+      v[1] = y1;
+      m2 = __vmaxu2(m2, __vmaxu2(absmax8(y0), absmax8(y1)));
+    }
+  }
+  uint32_t m = fold16(m2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if constexpr (kCluster) {
+    __shared__ float cta_max;
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kWarpsOp; ++w) m = max(m, red[w]);
+      cta_max = __uint_as_float(m << 16);
+    }
+    ptx::cluster_sync();
+    if (threadIdx.x == 0) {
+      float mx = 0.0f;
+      for (uint32_t r = 0; r < gridDim.x; ++r)
+        mx = fmaxf(mx, ptx::ld_cluster_f32(ptx::mapa_shared(ptx::smem_addr(&cta_max), r)));
+      const float gs = __fdiv_rn(fmaxf(mx, kAmaxFloor), kGsDivisor);
+      gs_sh = gs;
+      if (blockIdx.x == 0) gs_out[0] = gs;
+    }
+    ptx::cluster_sync();  // no CTA leaves while a peer may still read its maximum
+  } else if (threadIdx.x == 0) {
+    for (int w = 1; w < kWarpsOp; ++w) m = max(m, red[w]);
+    atomicMax(&ws->amax_bits, m << 16);
+    __threadfence();
+    atomicAdd(&ws->done, 1u);
+    volatile uint32_t* arrived = &ws->done;
+    const long long t0 = clock64();
+    bool late = false;
+    while (*arrived < gridDim.x) {
+      if (clock64() - t0 > kBarrierCycles) {
+        late = true;
+        break;
+      }
+    }
+    if (late) atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+    __threadfence();
+    const uint32_t bits = atomicAdd(&ws->amax_bits, 0u);
+    const float gs = __fdiv_rn(fmaxf(__uint_as_float(bits), kAmaxFloor), kGsDivisor);
+    gs_sh = gs;
+    if (blockIdx.x == 0) gs_out[0] = gs;
+  }
+  __syncthreads();
+  Scales sc;
+  sc.gs = gs_sh;
+  sc.r_gs = __frcp_rn(sc.gs);
+  sc.r_six = __frcp_rn(6.0f);
+  const uint4* sv = reinterpret_cast<const uint4*>(data);
+  const int64_t n_blocks = n_rows * nb;
+  for (int64_t i = threadIdx.x; i < n_blocks; i += kOnePassThreads) {
+    uint32_t sbyte;
+    uint2 codes;
+    quantize_block(sv[2 * i], sv[2 * i + 1], sc, sbyte, codes);
+    const int64_t blk = r0 * nb + i;
+    __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
+    sf[blk] = static_cast<uint8_t>(sbyte);
+  }
+  if constexpr (kCluster) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (atomicAdd(&ws->depart, 1u) == gridDim.x - 1) {
+      atomicExch(&ws->amax_bits, 0u);
+      atomicExch(&ws->done, 0u);
+      atomicExch(&ws->depart, 0u);
+    }
+  }
+}
+
+// Launch RMSNorm + quantize: one pass when whole rows fit in the SMs'
+// shared memory (one cluster up to 512 KB, else a cooperative grid of one
+// CTA per SM), otherwise the two row-parallel passes.
+cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                         const uint16_t* wt, float eps, uint8_t* q, uint8_t* sf, float* gs,
+                                         Workspace* ws, cudaStream_t stream) {
+  const int nb = static_cast<int>(cols / 16);
+  const int64_t row_bytes = cols * 2;
+  const int sms = sm_count();
+  if (rows > 0) {
+    const int64_t scratch = static_cast<int64_t>(kOnePassThreads / 32) * nb * 4;
+    const int64_t rows_cap = (static_cast<int64_t>(kOnePassMaxBytes) - scratch) / row_bytes;
+    if (rows_cap >= 1 && rows <= rows_cap * sms) {
+      const bool cluster = rows * row_bytes <= kClusterMaxBytes;
+      const int64_t cap = cluster ? 16 : sms;
+      int64_t grid = (rows * row_bytes + 8191) / 8192;
+      if (grid > cap) grid = cap;
+      if (grid > rows) grid = rows;
+      int64_t per = (rows + grid - 1) / grid;
+      if (per > rows_cap) per = rows_cap;
+      grid = (rows + per - 1) / per;
+      if (grid <= cap) {
+        const size_t smem = static_cast<size_t>(per * row_bytes + scratch);
+        auto kernel = cluster ? rmsnorm_quantize_onepass_kernel<true> : rmsnorm_quantize_onepass_kernel<false>;
+        bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem)) == cudaSuccess;
+        if (ok && cluster)
+          ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+        cfg.blockDim = dim3(kOnePassThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        if (cluster) {
+          attr[0].id = cudaLaunchAttributeClusterDimension;
+          attr[0].val.clusterDim.x = static_cast<unsigned>(grid);
+          attr[0].val.clusterDim.y = 1;
+          attr[0].val.clusterDim.z = 1;
+          attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+          attr[1].val.programmaticStreamSerializationAllowed = 1;
+        } else {
+          attr[0].id = cudaLaunchAttributeCooperative;
+          attr[0].val.cooperative = 1;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = cluster ? 2 : 1;
+        if (ok && cluster) {
+          int n = 0;
+          ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1;
+        }
+        if (ok) {
+          count_launch();
+          return cudaLaunchKernelEx(&cfg, kernel, x, rows, cols, ld, wt, eps, per, q, sf, gs, ws);
+        }
+        cudaGetLastError();  // fall through to the two passes
+      }
+    }
+  }
+  const size_t scratch2 = static_cast<size_t>(kRmsThreads / 32) * nb * 4;
+  cudaError_t e = cudaSuccess;
+  if (scratch2 > 48 * 1024)
+    e = cudaFuncSetAttribute(rmsnorm_amax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(scratch2));
+  if (e == cudaSuccess && scratch2 > 48 * 1024)
+    e = cudaFuncSetAttribute(rmsnorm_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(scratch2));
+  if (e != cudaSuccess) return e;
+  const int64_t warps_needed = rows > 0 ? rows : 1;
+  int64_t grid = (warps_needed + kRmsThreads / 32 - 1) / (kRmsThreads / 32);
+  if (grid > 4ll * sms) grid = 4ll * sms;
+  count_launch();
+  rmsnorm_amax_kernel<<<static_cast<unsigned>(grid), kRmsThreads, scratch2, stream>>>(x, rows, cols, ld, wt, eps,
+                                                                                       gs, ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || rows == 0) return e;
+  count_launch();
+  rmsnorm_quantize_kernel<<<static_cast<unsigned>(grid), kRmsThreads, scratch2, stream>>>(x, rows, cols, ld, wt,
+                                                                                           eps, q, sf, gs);
+  return cudaGetLastError();
+}
+
 int grid_for(int64_t work_items, int blocks_per_sm) {
   const int64_t need = (work_items + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
@@ -608,6 +954,12 @@ int grid_for(int64_t work_items, int blocks_per_sm) {
 }
 
 }  // namespace
+
+cudaError_t launch_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                    const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs,
+                                    Workspace* ws, cudaStream_t stream) {
+  return launch_rmsnorm_quantize_impl(x, rows, cols, ld, weight, eps, q, sf, gs, ws, stream);
+}
 
 bool launch_quantize_onepass(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,
                              uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream, cudaError_t* err) {

@@ -101,3 +101,15 @@ def test_gemm_validation(L):
     assert _gemm(L, sfa=FAKE + 2) == 2             # scales 4-byte aligned
     assert _gemm(L, ws=0) == 3
     assert _gemm(L, ws_bytes=16) == 3
+
+
+def test_rmsnorm_quantize_validation(L):
+    P, ws = _p, _p(FAKE)
+    f = ctypes.c_float
+    call = lambda x=FAKE, rows=4, cols=64, ld=64, w=FAKE, eps=1e-6: L.nvfp4_rmsnorm_quantize(
+        P(x) if x else None, rows, cols, ld, P(w) if w else None, f(eps), P(FAKE), P(FAKE), P(FAKE), ws, 256, None)
+    assert call(w=0) == 1                 # weight required
+    assert call(eps=-1.0) == 1            # eps must be >= 0
+    assert call(cols=40, ld=40) == 2      # cols multiple of 16
+    assert call(cols=16400, ld=16400) == 2  # at most 16384 columns
+    assert call(w=FAKE + 8) == 2          # weight 16-byte aligned

@@ -1,0 +1,87 @@
+"""GPU parity of nvfp4_rmsnorm_quantize (RMSNorm fused into the quantize)
+with the oracle: bit-exact codes, scales and global scale.  Sizes cover the
+three kernel paths: one cluster (up to 512 KB of input), one cooperative
+grid (rows that fit in the SMs' shared memory), and the two row-parallel
+passes beyond.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module")
+def nv():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantize_block_scaled_gb300 import build as b
+    b.build()
+    import quantize_block_scaled_gb300 as nv
+    nv.lib()
+    return nv
+
+
+@pytest.fixture(scope="module")
+def ws(nv):
+    return nv.workspace()
+
+
+def norm_weight(cols, seed):
+    rng = np.random.default_rng(seed)
+    return workloads.bf16_bits((1.0 + 0.1 * rng.standard_normal(cols)).astype(np.float32))
+
+
+def run(nv, ws, x, w, ld=None):
+    rows, cols = x.shape
+    if ld is None or ld == cols:
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+    else:
+        wide = np.zeros((rows, ld), np.uint16)
+        wide[:, :cols] = x
+        xd = torch.from_numpy(wide.view(np.int16)).cuda()[:, :cols]
+    wd = torch.from_numpy(w.view(np.int16)).cuda()
+    q, sf, gs = nv.rmsnorm_quantize(xd, wd, EPS, ws)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), sf.cpu().numpy(), gs.cpu().numpy()[0]
+
+
+def check(got, ref, what):
+    q, sf, gs = got
+    rq, rsf, rgs = ref
+    assert np.float32(gs).view(np.uint32) == np.float32(rgs).view(np.uint32), f"{what}: gs {gs} vs {rgs}"
+    assert np.array_equal(sf, rsf), f"{what}: {int((sf != rsf).sum())} scale bytes differ"
+    assert np.array_equal(q, rq), f"{what}: {int((q != rq).sum())} code bytes differ"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 7168), (32, 7168), (5, 16), (40, 16384), (300, 4096),
+                                       (1500, 7168), (2600, 7168)])
+def test_rmsnorm_quantize_shapes(nv, ws, rows, cols):
+    x = workloads.quantize_input(rows, seed=rows + cols, cols=cols)
+    w = norm_weight(cols, cols)
+    check(run(nv, ws, x, w), oracle.rmsnorm_quantize(x, w, EPS), f"{rows}x{cols}")
+
+
+def test_rmsnorm_quantize_strided_and_outliers(nv, ws):
+    d = workloads.router_prefill(tokens=64)
+    x = d["x"]
+    w = norm_weight(x.shape[1], 3)
+    check(run(nv, ws, x, w, ld=7168 + 64), oracle.rmsnorm_quantize(x, w, EPS), "prefill rows, ld 7232")
+
+
+def test_rmsnorm_quantize_two_calls_and_zero_rows(nv, ws):
+    x1 = workloads.quantize_input(16, seed=91)
+    x2 = workloads.quantize_input(16, seed=92) // 2
+    w = norm_weight(7168, 5)
+    for x in (x1, x2):
+        check(run(nv, ws, x, w), oracle.rmsnorm_quantize(x, w, EPS), "repeat")
+    assert nv.read_device_status(ws) == 0
+    xd = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    wd = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    q, sf, gs = nv.rmsnorm_quantize(xd, wd, EPS, ws)
+    torch.cuda.synchronize()
+    assert gs.item() == float(np.float32(1e-8) / np.float32(2688.0))
