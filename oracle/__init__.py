@@ -68,6 +68,7 @@ def _load():
             "orc_topk": (None, [P, P, I64, I64, ctypes.c_int, P, P, P]),
             "orc_normalize_topk_weights": (None, [P, P, I64, ctypes.c_int]),
             "orc_rmsnorm": (None, [P, I64, I64, I64, P, F, P]),
+            "orc_indexer_scores": (None, [P, P, F, P, P, F, I64, I64, I64, I64, P, P]),
             "orc_rmsnorm_quantize": (None, [P, I64, I64, I64, P, F, P, P, P]),
             "orc_gemm_topk_rows": (None, [P, P, F, P, P, F, I64, I64, ctypes.c_int, P,
                                           ctypes.c_int, I64, I64, P, P, P]),
@@ -205,6 +206,19 @@ def topk(score: np.ndarray, k: int, weight=None):
     wout = np.zeros((rows, k), np.float32)
     _load().orc_topk(_ptr(score), _ptr(w), rows, N, int(k), _ptr(idx), _ptr(val), _ptr(wout))
     return idx, val, wout
+
+
+def indexer_scores(qa, sfa, gsa, qb, sfb, gsb, heads: int, head_w: np.ndarray) -> np.ndarray:
+    """I[t, s] = sum_h w[t, h] * ReLU(q[t, h] . K[s]); A rows are t * heads + h."""
+    qa, sfa, qb, sfb = (_c(a, np.uint8) for a in (qa, sfa, qb, sfb))
+    M, K = qa.shape[0], qa.shape[1] * 2
+    N = qb.shape[0]
+    T = M // heads
+    w = _c(head_w, np.float32)
+    out = np.zeros((T, N), np.float32)
+    _load().orc_indexer_scores(_ptr(qa), _ptr(sfa), float(gsa), _ptr(qb), _ptr(sfb), float(gsb), T, heads, N, K,
+                               _ptr(w), _ptr(out))
+    return out
 
 
 def rmsnorm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:

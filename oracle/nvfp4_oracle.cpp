@@ -315,6 +315,29 @@ void orc_gemm_logits(const uint8_t* qa, const uint8_t* sfa, float gsa,
   }
 }
 
+// Full indexer score (page "commit 0d1cd1e", dsv4/_archive/kernels/indexer/
+// csa_indexer.py docstring, paper eq. 13-17 as quoted there; the key is
+// shared across heads):  I[t, s] = sum_h w[t, h] * ReLU(q[t, h] . K[s]).
+// The query rows of token t are rows t * H .. t * H + H - 1 of A (head-major
+// per token), the logits are those of orc_gemm_logits, the head sum is
+// taken in double and stored as float.
+void orc_indexer_scores(const uint8_t* qa, const uint8_t* sfa, float gsa, const uint8_t* qb,
+                        const uint8_t* sfb, float gsb, int64_t T, int64_t H, int64_t N, int64_t K,
+                        const float* head_w, float* out) {
+  std::vector<float> logits(static_cast<size_t>(H * N));
+  for (int64_t t = 0; t < T; ++t) {
+    orc_gemm_logits(qa, sfa, gsa, qb, sfb, gsb, N, K, t * H, t * H + H, logits.data());
+    for (int64_t s = 0; s < N; ++s) {
+      double acc = 0.0;
+      for (int64_t h = 0; h < H; ++h) {
+        const double z = logits[h * N + s];
+        acc += static_cast<double>(head_w[t * H + h]) * (z > 0.0 ? z : 0.0);
+      }
+      out[t * N + s] = static_cast<float>(acc);
+    }
+  }
+}
+
 // Epilogue on a rows x N logit matrix.
 //   epilogue 0 (identity, indexer-shaped): score = weight = logit
 //   epilogue 1 (router-shaped): weight = sqrt(softplus(logit)),

@@ -424,3 +424,41 @@ def test_rmsnorm_quantize_is_rmsnorm_then_quantize():
     q, sf, gs = oracle.rmsnorm_quantize(x, w, 1e-6)
     rq, rsf, rgs = oracle.quantize(oracle.rmsnorm(x, w, 1e-6))
     assert np.array_equal(q, rq) and np.array_equal(sf, rsf) and gs == rgs
+
+
+# ---- full indexer score (head reduction), I[t,s] = sum_h w[t,h] ReLU(q[t,h] . K[s])
+
+def _indexer_case(T, H, N, K, seed):
+    rng = np.random.default_rng(seed)
+    qa, sfa, gsa = oracle.quantize(bf16_bits(rng.standard_normal((T * H, K)).astype(np.float32)))
+    qb, sfb, gsb = oracle.quantize(bf16_bits(rng.standard_normal((N, K)).astype(np.float32)))
+    return qa, sfa, gsa, qb, sfb, gsb
+
+
+def test_indexer_single_head_unit_weight_is_relu_of_logits():
+    qa, sfa, gsa, qb, sfb, gsb = _indexer_case(3, 1, 40, 64, 41)
+    I = oracle.indexer_scores(qa, sfa, gsa, qb, sfb, gsb, 1, np.ones((3, 1), np.float32))
+    lg = oracle.gemm_logits(qa, sfa, gsa, qb, sfb, gsb)
+    assert np.array_equal(I, np.maximum(lg, 0))
+
+
+def test_indexer_scores_against_dequantized_einsum():
+    # the textbook: dequantize both operands, einsum 'thd,sd->ths' in double,
+    # ReLU, weighted head sum (the row order t * H + h is what is pinned)
+    T, H, N, K = 2, 4, 24, 128
+    qa, sfa, gsa, qb, sfb, gsb = _indexer_case(T, H, N, K, 42)
+    rng = np.random.default_rng(43)
+    w = rng.standard_normal((T, H)).astype(np.float32)
+    A = oracle.dequantize(qa, sfa, gsa).astype(np.float64).reshape(T, H, K)
+    B = oracle.dequantize(qb, sfb, gsb).astype(np.float64)
+    ref = (np.maximum(np.einsum("thd,sd->ths", A, B), 0) * w[:, :, None].astype(np.float64)).sum(axis=1)
+    I = oracle.indexer_scores(qa, sfa, gsa, qb, sfb, gsb, H, w)
+    np.testing.assert_allclose(I, ref, rtol=1e-5, atol=1e-6)
+
+
+def test_indexer_scores_linear_in_head_weights():
+    qa, sfa, gsa, qb, sfb, gsb = _indexer_case(1, 8, 16, 64, 44)
+    w = np.arange(1, 9, dtype=np.float32).reshape(1, 8)
+    I1 = oracle.indexer_scores(qa, sfa, gsa, qb, sfb, gsb, 8, w)
+    I2 = oracle.indexer_scores(qa, sfa, gsa, qb, sfb, gsb, 8, 2 * w)
+    np.testing.assert_allclose(I2, 2 * I1, rtol=1e-6)
