@@ -402,6 +402,17 @@ def secondary(nv, ws, pk, flush):
     by = gemm_bytes(M, N, K, k, bias=False) - M * k * 4
     out["indexer_M64_N2048_k512"] = dict(us=round(ti * 1e6, 2), hbm_frac=round(by / ti / hbm, 4),
                                          rows_per_s=round(M / ti, 1))
+    # NEXT-1: the indexer's weighted ReLU head sum fused in (one token, 64 heads x 128 dims)
+    hw = torch.from_numpy((np.random.default_rng(64).standard_normal((1, 64)) / 8).astype(np.float32)).cuda()
+    qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
+    qb, sfb, gsb = nv.quantize(torch.from_numpy(d["w"].view(np.int16)).cuda(), ws)
+    idx1 = torch.empty(1, k, dtype=torch.int32, device="cuda")
+    sc1 = torch.empty(1, k, dtype=torch.float32, device="cuda")
+    th = time_op_flushed(lambda: nv.nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, 64, hw, k, idx1, sc1, None, ws),
+                         30, flush)
+    by = gemm_bytes(64, N, K, k, bias=False) - 64 * k * 12 + k * 8 + 64 * 4
+    out["indexer_heads64_T1_N2048_k512"] = dict(us=round(th * 1e6, 2), hbm_frac=round(by / th / hbm, 4),
+                                                tokens_per_s=round(1 / th, 1))
     # router variant: 384 experts, top-6, normalised gating weights (decode, T = 32)
     rng = np.random.default_rng(384)
     E, kv = 384, 6

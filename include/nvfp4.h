@@ -13,6 +13,8 @@
  *                                norm fused in
  *   nvfp4_gemm_topk              block-scaled FP4 GEMM with a fused scoring
  *                                epilogue and per-row top-k
+ *   nvfp4_indexer_topk           the same GEMM with the indexer's weighted
+ *                                ReLU head sum fused in, top-k per token
  *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
@@ -205,6 +207,29 @@ int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
  */
 int nvfp4_quantize_noalloc(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                            uint8_t* q, uint8_t* sf, float* gs, cudaStream_t stream);
+
+/*
+ * Full indexer score with head reduction, then per-token top-k (page
+ * "commit 0d1cd1e", the csa_indexer.py docstring: I[t, s] = sum_h w[t, h] *
+ * ReLU(q[t, h] . K[s]), the key shared across heads; Selected = TopK(I[t, :])):
+ *
+ *   logit[t*heads + h, s] = gsa * gsb * sum_k A[t*heads + h, k] * B[s, k]
+ *   I[t, s] = sum_h head_w[t, h] * max(logit[t*heads + h, s], 0)     (FP32)
+ *   per token t: the k largest I[t, s], descending, ties by lower s.
+ *
+ * A: qa [tokens*heads, K/2], sfa [tokens*heads, K/16], gsa (query rows
+ *    head-major per token).  B: qb [N, K/2], sfb [N, K/16], gsb (the keys).
+ * heads: 32, 64 or 128.  head_w: float [tokens, heads].  N <= 4096, K a
+ * positive multiple of 64, 1 <= k <= 1024.  Outputs [tokens, k]: topk_idx
+ * (int32), topk_score (float); slots beyond N hold -1 / -inf.  scores: NULL,
+ * or float [tokens, N] to receive I (for testing).  The head sum is fused in
+ * the GEMM epilogue; I does not reach memory unless `scores` is given.
+ */
+int nvfp4_indexer_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
+                       const uint8_t* qb, const uint8_t* sfb, const float* gsb,
+                       int64_t tokens, int heads, int64_t N, int64_t K, const float* head_w,
+                       int k, int32_t* topk_idx, float* topk_score, float* scores,
+                       void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Diagnostic: synchronise `stream`, copy the workspace's device status bits

@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_status_string.argtypes = [I]
         L.nvfp4_last_cuda_error.restype = I
         L.nvfp4_last_cuda_error.argtypes = []
+        L.nvfp4_indexer_topk.restype = I
+        L.nvfp4_indexer_topk.argtypes = [P, P, P, P, P, P, I64, I, I64, I64, P, I, P, P, P, P, SZ, P]
         L.nvfp4_rmsnorm_quantize.restype = I
         L.nvfp4_rmsnorm_quantize.argtypes = [P, I64, I64, I64, P, ctypes.c_float, P, P, P, P, SZ, P]
         L.nvfp4_kernel_launches.restype = ctypes.c_uint64
@@ -87,7 +89,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
                     "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
                     "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc",
-                    "nvfp4_kernel_launches", "nvfp4_rmsnorm_quantize")
+                    "nvfp4_kernel_launches", "nvfp4_rmsnorm_quantize", "nvfp4_indexer_topk")
 
 
 def _check(fn: str, status: int):
@@ -155,6 +157,28 @@ def rmsnorm_quantize(x, weight, eps, ws, stream=None):
     gs = torch.empty(1, dtype=torch.float32, device=x.device)
     nvfp4_rmsnorm_quantize(x, weight, eps, q, sf, gs, ws, stream)
     return q, sf, gs
+
+
+def nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, heads, head_w, k, idx, score, scores=None, ws=None,
+                       stream=None):
+    rows = qa.shape[0]
+    K = qa.shape[1] * 2
+    N = qb.shape[0]
+    _check("nvfp4_indexer_topk", lib().nvfp4_indexer_topk(
+        _ptr(qa), _ptr(sfa), _ptr(gsa), _ptr(qb), _ptr(sfb), _ptr(gsb), rows // heads, int(heads), N, K,
+        _ptr(head_w), int(k), _ptr(idx), _ptr(score), _ptr(scores), _ptr(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
+
+
+def indexer_topk(qa, sfa, gsa, qb, sfb, gsb, heads, head_w, k, ws, want_scores=False, stream=None):
+    """Allocating convenience: (idx, score, I or None) per token."""
+    T = qa.shape[0] // heads
+    dev = qa.device
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    score = torch.empty(T, k, dtype=torch.float32, device=dev)
+    scores = torch.empty(T, qb.shape[0], dtype=torch.float32, device=dev) if want_scores else None
+    nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, heads, head_w, k, idx, score, scores, ws, stream)
+    return idx, score, scores
 
 
 def kernel_launches() -> int:

@@ -171,6 +171,52 @@ int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa, con
   return rc;
 }
 
+int nvfp4_indexer_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa, const uint8_t* qb,
+                       const uint8_t* sfb, const float* gsb, int64_t tokens, int heads, int64_t N, int64_t K,
+                       const float* head_w, int k, int32_t* topk_idx, float* topk_score, float* scores,
+                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+  // With tokens == 0 nothing is launched (queries, weights and outputs may be NULL).
+  if (gsa == nullptr || qb == nullptr || sfb == nullptr || gsb == nullptr) return NVFP4_ERR_INVALID;
+  if (tokens != 0 && (qa == nullptr || sfa == nullptr || head_w == nullptr || topk_idx == nullptr ||
+                      topk_score == nullptr))
+    return NVFP4_ERR_INVALID;
+  if (tokens < 0 || N < 1 || K < 1 || N > kInt32Max || K > kInt32Max) return NVFP4_ERR_INVALID;
+  if (heads != 32 && heads != 64 && heads != 128) return NVFP4_ERR_UNSUPPORTED;
+  if (tokens * heads > kInt32Max) return NVFP4_ERR_INVALID;
+  if (k < 1 || k > 1024) return NVFP4_ERR_INVALID;
+  if (K % 64 != 0 || N > 4096) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sfa, 4) || !aligned(sfb, 4) || !aligned(gsa, 4) ||
+      !aligned(gsb, 4) || !aligned(head_w, 4) || !aligned(topk_idx, 4) || !aligned(topk_score, 4) ||
+      (scores != nullptr && !aligned(scores, 4)))
+    return NVFP4_ERR_UNSUPPORTED;
+  const int st = check_workspace(ws, ws_bytes);
+  if (st != NVFP4_OK) return st;
+  nvfp4::GemmTopkArgs a;
+  a.qa = qa;
+  a.sfa = sfa;
+  a.gsa = gsa;
+  a.qb = qb;
+  a.sfb = sfb;
+  a.gsb = gsb;
+  a.M = tokens * heads;
+  a.N = N;
+  a.K = K;
+  a.epilogue = NVFP4_EPILOGUE_IDENTITY;
+  a.bias = nullptr;
+  a.k = k;
+  a.topk_idx = topk_idx;
+  a.topk_score = topk_score;
+  a.topk_weight = nullptr;
+  a.logits = scores;
+  a.ws = static_cast<nvfp4::Workspace*>(ws);
+  a.heads = heads;
+  a.head_w = head_w;
+  cudaError_t e = cudaSuccess;
+  const int rc = nvfp4::launch_gemm_topk(a, stream, &e);
+  if (rc == NVFP4_ERR_CUDA) return cuda_failure(e);
+  return rc;
+}
+
 int nvfp4_read_device_status(void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t stream) {
   if (status == nullptr) return NVFP4_ERR_INVALID;
   const int st = check_workspace(ws, ws_bytes);

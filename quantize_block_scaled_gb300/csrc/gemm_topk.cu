@@ -129,6 +129,8 @@ struct Params {
   uint32_t recv_bytes;    // reduce path, bulk: bytes of that receive area (at the start of rowmem)
   uint32_t bias_off;      // reduce path: offset in rowmem of the staged biases (N floats)
   int rpc;                // rows per cluster tile (<= BM; smaller spreads few long rows over more clusters)
+  int heads;              // indexer head reduction: A rows per token (32, 64 or 128), 0 = off
+  const float* head_w;    // [tokens, heads] head weights (head reduction)
   int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 512)
   int cand_cap;           // large path: power of two >= k
   uint32_t row_bytes;     // large path: bytes of one warp's key buffer (16-byte multiple)
@@ -284,6 +286,28 @@ __device__ __forceinline__ float row_logit(const RowCtx& c, int rr, int n) {
   for (int ks = 0; ks < c.k_split; ++ks) acc += c.recv[(ks * c.ro + rr) * c.rs + n];
   return acc * c.gab;
 }
+
+// Sum of v[j] over the 32 lanes of the warp, column j ending in lane j
+// (recursive halving: each step keeps one half of the columns and adds the
+// partner lane's copy of it).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & static_cast<uint32_t>(half)) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, half);
+    }
+  }
+  return v[0];
+}
+
+// Floats of the staged token rows ahead of the per-quarter partial sums
+// (head reduction: at most 4 tokens of BN + 4 floats in a 128-row tile).
+__host__ __device__ constexpr int vrow_cap_floats(int bn) { return 4 * (bn + 4); }
 
 // Sorting networks on keys where a larger key is a better entry.
 template <typename T>
@@ -823,6 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m0 = mt * p.rpc;
   const int n0 = n_idx * BN;
   const int vr = min(p.rpc, p.M - m0);  // valid rows of this tile
+  // rows as the epilogue owns them: A rows, or tokens under head reduction
+  const int vrow = p.heads ? vr / p.heads : vr;
+  const int64_t out0 = p.heads ? m0 / p.heads : m0;  // output row of the tile's first owned row
   const int kt0 = k_idx * p.num_k_tiles / p.k_split;
   const int nk = (k_idx + 1) * p.num_k_tiles / p.k_split - kt0;
   const int ncols = min(BN, p.N - n0);
@@ -844,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.bulk) {
       // Bytes this CTA will receive: each K slice's partials of its own rows,
       // every column slice padded to 4 floats.
-      const int owned = max(0, min(p.ro, vr - rank * p.ro));
+      const int owned = max(0, min(p.ro, vrow - rank * p.ro));
       uint32_t per_row = 0;
       for (int ni = 0; ni < p.n_split; ++ni) per_row += ((min(BN, p.N - ni * BN) + 3) & ~3) * 4;
       mbar_arrive_expect_tx(smem_addr(&bars[3 * kMaxStages + 2]),
@@ -1247,7 +1274,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // conflict-free vector stores) in its own stage region, then send each
       // row to its owner with one bulk copy counted on the owner's barrier.
       if (warp >= 2) {
-        if (acc_ready && quarter * 32 < vr) {  // warp-uniform (tcgen05.ld is collective)
+       if (p.heads) {
+        // Indexer head reduction: I[t, n] = sum_h w[t, h] * ReLU(logit[t*H + h, n]).
+        // Each warp folds its 32 rows (heads) per column (warp reduce-scatter:
+        // lane l ends with column c0 + l), the quarters of a token are added in
+        // quarter order, and the token's row of I is staged for its owner.
+        float* part = reinterpret_cast<float*>(smem) + vrow_cap_floats(BN);  // [4][BN] per-quarter sums
+        if (acc_ready) {  // warp-uniform
+          const int tok = static_cast<int>(out0) + row / p.heads;
+          const float hw = row < vr ? __ldg(p.head_w + static_cast<int64_t>(tok) * p.heads + row % p.heads) : 0.0f;
+          for (int c0 = 0; c0 < mma_n; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+            tmem_wait_ld();
+            float val[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) val[j] = hw * fmaxf(__uint_as_float(v[j]) * gab, 0.0f);
+            part[quarter * BN + c0 + static_cast<int>(lane)] = warp_reduce_scatter32(val);
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        const int qpt = p.heads / 32;  // quarters per token
+        for (int i = (warp - 2) * 32 + static_cast<int>(lane); i < vrow * BN; i += 128) {
+          const int t = i / BN, cc = i - t * BN;
+          float acc = 0.0f;
+          for (int q = t * qpt; q < (t + 1) * qpt; ++q) acc += part[q * BN + cc];
+          reinterpret_cast<float*>(smem)[t * (BN + 4) + cc] = acc;
+        }
+        fence_proxy_async_smem();  // staged rows are read by the async (bulk copy) proxy
+       } else if (acc_ready && quarter * 32 < vr) {  // warp-uniform (tcgen05.ld is collective)
           for (int c0 = 0; c0 < mma_n; c0 += 64) {  // two 32-column loads in flight
             const bool two = c0 + 32 < mma_n;       // then c0 + 64 <= BN
             uint32_t v[32], u[32];
@@ -1273,7 +1328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bytes = static_cast<uint32_t>(((ncols + 3) & ~3) * 4);
           const uint32_t recv_local = smem_addr(rowmem);
           const uint32_t bar_local = smem_addr(&bars[3 * kMaxStages + 2]);
-          for (int r = (warp - 2) + 4 * static_cast<int>(lane); r < vr; r += 128) {  // 4 warps share few rows
+          for (int r = (warp - 2) + 4 * static_cast<int>(lane); r < vrow; r += 128) {  // 4 warps share few rows
             const int o = r / p.ro;
             const int rr = r - o * p.ro;
             bulk_copy_to_peer(
@@ -1322,14 +1377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.ro = p.ro;
     c.rs = rs;
     c.k_split = p.k_split;
-    c.gab = gab;
+    c.gab = p.heads ? 1.0f : gab;  // head-reduced scores are final
     const int r0 = rank * p.ro;
-    const int owned = min(p.ro, vr - r0);
+    const int owned = min(p.ro, vrow - r0);
     if (!p.large) {
-      rows_small(p, c, owned, m0 + r0);
+      rows_small(p, c, owned, out0 + r0);
     } else {
       uint8_t* mine = rowmem + p.recv_bytes;
-      rows_large(p, c, owned, m0 + r0, reinterpret_cast<uint32_t*>(mine),
+      rows_large(p, c, owned, out0 + r0, reinterpret_cast<uint32_t*>(mine),
                  reinterpret_cast<uint64_t*>(mine + p.row_bytes),
                  reinterpret_cast<uint32_t*>(mine + p.row_bytes + p.cand_cap * 8));
     }
@@ -1388,7 +1443,7 @@ struct Plan {
   int stages;
   int direct, ro, bulk;
   uint32_t recv_bytes, bias_off;
-  int rpc;
+  int rpc, heads;
   int large, cand_cap;
   uint32_t row_bytes;
   uint32_t region;
@@ -1398,9 +1453,10 @@ struct Plan {
 // Pick the split, epilogue and shared-memory layout of one problem; false if
 // it cannot be laid out.
 bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, int max_cluster,
-               int rpc, Plan* out) {
+               int rpc, int heads, Plan* out) {
   Plan pl{};
   pl.rpc = rpc;
+  pl.heads = heads;
   const int64_t m_tiles = (M + rpc - 1) / rpc;
   const int kt = static_cast<int>((K / 2 + BKB - 1) / BKB);
   if (N <= 128) {
@@ -1415,16 +1471,18 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   pl.n_split = static_cast<int>((N + pl.bn - 1) / pl.bn);
   if (pl.n_split > max_cluster) return false;
   pl.k_split = 1;
-  if (m_tiles * pl.n_split < sms / 2) {  // few tiles: spread K over the rest of the cluster
+  // (head reduction takes ReLU of complete logits: no K split)
+  if (heads == 0 && m_tiles * pl.n_split < sms / 2) {  // few tiles: spread K over the rest of the cluster
     const int64_t want = (sms + m_tiles * pl.n_split - 1) / (m_tiles * pl.n_split);
     int ks = static_cast<int>(want < max_cluster / pl.n_split ? want : max_cluster / pl.n_split);
     if (ks > kt) ks = kt;
     pl.k_split = ks < 1 ? 1 : ks;
   }
   const int csize = pl.n_split * pl.k_split;
-  const int vr_max = static_cast<int>(M < rpc ? M : rpc);
+  // rows the epilogue owns per tile: A rows, or tokens under head reduction
+  const int vr_max = static_cast<int>(M < rpc ? M : rpc) / (heads ? heads : 1);
   pl.ro = (vr_max + csize - 1) / csize;
-  pl.direct = (pl.k_split == 1 && k <= 32) ? 1 : 0;
+  pl.direct = (heads == 0 && pl.k_split == 1 && k <= 32) ? 1 : 0;
   pl.kmax = k <= 8 ? 8 : (k <= 16 ? 16 : 32);
   pl.large = (!pl.direct && (k > 32 || N > 32 * kSmallCols)) ? 1 : 0;
   pl.cand_cap = pl.large ? (k <= 64 ? 64 : next_pow2(k)) : 0;  // 2 .. 32 per lane of the sort
@@ -1433,7 +1491,9 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   const uint32_t sb = pl.bn == 128 ? Layout<128>::kStage : Layout<256>::kStage;
   const uint32_t recv = static_cast<uint32_t>(pl.k_split) * static_cast<uint32_t>(pl.ro) *
                         static_cast<uint32_t>(pl.n_split * pl.bn) * 4u;
-  const uint32_t staging = static_cast<uint32_t>(vr_max) * static_cast<uint32_t>(pl.bn + 4) * 4u;
+  const uint32_t staging =
+      heads ? static_cast<uint32_t>(vrow_cap_floats(pl.bn) + 4 * pl.bn) * 4u  // token rows + quarter sums
+            : static_cast<uint32_t>(vr_max) * static_cast<uint32_t>(pl.bn + 4) * 4u;
   pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
   // After the main loop the stage region holds the direct epilogue's bias
   // copies, or the reduce epilogue's staged tile (bulk) / received partials.
@@ -1465,6 +1525,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
   pl.smem = total();
   if (pl.smem > static_cast<size_t>(smem_optin)) return false;
+  if (heads && !pl.bulk) return false;  // head reduction stages token rows for bulk copies
   *out = pl;
   return true;
 }
@@ -1596,7 +1657,7 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   Plan pl;
   int cap = kMaxCluster;
   for (;;) {
-    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, BM, &pl)) return NVFP4_ERR_UNSUPPORTED;
+    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, BM, a.heads, &pl)) return NVFP4_ERR_UNSUPPORTED;
     if (active(pl) > 0) break;
     const int c = pl.n_split * pl.k_split;
     if (c <= 1 || cap <= 1) return NVFP4_ERR_UNSUPPORTED;
@@ -1606,9 +1667,12 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
     // Row selection dominates: spread the rows over every cluster that can
     // be resident (fewer rows per tile, so fewer rows per owning CTA).
     const int n_active = active(pl);
-    const int64_t rpc = n_active > 0 ? (a.M + n_active - 1) / n_active : BM;
+    const int64_t unit = a.heads ? a.heads : 1;  // tiles hold whole tokens under head reduction
+    int64_t rpc = n_active > 0 ? (a.M + n_active - 1) / n_active : BM;
+    rpc = (rpc + unit - 1) / unit * unit;
     Plan spread;
-    if (rpc < BM && make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, static_cast<int>(rpc), &spread) &&
+    if (rpc < BM &&
+        make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, static_cast<int>(rpc), a.heads, &spread) &&
         spread.n_split == pl.n_split && spread.k_split == pl.k_split && active(spread) > 0)
       pl = spread;
   }
@@ -1655,6 +1719,8 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.recv_bytes = pl.recv_bytes;
   p.bias_off = pl.bias_off;
   p.rpc = pl.rpc;
+  p.heads = a.heads;
+  p.head_w = a.head_w;
   p.large = pl.large;
   p.cand_cap = pl.cand_cap;
   p.row_bytes = pl.row_bytes;

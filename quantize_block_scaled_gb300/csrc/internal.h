@@ -67,6 +67,8 @@ struct GemmTopkArgs {
   float* topk_weight;
   float* logits;
   Workspace* ws;
+  int heads = 0;                  // indexer head reduction (A rows per token), 0 = off
+  const float* head_w = nullptr;  // [M / heads, heads]
 };
 
 // Returns an nvfp4_status; on NVFP4_ERR_CUDA the CUDA error is in *err.

@@ -113,3 +113,15 @@ def test_rmsnorm_quantize_validation(L):
     assert call(cols=40, ld=40) == 2      # cols multiple of 16
     assert call(cols=16400, ld=16400) == 2  # at most 16384 columns
     assert call(w=FAKE + 8) == 2          # weight 16-byte aligned
+
+
+def test_indexer_topk_validation(L):
+    P, ws = _p, _p(FAKE)
+    call = lambda heads=64, N=2048, K=128, k=512, hw=FAKE: L.nvfp4_indexer_topk(
+        P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, heads, N, K, P(hw) if hw else None, k,
+        P(FAKE), P(FAKE), None, ws, 256, None)
+    assert call(heads=48) == 2            # 32, 64 or 128 heads
+    assert call(hw=0) == 1                # head weights required
+    assert call(k=0) == 1
+    assert call(N=5000) == 2              # keys on chip: N <= 4096
+    assert call(K=100) == 2               # K a multiple of 64
