@@ -596,6 +596,19 @@ def run_profile(kind: str, iters: int):
                              .view(np.int16)).cuda()
         q, sf, gs = nv.quantize(x, ws)
         fns = [lambda: nv.nvfp4_quantize(x, q, sf, gs, ws)]
+    elif kind == "rmsnorm2048":
+        x = torch.from_numpy(workloads.quantize_input(2048).view(np.int16)).cuda()
+        wn = torch.ones(HIDDEN, dtype=torch.bfloat16, device="cuda")
+        q, sf, gs = nv.rmsnorm_quantize(x, wn, 1e-6, ws)
+        fns = [lambda: nv.nvfp4_rmsnorm_quantize(x, wn, 1e-6, q, sf, gs, ws)]
+    elif kind == "indexer_heads":
+        d = workloads.indexer()
+        qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
+        qb, sfb, gsb = nv.quantize(torch.from_numpy(d["w"].view(np.int16)).cuda(), ws)
+        hw = torch.full((1, 64), 0.125, dtype=torch.float32, device="cuda")
+        idx = torch.empty(1, 512, dtype=torch.int32, device="cuda")
+        sc = torch.empty(1, 512, dtype=torch.float32, device="cuda")
+        fns = [lambda: nv.nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, 64, hw, 512, idx, sc, None, ws)]
     elif kind == "indexer":
         d = workloads.indexer()
         qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
@@ -625,7 +638,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--tokens", type=int, default=32, choices=(1, 32))
     ap.add_argument("--quick", action="store_true", help="skip the secondary per-config figures")
-    ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "quantize2048", "indexer"),
+    ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "quantize2048", "indexer",
+                                          "indexer_heads", "rmsnorm2048"),
                     help="run --warmup eager iterations of one workload in an NVTX range and exit")
     args = ap.parse_args()
     if args.profile:

@@ -1274,35 +1274,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // conflict-free vector stores) in its own stage region, then send each
       // row to its owner with one bulk copy counted on the owner's barrier.
       if (warp >= 2) {
-       if (p.heads) {
-        // Indexer head reduction: I[t, n] = sum_h w[t, h] * ReLU(logit[t*H + h, n]).
-        // Each warp folds its 32 rows (heads) per column (warp reduce-scatter:
-        // lane l ends with column c0 + l), the quarters of a token are added in
-        // quarter order, and the token's row of I is staged for its owner.
-        float* part = reinterpret_cast<float*>(smem) + vrow_cap_floats(BN);  // [4][BN] per-quarter sums
-        if (acc_ready) {  // warp-uniform
-          const int tok = static_cast<int>(out0) + row / p.heads;
-          const float hw = row < vr ? __ldg(p.head_w + static_cast<int64_t>(tok) * p.heads + row % p.heads) : 0.0f;
-          for (int c0 = 0; c0 < mma_n; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
-            tmem_wait_ld();
-            float val[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) val[j] = hw * fmaxf(__uint_as_float(v[j]) * gab, 0.0f);
-            part[quarter * BN + c0 + static_cast<int>(lane)] = warp_reduce_scatter32(val);
+        if (p.heads) {
+          // Indexer head reduction: I[t, n] = sum_h w[t, h] * ReLU(logit[t*H + h, n]).
+          // Each warp folds its 32 rows (heads) per column (warp reduce-scatter:
+          // lane l ends with column c0 + l), the quarters of a token are added in
+          // quarter order, and the token's row of I is staged for its owner.
+          float* part = reinterpret_cast<float*>(smem) + vrow_cap_floats(BN);  // [4][BN] per-quarter sums
+          if (acc_ready) {  // warp-uniform
+            const int tok = static_cast<int>(out0) + row / p.heads;
+            const float hw = row < vr ? __ldg(p.head_w + static_cast<int64_t>(tok) * p.heads + row % p.heads) : 0.0f;
+            for (int c0 = 0; c0 < mma_n; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+              tmem_wait_ld();
+              float val[32];
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) val[j] = hw * fmaxf(__uint_as_float(v[j]) * gab, 0.0f);
+              part[quarter * BN + c0 + static_cast<int>(lane)] = warp_reduce_scatter32(val);
+            }
           }
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
-        const int qpt = p.heads / 32;  // quarters per token
-        for (int i = (warp - 2) * 32 + static_cast<int>(lane); i < vrow * BN; i += 128) {
-          const int t = i / BN, cc = i - t * BN;
-          float acc = 0.0f;
-          for (int q = t * qpt; q < (t + 1) * qpt; ++q) acc += part[q * BN + cc];
-          reinterpret_cast<float*>(smem)[t * (BN + 4) + cc] = acc;
-        }
-        fence_proxy_async_smem();  // staged rows are read by the async (bulk copy) proxy
-       } else if (acc_ready && quarter * 32 < vr) {  // warp-uniform (tcgen05.ld is collective)
+          asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+          const int qpt = p.heads / 32;  // quarters per token
+          for (int i = (warp - 2) * 32 + static_cast<int>(lane); i < vrow * BN; i += 128) {
+            const int t = i / BN, cc = i - t * BN;
+            float acc = 0.0f;
+            for (int q = t * qpt; q < (t + 1) * qpt; ++q) acc += part[q * BN + cc];
+            reinterpret_cast<float*>(smem)[t * (BN + 4) + cc] = acc;
+          }
+          fence_proxy_async_smem();  // staged rows are read by the async (bulk copy) proxy
+        } else if (acc_ready && quarter * 32 < vr) {  // warp-uniform (tcgen05.ld is collective)
           for (int c0 = 0; c0 < mma_n; c0 += 64) {  // two 32-column loads in flight
             const bool two = c0 + 32 < mma_n;       // then c0 + 64 <= BN
             uint32_t v[32], u[32];
