@@ -72,6 +72,9 @@ def _load():
             "orc_rmsnorm_quantize": (None, [P, I64, I64, I64, P, F, P, P, P]),
             "orc_gemm_topk_rows": (None, [P, P, F, P, P, F, I64, I64, ctypes.c_int, P,
                                           ctypes.c_int, I64, I64, P, P, P]),
+            "orc_grouped_swiglu": (None, [P, P, F, P, P, P, P, I64, I64, I64, I64,
+                                          ctypes.c_double, P, P]),
+            "orc_to_bf16": (None, [P, I64, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -287,3 +290,52 @@ def gemm_topk(qa, sfa, gsa, qb, sfb, gsb, kind: int, bias, k: int,
         for t in ts:
             t.join()
     return idx, val, wout
+
+
+# ---- grouped GEMM + SwiGLU (MoE first projection) -----------------------------------
+
+def grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offsets, inter: int, granularity: int,
+                   limit: float = float("inf")):
+    """SwiGLU of a grouped NVFP4 GEMM, in double: returns (h, a), each [M, I].
+
+    qb/sfb hold E experts' [2I, K] weights stacked as [E*2I, K/2] / [E*2I, K/16];
+    gsb has E entries; offsets (E + 1 int32) give each expert's rows of A.
+    h = silu(min(gate, limit)) * clip(up, -limit, limit); a = silu(min(gate, limit)).
+    Rows outside every group stay 0.
+    """
+    qa, sfa, qb, sfb = (_c(a, np.uint8) for a in (qa, sfa, qb, sfb))
+    gsb = _c(np.atleast_1d(gsb), np.float32)
+    offs = _c(offsets, np.int32)
+    M, K = qa.shape[0], qa.shape[1] * 2
+    E = offs.size - 1
+    assert gsb.size == E and qb.shape[0] == E * 2 * inter
+    h = np.zeros((M, inter), np.float64)
+    a = np.zeros((M, inter), np.float64)
+    _load().orc_grouped_swiglu(_ptr(qa), _ptr(sfa), float(gsa), _ptr(qb), _ptr(sfb), _ptr(gsb), _ptr(offs),
+                               E, inter, K, granularity, float(limit), _ptr(h), _ptr(a))
+    return h, a
+
+
+def to_bf16(v: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of doubles (rounded to float, then to bf16, nearest even)."""
+    v = _c(v, np.float64)
+    out = np.zeros(v.shape, np.uint16)
+    _load().orc_to_bf16(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def grouped_swiglu_bf16(qa, sfa, gsa, qb, sfb, gsb, offsets, inter: int, granularity: int,
+                        limit: float = float("inf"), layout: int = 0) -> np.ndarray:
+    """The stored bf16 output: layout 0 = h [M, I]; layout 1 = [M, 2I] with the
+    gate columns of the weights' interleave holding a and the up columns h."""
+    h, a = grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offsets, inter, granularity, limit)
+    if layout == 0:
+        return to_bf16(h)
+    M = h.shape[0]
+    g = granularity
+    out = np.zeros((M, 2 * inter), np.float64)
+    for j0 in range(0, inter, g):
+        base = 2 * j0
+        out[:, base:base + g] = a[:, j0:j0 + g]
+        out[:, base + g:base + 2 * g] = h[:, j0:j0 + g]
+    return to_bf16(out)

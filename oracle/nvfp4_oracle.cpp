@@ -30,6 +30,11 @@
 //                        normalisation is not spelled out (reading below)
 //   deinterleave         page "commit 0d1cd1e", fused_deinterleave commit;
 //                        docs/PERFORMANCE_AUDIT.md P1 (granularity 8)
+//   grouped SwiGLU GEMM  compare view: MoE kernel notes (fused SwiGLU
+//                        grouped GEMM, granularity-8 interleaved L1
+//                        weights), model notes (swiglu_limit = 10),
+//                        PERFORMANCE_AUDIT.md P1 ([silu(gate), silu(gate)*up]
+//                        interleaved output)
 //
 // Readings where the pages are silent (each one is listed in the design
 // notes): block scale s = (bamax / 6) / gs in FP32; E4M3 round-to-nearest-
@@ -38,7 +43,9 @@
 // negative value that rounds to zero encodes as 0x8); a block whose scale
 // byte is zero encodes every element as a signed zero; the even element of a
 // pair goes to the low nibble; softplus(z) = z for z > 20; normalised
-// router weights (epilogue 2) are the selected weights over their sum.
+// router weights (epilogue 2) are the selected weights over their sum;
+// the SwiGLU limit clamps the gate from above and the up value on both
+// sides.
 //
 // Floating point: every FP32 step is one IEEE single operation (compile with
 // -ffp-contract=off and without fast-math); the GEMM accumulates in double.
@@ -416,6 +423,58 @@ void orc_gemm_topk_rows(const uint8_t* qa, const uint8_t* sfa, float gsa,
   orc_epilogue(logits.data(), rows, N, epilogue == 2 ? 1 : epilogue, bias, score.data(), weight.data());
   orc_topk(score.data(), weight.data(), rows, N, k, idx_out, score_out, weight_out);
   if (epilogue == 2 && weight_out) orc_normalize_topk_weights(idx_out, weight_out, rows, k);
+}
+
+// Grouped block-scaled GEMM with the SwiGLU epilogue of the MoE first
+// projection (compare view, MoE kernel notes "FusedSwiGLUScaledGroupedGemm-
+// Kernel": SwiGLU and clamp applied between the TMEM read and the store,
+// L1 weights with gate and up interleaved at granularity 8; model notes
+// "SwiGLU activation with swiglu_limit=10.0"; the shared-expert fix (P1):
+// the fused kernel writes [silu(gate), silu(gate) * up] interleaved at the
+// weights' granularity).
+//
+// Group e owns the A rows [offs[e], offs[e+1]) and the 2I weight rows
+// [e * 2I, (e + 1) * 2I) of B, whose rows hold gate and up columns in
+// alternating runs of g (as orc_deinterleave reads them), and its own
+// global scale gsb[e].  For a row m of group e:
+//   logit[n]  = float(gsa * gsb[e] * sum_k A[m, k] B[e*2I + n, k])  (as orc_gemm_logits)
+//   gate[j]   = logit[2g*floor(j/g) + j mod g],  up[j] = logit[2g*floor(j/g) + g + j mod g]
+//   gate'     = min(gate, limit),  up' = min(max(up, -limit), limit)
+//   a[j]      = silu(gate') = gate' / (1 + exp(-gate'))              (double)
+//   h[j]      = a[j] * up'
+// The clamp form (gate from above, up on both sides, one limit) is the
+// reading taken: the pages name the limit but not where it applies.
+// Outputs, double, [M, I] each: h (the SwiGLU result) and a (the SiLU of
+// the clamped gate).  Rows outside every group are left untouched.
+void orc_grouped_swiglu(const uint8_t* qa, const uint8_t* sfa, float gsa, const uint8_t* qb,
+                        const uint8_t* sfb, const float* gsb, const int32_t* offs, int64_t E,
+                        int64_t inter, int64_t K, int64_t g, double limit, double* h_out,
+                        double* a_out) {
+  const int64_t two_i = 2 * inter;
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t lo = offs[e], hi = offs[e + 1];
+    if (hi <= lo) continue;
+    std::vector<float> logits(static_cast<size_t>((hi - lo) * two_i));
+    orc_gemm_logits(qa, sfa, gsa, qb + e * two_i * (K / 2), sfb + e * two_i * (K / 16), gsb[e],
+                    two_i, K, lo, hi, logits.data());
+    for (int64_t m = lo; m < hi; ++m) {
+      const float* z = logits.data() + (m - lo) * two_i;
+      for (int64_t j = 0; j < inter; ++j) {
+        const int64_t base = 2 * g * (j / g) + (j % g);
+        const double gate = std::min(static_cast<double>(z[base]), limit);
+        const double up = std::min(std::max(static_cast<double>(z[base + g]), -limit), limit);
+        const double a = gate / (1.0 + std::exp(-gate));
+        h_out[m * inter + j] = a * up;
+        if (a_out) a_out[m * inter + j] = a;
+      }
+    }
+  }
+}
+
+// Round doubles to bf16 bit patterns (through float; both roundings to
+// nearest even).
+void orc_to_bf16(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = bf16_round(static_cast<float>(v[i]));
 }
 
 }  // extern "C"

@@ -462,3 +462,124 @@ def test_indexer_scores_linear_in_head_weights():
     I1 = oracle.indexer_scores(qa, sfa, gsa, qb, sfb, gsb, 8, w)
     I2 = oracle.indexer_scores(qa, sfa, gsa, qb, sfb, gsb, 8, 2 * w)
     np.testing.assert_allclose(I2, 2 * I1, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- grouped GEMM + SwiGLU
+
+def _decode_by_table(q, sf):
+    """NVFP4 values without the global scale, decoded with the page's table and
+    torch's E4M3 conversion (no oracle code): [rows, 2 * bytes]."""
+    lo, hi = q & 0xF, q >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(q.shape[0], -1)
+    mag = np.array(E2M1_VALUES)[codes & 7]
+    vals = np.where(codes & 8, -mag, mag)
+    s = torch.from_numpy(np.ascontiguousarray(sf)).view(torch.float8_e4m3fn).double().numpy()
+    return vals * np.repeat(s, 16, axis=1)
+
+
+def _swiglu_case(rng, M, E, I, K, g, sizes):
+    qa = rng.integers(0, 256, (M, K // 2)).astype(np.uint8)
+    qb = rng.integers(0, 256, (E * 2 * I, K // 2)).astype(np.uint8)
+    # power-of-two block scales (E4M3 bytes 0x30 = 0.5, 0x38 = 1, 0x40 = 2)
+    sfa = rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), (M, K // 16))
+    sfb = rng.choice(np.array([0x28, 0x30, 0x38], np.uint8), (E * 2 * I, K // 16))
+    gsb = (2.0 ** rng.integers(-8, -4, E)).astype(np.float32)
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    assert offs[-1] <= M
+    return qa, sfa, qb, sfb, gsb, offs
+
+
+@pytest.mark.parametrize("g", [1, 8])
+def test_grouped_swiglu_against_library_math(g):
+    # Expected values from the page's E2M1 table, torch's E4M3, numpy matmul,
+    # a reshape-based split of the interleaved weight rows and scipy's
+    # logistic function; groups of size 5, 0, 3 and 4 over 12 of 14 rows.
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(21)
+    M, E, I, K = 14, 4, 16, 128
+    qa, sfa, qb, sfb, gsb, offs = _swiglu_case(rng, M, E, I, K, g, [5, 0, 3, 4])
+    gsa = np.float32(2.0)
+    limit = 1.0
+    h, a = oracle.grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offs, I, g, limit)
+    clamped = {"gate": 0, "up_hi": 0, "up_lo": 0}
+    A = _decode_by_table(qa, sfa)
+    B = _decode_by_table(qb, sfb)
+    for e in range(E):
+        rows = slice(offs[e], offs[e + 1])
+        We = B[e * 2 * I:(e + 1) * 2 * I].reshape(I // g, 2, g, K)
+        gate_w, up_w = We[:, 0].reshape(I, K), We[:, 1].reshape(I, K)
+        s = float(gsa) * float(gsb[e])
+        gate = (A[rows] @ gate_w.T * s).astype(np.float32).astype(np.float64)
+        up = (A[rows] @ up_w.T * s).astype(np.float32).astype(np.float64)
+        clamped["gate"] += int(np.sum(gate > limit))
+        clamped["up_hi"] += int(np.sum(up > limit))
+        clamped["up_lo"] += int(np.sum(up < -limit))
+        gate = np.minimum(gate, limit)
+        up = np.clip(up, -limit, limit)
+        silu = gate * special.expit(gate)
+        np.testing.assert_allclose(a[rows], silu, rtol=1e-13, atol=1e-300)
+        np.testing.assert_allclose(h[rows], silu * up, rtol=1e-13, atol=1e-300)
+    # rows past the last group are not written
+    assert np.all(h[offs[-1]:] == 0) and np.all(a[offs[-1]:] == 0)
+    # every side of the clamp is exercised, and a clamped gate gives silu(limit)
+    assert min(clamped.values()) > 0, clamped
+    assert np.max(a) == limit / (1.0 + math.exp(-limit))
+
+
+def test_grouped_swiglu_closed_forms():
+    # Zero up weights give h = 0; zero gate weights give a = silu(0) = 0; an
+    # unbounded limit is no clamp; a group equals the same rows run as a
+    # one-expert problem with that expert's weights.
+    rng = np.random.default_rng(22)
+    M, E, I, K, g = 9, 3, 8, 64, 8
+    qa, sfa, qb, sfb, gsb, offs = _swiglu_case(rng, M, E, I, K, g, [2, 4, 3])
+    gsa = np.float32(1.0)
+    qb_up0 = qb.copy()
+    for e in range(E):
+        for p in range(I // g):
+            r0 = e * 2 * I + 2 * g * p + g
+            qb_up0[r0:r0 + g] = 0
+    h, a = oracle.grouped_swiglu(qa, sfa, gsa, qb_up0, sfb, gsb, offs, I, g)
+    assert np.all(h == 0) and np.any(a != 0)
+    qb_gate0 = qb.copy()
+    for e in range(E):
+        for p in range(I // g):
+            r0 = e * 2 * I + 2 * g * p
+            qb_gate0[r0:r0 + g] = 0
+    h, a = oracle.grouped_swiglu(qa, sfa, gsa, qb_gate0, sfb, gsb, offs, I, g)
+    assert np.all(a == 0) and np.all(h == 0)
+    h_all, a_all = oracle.grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offs, I, g)
+    h_big, _ = oracle.grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offs, I, g, limit=1e30)
+    np.testing.assert_array_equal(h_all, h_big)
+    for e in range(E):
+        lo, hi = offs[e], offs[e + 1]
+        w = slice(e * 2 * I, (e + 1) * 2 * I)
+        h1, a1 = oracle.grouped_swiglu(qa[lo:hi], sfa[lo:hi], gsa, qb[w], sfb[w], gsb[e:e + 1],
+                                       np.array([0, hi - lo], np.int32), I, g)
+        np.testing.assert_array_equal(h1, h_all[lo:hi])
+        np.testing.assert_array_equal(a1, a_all[lo:hi])
+    # swapping two experts' weights and row ranges permutes the output rows
+    perm_offs = np.array([0, 4, 6, 9], np.int32)  # expert 1's rows first, then 0, then 2
+    rows = np.r_[2:6, 0:2, 6:9]
+    wperm = np.r_[2 * I:4 * I, 0:2 * I, 4 * I:6 * I]
+    h2, _ = oracle.grouped_swiglu(qa[rows], sfa[rows], gsa, qb[wperm], sfb[wperm], gsb[[1, 0, 2]], perm_offs, I, g)
+    np.testing.assert_array_equal(h2, h_all[rows])
+
+
+def test_grouped_swiglu_interleaved_layout():
+    # Layout 1 deinterleaves (with the separately pinned deinterleave) into
+    # [bf16(silu(gate)) | bf16(h)]; layout 0 is bf16(h).
+    rng = np.random.default_rng(23)
+    M, E, I, K, g = 6, 2, 32, 64, 8
+    qa, sfa, qb, sfb, gsb, offs = _swiglu_case(rng, M, E, I, K, g, [4, 2])
+    h, a = oracle.grouped_swiglu(qa, sfa, 1.0, qb, sfb, gsb, offs, I, g, 10.0)
+    out0 = oracle.grouped_swiglu_bf16(qa, sfa, 1.0, qb, sfb, gsb, offs, I, g, 10.0, layout=0)
+    out1 = oracle.grouped_swiglu_bf16(qa, sfa, 1.0, qb, sfb, gsb, offs, I, g, 10.0, layout=1)
+    assert out0.shape == (M, I) and out1.shape == (M, 2 * I)
+    de = oracle.deinterleave(out1, g)
+    np.testing.assert_array_equal(de[:, I:], out0)
+    # bf16 rounding of the stored values: within half a bf16 ulp of the doubles
+    got = bf16_to_f32(out0).astype(np.float64)
+    assert np.all(np.abs(got - h) <= 2.0 ** -8 * np.abs(h) + 1e-300)
+    got_a = bf16_to_f32(de[:, :I]).astype(np.float64)
+    assert np.all(np.abs(got_a - a) <= 2.0 ** -8 * np.abs(a) + 1e-300)
