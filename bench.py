@@ -336,6 +336,57 @@ def time_op_flushed(fn, iters, flush):
     return sum(a.elapsed_time(b) for a, b in evs) / iters / 1e3
 
 
+class MoeL1:
+    """The MoE first projection of one layer: 256 experts' [2I, 7168] gate/up
+    weights (N(0, 0.02), drawn on the device per expert and quantized by the
+    library, each with its own global scale), and the grouped activations of
+    T tokens routed top-8 (the token rows gathered by expert, then quantized
+    together).  Set-up only; the timed call is nvfp4_grouped_swiglu_gemm."""
+
+    LIMIT = 10.0
+
+    def __init__(self, nv, ws, seed=2048):
+        import torch
+        E, I, K = EXPERTS, INTER, HIDDEN
+        self.qb = torch.empty(E * 2 * I, K // 2, dtype=torch.uint8, device="cuda")
+        self.sfb = torch.empty(E * 2 * I, K // 16, dtype=torch.uint8, device="cuda")
+        self.gsb = torch.empty(E, dtype=torch.float32, device="cuda")
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        for e in range(E):
+            w = (torch.randn(2 * I, K, generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            r = slice(e * 2 * I, (e + 1) * 2 * I)
+            nv.nvfp4_quantize(w, self.qb[r], self.sfb[r], self.gsb[e:e + 1], ws)
+        torch.cuda.synchronize()
+
+    def batch(self, nv, ws, tokens, seed):
+        import torch
+        tok, offs = workloads.moe_routing(tokens, EXPERTS, TOPK, seed)
+        x = torch.from_numpy(workloads.quantize_input(tokens, seed=seed + 1).view(np.int16)).cuda()
+        xg = x[torch.from_numpy(tok).cuda()].contiguous()
+        qa, sfa, gsa = nv.quantize(xg, ws)
+        out = torch.empty(xg.shape[0], INTER, dtype=torch.bfloat16, device="cuda")
+        active = int((offs[1:] > offs[:-1]).sum())
+        return dict(qa=qa, sfa=sfa, gsa=gsa, offs=torch.from_numpy(offs).cuda(), out=out, M=xg.shape[0],
+                    active=active)
+
+    def call(self, nv, ws, b):
+        nv.nvfp4_grouped_swiglu_gemm(b["qa"], b["sfa"], b["gsa"], self.qb, self.sfb, self.gsb, b["offs"], INTER,
+                                     GRAN, self.LIMIT, 0, b["out"], ws)
+
+    @staticmethod
+    def bytes(b):
+        """A codes + scales, the used experts' weights (codes + scales), the
+        global scales and offsets, the bf16 output."""
+        K = HIDDEN
+        return (b["M"] * (K // 2 + K // 16) + b["active"] * 2 * INTER * (K // 2 + K // 16)
+                + EXPERTS * 4 * 2 + 8 + b["M"] * INTER * 2)
+
+    @staticmethod
+    def flops(b):
+        return 2.0 * b["M"] * 2 * INTER * HIDDEN
+
+
 def secondary(nv, ws, pk, flush):
     """Per-kernel figures on the other pages' shapes (L2 flushed before each call)."""
     import torch
@@ -431,6 +482,20 @@ def secondary(nv, ws, pk, flush):
     by = gemm_bytes(32, E, HIDDEN, kv)
     out["router_E384_k6_norm_decode_T32"] = dict(us=round(tv * 1e6, 2), hbm_frac=round(by / tv / hbm, 4),
                                                  rows_per_s=round(32 / tv, 1))
+    # NEXT-4: grouped NVFP4 GEMM + SwiGLU, MoE first projection (256 experts,
+    # I = 2048, granularity 8, limit 10): decode (32 tokens x top-8) and
+    # prefill (8192 tokens x top-8)
+    moe = MoeL1(nv, ws)
+    for T, seed in ((32, 90), (8192, 91)):
+        b = moe.batch(nv, ws, T, seed)
+        tm = time_op_flushed(lambda: moe.call(nv, ws, b), 10 if T > 32 else 20, flush)
+        by, fl = MoeL1.bytes(b), MoeL1.flops(b)
+        out[f"moe_l1_T{T}_E256_I2048"] = dict(
+            us=round(tm * 1e6, 2), rows=b["M"], active_experts=b["active"], gbs=round(by / tm / 1e9, 1),
+            hbm_frac=round(by / tm / hbm, 3), tflops=round(fl / tm / 1e12, 1),
+            fp4_tensor_frac=round(fl / tm / fp4_peak, 3), tokens_per_s=round(T / tm, 1))
+        del b
+    del moe
     torch.cuda.synchronize()
     return out
 
@@ -609,6 +674,10 @@ def run_profile(kind: str, iters: int):
         idx = torch.empty(1, 512, dtype=torch.int32, device="cuda")
         sc = torch.empty(1, 512, dtype=torch.float32, device="cuda")
         fns = [lambda: nv.nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, 64, hw, 512, idx, sc, None, ws)]
+    elif kind in ("moe_decode", "moe_prefill"):
+        moe = MoeL1(nv, ws)
+        b = moe.batch(nv, ws, 32 if kind == "moe_decode" else 8192, 90)
+        fns = [lambda: moe.call(nv, ws, b)]
     elif kind == "indexer":
         d = workloads.indexer()
         qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
@@ -639,7 +708,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=32, choices=(1, 32))
     ap.add_argument("--quick", action="store_true", help="skip the secondary per-config figures")
     ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "quantize2048", "indexer",
-                                          "indexer_heads", "rmsnorm2048"),
+                                          "indexer_heads", "rmsnorm2048", "moe_decode", "moe_prefill"),
                     help="run --warmup eager iterations of one workload in an NVTX range and exit")
     args = ap.parse_args()
     if args.profile:

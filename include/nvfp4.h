@@ -15,6 +15,8 @@
  *                                epilogue and per-row top-k
  *   nvfp4_indexer_topk           the same GEMM with the indexer's weighted
  *                                ReLU head sum fused in, top-k per token
+ *   nvfp4_grouped_swiglu_gemm    grouped (per-expert) block-scaled FP4 GEMM
+ *                                with the MoE SwiGLU epilogue, bf16 out
  *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
@@ -71,6 +73,7 @@ typedef enum nvfp4_epilogue {
 
 /* Device-side status bits a kernel may record in the workspace. */
 #define NVFP4_DEVICE_TIMEOUT 0x1u /* a bounded wait inside a kernel gave up */
+#define NVFP4_DEVICE_BAD_GROUPS 0x2u /* group offsets broke their contract (grouped GEMM) */
 
 /* Bytes of workspace every call needs (a small constant). */
 size_t nvfp4_workspace_bytes(void);
@@ -231,6 +234,48 @@ int nvfp4_indexer_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
                        int k, int32_t* topk_idx, float* topk_score, float* scores,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Grouped block-scaled FP4 GEMM with the SwiGLU epilogue of the MoE first
+ * projection (compare view: the MoE kernel notes, fused SwiGLU grouped GEMM
+ * with L1 weights whose gate and up rows are interleaved at granularity 8;
+ * the model notes, "SwiGLU activation with swiglu_limit=10.0";
+ * PERFORMANCE_AUDIT.md P1, the [silu(gate), silu(gate)*up] interleaved
+ * output):
+ *
+ *   group e: A rows offsets[e] .. offsets[e+1]-1, weights W_e = B rows
+ *            e*2I .. e*2I + 2I - 1, global scale gsb[e]
+ *   logit[m, n] = gsa * gsb[e] * sum_k A[m, k] * W_e[n, k]   (FP32 accumulate)
+ *   gate_j = logit[m, 2g*floor(j/g) + j mod g],  up_j = the column g after it
+ *   a_j = silu(min(gate_j, limit)) = gate' / (1 + exp(-gate'))
+ *   h_j = a_j * min(max(up_j, -limit), limit)                  (FP32)
+ *   layout 0: out[m, j] = bf16(h_j)                 out is [M, ld_out], j < inter
+ *   layout 1: out[m, n] = bf16(a) where W row n is a gate row, bf16(h) where
+ *             it is an up row (the pages' interleaved output, the input of
+ *             nvfp4_deinterleave_quantize)             n < 2*inter
+ * (where the limit applies is not spelled out on the pages: the gate is
+ * clamped from above, the up value on both sides; pass INFINITY for none)
+ *
+ * A: qa [M, K/2], sfa [M, K/16], gsa (one quantize call for all rows; the
+ *    rows of each group contiguous, groups in order).
+ * B: qb [E*2I, K/2], sfb [E*2I, K/16] (the E experts' [2I, K] weights
+ *    stacked), gsb: E floats.  All four code/scale pointers 16-byte aligned.
+ * offsets: int32 [E+1] in DEVICE memory (written by the router on the GPU;
+ *    the host never reads it): non-decreasing, offsets[0] >= 0,
+ *    offsets[E] <= M.  Rows outside every group are not written.  Offsets
+ *    that break this are clamped into [0, M] (no access leaves the
+ *    buffers), the result is unspecified, and NVFP4_DEVICE_BAD_GROUPS is
+ *    recorded in the workspace.
+ * 1 <= E <= 1024.  inter (I): a positive multiple of 128.  K: a positive
+ * multiple of 256.  granularity: 1, 2, 4, 8 or 16.  limit > 0 (may be
+ * INFINITY).  out: bf16, 16-byte aligned, ld_out a multiple of 8 and at
+ * least I (layout 0) or 2I (layout 1).  M == 0 launches nothing.
+ * One persistent launch (one CTA per SM); FP32 logits never reach memory.
+ */
+int nvfp4_grouped_swiglu_gemm(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
+                              const uint8_t* qb, const uint8_t* sfb, const float* gsb,
+                              const int32_t* offsets, int64_t M, int64_t E, int64_t inter, int64_t K,
+                              int granularity, float limit, int layout, uint16_t* out, int64_t ld_out,
+                              void* ws, size_t ws_bytes, cudaStream_t stream);
 /*
  * Diagnostic: synchronise `stream`, copy the workspace's device status bits
  * (NVFP4_DEVICE_*) to *status, and clear them.  Not for the hot path.

@@ -12,6 +12,8 @@ The three entry points keep the C names:
 * ``nvfp4_deinterleave_quantize(x, granularity, q, sf, gs, ws, stream=None)``
 * ``nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, idx, score,
   weight=None, logits=None, ws=..., stream=None)``
+* ``nvfp4_grouped_swiglu_gemm(qa, sfa, gsa, qb, sfb, gsb, offsets, inter,
+  granularity, limit, layout, out, ws, stream=None)``
 
 plus allocating conveniences (``quantize``, ``deinterleave_quantize``,
 ``gemm_topk``, ``workspace``).
@@ -31,6 +33,7 @@ EPILOGUE_IDENTITY = 0
 EPILOGUE_SQRT_SOFTPLUS_BIAS = 1
 EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM = 2
 DEVICE_TIMEOUT = 0x1
+DEVICE_BAD_GROUPS = 0x2
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or alignment",
            3: "workspace missing or too small", 4: "CUDA error"}
@@ -82,6 +85,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_kernel_launches.argtypes = []
         L.nvfp4_quantize_noalloc.restype = I
         L.nvfp4_quantize_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P]
+        L.nvfp4_grouped_swiglu_gemm.restype = I
+        L.nvfp4_grouped_swiglu_gemm.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, ctypes.c_float, I,
+                                                P, I64, P, SZ, P]
         _lib = L
         return L
 
@@ -89,7 +95,8 @@ def lib() -> ctypes.CDLL:
 EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quantize",
                     "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
                     "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc",
-                    "nvfp4_kernel_launches", "nvfp4_rmsnorm_quantize", "nvfp4_indexer_topk")
+                    "nvfp4_kernel_launches", "nvfp4_rmsnorm_quantize", "nvfp4_indexer_topk",
+                    "nvfp4_grouped_swiglu_gemm")
 
 
 def _check(fn: str, status: int):
@@ -214,6 +221,31 @@ def nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, epilogue, bias, k, idx, score, w
         _ptr(qa), _ptr(sfa), _ptr(gsa), _ptr(qb), _ptr(sfb), _ptr(gsb), M, N, K, int(epilogue),
         _ptr(bias), int(k), _ptr(idx), _ptr(score), _ptr(weight), _ptr(logits), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def nvfp4_grouped_swiglu_gemm(qa, sfa, gsa, qb, sfb, gsb, offsets, inter, granularity, limit, layout, out,
+                              ws, stream=None):
+    """Grouped GEMM + SwiGLU: qb/sfb hold E experts' [2I, K] weights stacked, offsets
+    (int32 [E+1], device) the groups' row ranges of A; out is bf16 [M, I] or [M, 2I]."""
+    M = qa.shape[0]
+    K = qa.shape[1] * 2
+    E = offsets.numel() - 1
+    if offsets.dtype != torch.int32:
+        raise TypeError("offsets must be int32")
+    _check("nvfp4_grouped_swiglu_gemm", lib().nvfp4_grouped_swiglu_gemm(
+        _ptr(qa), _ptr(sfa), _ptr(gsa), _ptr(qb), _ptr(sfb), _ptr(gsb), _ptr(offsets), M, E, int(inter), K,
+        int(granularity), float(limit), int(layout), _ptr(out), out.stride(0), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def grouped_swiglu_gemm(qa, sfa, gsa, qb, sfb, gsb, offsets, inter, granularity, ws,
+                        limit=float("inf"), layout=0, stream=None):
+    """Allocating convenience: the bf16 output (rows outside every group are left as zeros)."""
+    M = qa.shape[0]
+    out = torch.zeros(M, inter if layout == 0 else 2 * inter, dtype=torch.bfloat16, device=qa.device)
+    nvfp4_grouped_swiglu_gemm(qa, sfa, gsa, qb, sfb, gsb, offsets, inter, granularity, limit, layout, out,
+                              ws, stream)
+    return out
 
 
 def read_device_status(ws, stream=None) -> int:

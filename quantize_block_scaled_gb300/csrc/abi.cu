@@ -217,6 +217,53 @@ int nvfp4_indexer_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa, 
   return rc;
 }
 
+int nvfp4_grouped_swiglu_gemm(const uint8_t* qa, const uint8_t* sfa, const float* gsa, const uint8_t* qb,
+                              const uint8_t* sfb, const float* gsb, const int32_t* offsets, int64_t M, int64_t E,
+                              int64_t inter, int64_t K, int granularity, float limit, int layout, uint16_t* out,
+                              int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  // With M == 0 nothing is launched (A, the offsets and out may be NULL).
+  if (gsa == nullptr || qb == nullptr || sfb == nullptr || gsb == nullptr) return NVFP4_ERR_INVALID;
+  if (M != 0 && (qa == nullptr || sfa == nullptr || offsets == nullptr || out == nullptr))
+    return NVFP4_ERR_INVALID;
+  if (M < 0 || M > kInt32Max || E < 1 || inter < 1 || K < 1 || K > kInt32Max) return NVFP4_ERR_INVALID;
+  if (E > 1024) return NVFP4_ERR_UNSUPPORTED;
+  if (layout != 0 && layout != 1) return NVFP4_ERR_INVALID;
+  if (!(limit > 0.0f)) return NVFP4_ERR_INVALID;  // also rejects NaN
+  if (granularity != 1 && granularity != 2 && granularity != 4 && granularity != 8 && granularity != 16)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (inter % 128 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (E * 2 * inter > kInt32Max) return NVFP4_ERR_UNSUPPORTED;
+  if (ld_out < (layout == 0 ? inter : 2 * inter) || ld_out % 8 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((M / 128 + E) * (2 * inter / 256) > kInt32Max) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned(qa, 16) || !aligned(sfa, 16) || !aligned(qb, 16) || !aligned(sfb, 16) || !aligned(gsa, 4) ||
+      !aligned(gsb, 4) || !aligned(offsets, 4) || !aligned(out, 16))
+    return NVFP4_ERR_UNSUPPORTED;
+  const int st = check_workspace(ws, ws_bytes);
+  if (st != NVFP4_OK) return st;
+  nvfp4::GroupedSwigluArgs a;
+  a.qa = qa;
+  a.sfa = sfa;
+  a.gsa = gsa;
+  a.qb = qb;
+  a.sfb = sfb;
+  a.gsb = gsb;
+  a.offsets = offsets;
+  a.M = M;
+  a.E = E;
+  a.inter = inter;
+  a.K = K;
+  a.granularity = granularity;
+  a.limit = limit;
+  a.layout = layout;
+  a.out = out;
+  a.ld_out = ld_out;
+  a.ws = static_cast<nvfp4::Workspace*>(ws);
+  cudaError_t e = cudaSuccess;
+  const int rc = nvfp4::launch_grouped_swiglu(a, stream, &e);
+  if (rc == NVFP4_ERR_CUDA) return cuda_failure(e);
+  return rc;
+}
+
 int nvfp4_read_device_status(void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t stream) {
   if (status == nullptr) return NVFP4_ERR_INVALID;
   const int st = check_workspace(ws, ws_bytes);

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
 namespace nvfp4 {
@@ -73,5 +74,30 @@ struct GemmTopkArgs {
 
 // Returns an nvfp4_status; on NVFP4_ERR_CUDA the CUDA error is in *err.
 int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* err);
+
+// Tensor map of a 2-D byte matrix [rows, width] (row stride = width) with
+// boxes of box_w bytes x box_rows rows, optional 128-byte swizzle; reads past
+// the matrix return zeros.  False if the driver refuses it.
+bool make_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t width, int box_w,
+              int box_rows, bool swizzle128);
+
+struct GroupedSwigluArgs {
+  const uint8_t* qa;
+  const uint8_t* sfa;
+  const float* gsa;
+  const uint8_t* qb;
+  const uint8_t* sfb;
+  const float* gsb;        // [E]
+  const int32_t* offsets;  // [E + 1], device
+  int64_t M, E, inter, K;
+  int granularity;
+  float limit;
+  int layout;
+  uint16_t* out;
+  int64_t ld_out;
+  Workspace* ws;
+};
+
+int launch_grouped_swiglu(const GroupedSwigluArgs& a, cudaStream_t stream, cudaError_t* err);
 
 }  // namespace nvfp4

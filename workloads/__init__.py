@@ -134,3 +134,27 @@ def swiglu_interleaved(tokens: int, inter: int = MOE_INTER, seed: int = 6) -> np
     the consumer reads the row, not of how it was drawn.
     """
     return quantize_input(tokens, seed=seed, cols=2 * inter)
+
+
+def moe_routing(tokens: int, experts: int, topk: int, seed: int):
+    """Token-to-expert routing of one MoE layer: each token picks ``topk``
+    distinct experts uniformly at random.  Returns (token_of_row, offsets):
+    the (token, expert) pairs sorted by expert (then token), as the source
+    token of each grouped row, and the int32 [experts + 1] group offsets."""
+    rng = np.random.default_rng(seed)
+    picks = np.stack([rng.choice(experts, size=topk, replace=False) for _ in range(tokens)]) \
+        if tokens else np.zeros((0, topk), np.int64)
+    tok = np.repeat(np.arange(tokens), topk)
+    exp_ = picks.reshape(-1)
+    order = np.lexsort((tok, exp_))
+    counts = np.bincount(exp_, minlength=experts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return tok[order].astype(np.int64), offsets
+
+
+def moe_l1_weights(experts: int, inter: int, hidden: int, seed: int, std: float = 0.02) -> np.ndarray:
+    """The experts' first-projection weights, [experts * 2I, hidden] bf16 N(0, std):
+    rows e*2I .. e*2I + 2I - 1 are expert e's gate/up rows (interleaved layout
+    is a matter of how they are read; the draws are i.i.d.)."""
+    rng = np.random.default_rng(seed)
+    return bf16_bits(_normal(rng, (experts * 2 * inter, hidden), std))
