@@ -345,9 +345,10 @@ class MoeL1:
 
     LIMIT = 10.0
 
-    def __init__(self, nv, ws, seed=2048):
+    def __init__(self, nv, ws, seed=2048, experts=EXPERTS):
         import torch
-        E, I, K = EXPERTS, INTER, HIDDEN
+        self.E = E = experts
+        I, K = INTER, HIDDEN
         self.qb = torch.empty(E * 2 * I, K // 2, dtype=torch.uint8, device="cuda")
         self.sfb = torch.empty(E * 2 * I, K // 16, dtype=torch.uint8, device="cuda")
         self.gsb = torch.empty(E, dtype=torch.float32, device="cuda")
@@ -361,7 +362,7 @@ class MoeL1:
 
     def batch(self, nv, ws, tokens, seed):
         import torch
-        tok, offs = workloads.moe_routing(tokens, EXPERTS, TOPK, seed)
+        tok, offs = workloads.moe_routing(tokens, self.E, TOPK, seed)
         x = torch.from_numpy(workloads.quantize_input(tokens, seed=seed + 1).view(np.int16)).cuda()
         xg = x[torch.from_numpy(tok).cuda()].contiguous()
         qa, sfa, gsa = nv.quantize(xg, ws)
@@ -374,13 +375,12 @@ class MoeL1:
         nv.nvfp4_grouped_swiglu_gemm(b["qa"], b["sfa"], b["gsa"], self.qb, self.sfb, self.gsb, b["offs"], INTER,
                                      GRAN, self.LIMIT, 0, b["out"], ws)
 
-    @staticmethod
-    def bytes(b):
+    def bytes(self, b):
         """A codes + scales, the used experts' weights (codes + scales), the
         global scales and offsets, the bf16 output."""
         K = HIDDEN
         return (b["M"] * (K // 2 + K // 16) + b["active"] * 2 * INTER * (K // 2 + K // 16)
-                + EXPERTS * 4 * 2 + 8 + b["M"] * INTER * 2)
+                + self.E * 4 * 2 + 8 + b["M"] * INTER * 2)
 
     @staticmethod
     def flops(b):
@@ -489,7 +489,7 @@ def secondary(nv, ws, pk, flush):
     for T, seed in ((32, 90), (8192, 91)):
         b = moe.batch(nv, ws, T, seed)
         tm = time_op_flushed(lambda: moe.call(nv, ws, b), 10 if T > 32 else 20, flush)
-        by, fl = MoeL1.bytes(b), MoeL1.flops(b)
+        by, fl = moe.bytes(b), MoeL1.flops(b)
         out[f"moe_l1_T{T}_E256_I2048"] = dict(
             us=round(tm * 1e6, 2), rows=b["M"], active_experts=b["active"], gbs=round(by / tm / 1e9, 1),
             hbm_frac=round(by / tm / hbm, 3), tflops=round(fl / tm / 1e12, 1),
@@ -674,9 +674,11 @@ def run_profile(kind: str, iters: int):
         idx = torch.empty(1, 512, dtype=torch.int32, device="cuda")
         sc = torch.empty(1, 512, dtype=torch.float32, device="cuda")
         fns = [lambda: nv.nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, 64, hw, 512, idx, sc, None, ws)]
-    elif kind in ("moe_decode", "moe_prefill"):
-        moe = MoeL1(nv, ws)
-        b = moe.batch(nv, ws, 32 if kind == "moe_decode" else 8192, 90)
+    elif kind in ("moe_decode", "moe_prefill", "moe_small"):
+        # moe_small: 32 experts (0.5 GB of weights), 1024 tokens: a capture-sized
+        # case with full 128-row tiles
+        moe = MoeL1(nv, ws, experts=32 if kind == "moe_small" else EXPERTS)
+        b = moe.batch(nv, ws, {"moe_decode": 32, "moe_prefill": 8192, "moe_small": 1024}[kind], 90)
         fns = [lambda: moe.call(nv, ws, b)]
     elif kind == "indexer":
         d = workloads.indexer()
@@ -708,7 +710,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=32, choices=(1, 32))
     ap.add_argument("--quick", action="store_true", help="skip the secondary per-config figures")
     ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "quantize2048", "indexer",
-                                          "indexer_heads", "rmsnorm2048", "moe_decode", "moe_prefill"),
+                                          "indexer_heads", "rmsnorm2048", "moe_decode", "moe_prefill", "moe_small"),
                     help="run --warmup eager iterations of one workload in an NVTX range and exit")
     args = ap.parse_args()
     if args.profile:

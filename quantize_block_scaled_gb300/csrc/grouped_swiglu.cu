@@ -29,7 +29,10 @@
 // Per CTA, 6 warps:
 //   warp 0     producer: TMA loads of the A and B code tiles (128-byte rows,
 //              128-byte swizzle) and the row-major E4M3 scale boxes into a
-//              3-stage ring that runs on across work items.
+//              3-stage ring that runs on across work items.  The scale boxes
+//              complete on a barrier of their own, so their rearrangement
+//              and copy into TMEM overlap the landing of the code tiles; A
+//              comes in 32-row boxes, only those holding the item's rows.
 //   warp 1     MMA issuer (one thread): four 128 x 256 x 64 kind::mxf4nvf4
 //              block-scaled MMAs per stage into one TMEM accumulator; before
 //              the first MMA of an item it waits until the epilogue has read
@@ -87,10 +90,16 @@ constexpr uint32_t offSfaMma = offSfbStage + kSfbStage;
 constexpr uint32_t offSfbMma = offSfaMma + 4 * kSfChunk;
 constexpr uint32_t kStage = offSfbMma + 8 * kSfChunk;  // 60 KB
 constexpr uint32_t kSfTmemPerStage = 16 + 32;          // SFA: 4 x 4 columns, SFB: 4 x 8
-constexpr uint32_t kTx = kA + kB + kSfaStage + kSfbStage;
+// A and its scales arrive in boxes of 32 rows, only as many as the item's
+// rows need (a decode-sized group fills one); the MMA still reads 128 rows,
+// and rows past the loaded boxes only feed accumulator rows never stored.
+constexpr int kABox = 32;
+constexpr uint32_t kABoxBytes = kABox * BKB;
+constexpr uint32_t kSfaBoxBytes = kABox * 16;
 static_assert(kStage % 1024 == 0, "stages keep the 1 KB alignment of the 128-byte swizzle");
+static_assert(kABoxBytes % 1024 == 0, "A boxes keep the 8-row swizzle pattern");
 static_assert(kSfTmemBase + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
-static_assert((3 * kStages + 4) * 8 <= 128, "barriers precede the TMEM slot");
+static_assert((4 * kStages + 4) * 8 <= 128, "barriers precede the TMEM slot");
 
 struct Params {
   const float* gsa;
@@ -175,10 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return smem_addr(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_addr(&bars[kStages + s]); };
   auto sfready_bar = [&](int s) { return smem_addr(&bars[2 * kStages + s]); };
-  const uint32_t tfull_bar = smem_addr(&bars[3 * kStages]);       // accumulator complete
-  const uint32_t tempty_bar = smem_addr(&bars[3 * kStages + 1]);  // accumulator read out
-  const uint32_t drain_bar = smem_addr(&bars[3 * kStages + 2]);   // MMAs drained
-  const uint32_t xdrain_bar = smem_addr(&bars[3 * kStages + 3]);  // scale copies drained
+  auto sffull_bar = [&](int s) { return smem_addr(&bars[3 * kStages + s]); };  // scale boxes landed
+  const uint32_t tfull_bar = smem_addr(&bars[4 * kStages]);       // accumulator complete
+  const uint32_t tempty_bar = smem_addr(&bars[4 * kStages + 1]);  // accumulator read out
+  const uint32_t drain_bar = smem_addr(&bars[4 * kStages + 2]);   // MMAs drained
+  const uint32_t xdrain_bar = smem_addr(&bars[4 * kStages + 3]);  // scale copies drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
   volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 132);
   int* tstart = reinterpret_cast<int*>(ctrl + kCtrlBytes);  // [E + 1] first row tile of each group
@@ -188,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
+      mbar_init(sffull_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sfready_bar(s), 4);  // one tcgen05.commit per scale-layout warp
     }
@@ -250,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
       const Item it = item_of(w, p, tstart, glo, ghi);
       const int brow = it.e * p.two_i + it.n0;
+      const int na = (it.vr + kABox - 1) / kABox;  // A boxes holding the item's rows
       for (int kt = 0; kt < nk; ++kt, ++i) {
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
@@ -260,11 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
           const uint32_t st = sbase + s * kStage;
-          mbar_arrive_expect_tx(full_bar(s), kTx);
-          tma_load_2d(st, &tma_a, full_bar(s), kt * BKB, it.m0);
+          mbar_arrive_expect_tx(sffull_bar(s), na * kSfaBoxBytes + kSfbStage);
+          for (int q = 0; q < na; ++q)
+            tma_load_2d(st + offSfaStage + q * kSfaBoxBytes, &tma_sfa, sffull_bar(s), kt * 16, it.m0 + q * kABox);
+          tma_load_2d(st + offSfbStage, &tma_sfb, sffull_bar(s), kt * 16, brow);
+          mbar_arrive_expect_tx(full_bar(s), na * kABoxBytes + kB);
+          for (int q = 0; q < na; ++q)
+            tma_load_2d(st + q * kABoxBytes, &tma_a, full_bar(s), kt * BKB, it.m0 + q * kABox);
           tma_load_2d(st + offB, &tma_b, full_bar(s), kt * BKB, brow);
-          tma_load_2d(st + offSfaStage, &tma_sfa, full_bar(s), kt * 16, it.m0);
-          tma_load_2d(st + offSfbStage, &tma_sfb, full_bar(s), kt * 16, brow);
         }
         __syncwarp();
       }
@@ -275,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) {
         const int i_s = last - (((last - s) % kStages) + kStages) % kStages;
         if (last >= 0 && i_s >= 0 &&
-            !mbar_wait_bounded(full_bar(s), (i_s / kStages) & 1, &never, kWaitLimit))
+            (!mbar_wait_bounded(full_bar(s), (i_s / kStages) & 1, &never, kWaitLimit) ||
+             !mbar_wait_bounded(sffull_bar(s), (i_s / kStages) & 1, &never, kWaitLimit)))
           record_timeout(p.status, abort);
       }
     }
@@ -333,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < nk; ++kt, ++i) {
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!warp_wait(full_bar(s), ph, abort)) {
+        if (!warp_wait(sffull_bar(s), ph, abort)) {
           if (lane == 0) record_timeout(p.status, abort);
           ok = false;
           break;
@@ -466,9 +482,9 @@ int launch_grouped_swiglu(const GroupedSwigluArgs& a, cudaStream_t stream, cudaE
   if (a.M == 0) return NVFP4_OK;
   const int64_t two_i = 2 * a.inter;
   CUtensorMap ma, mb, msa, msb;
-  if (!make_map(&ma, a.qa, a.M, a.K / 2, BKB, BM, true) ||
+  if (!make_map(&ma, a.qa, a.M, a.K / 2, BKB, kABox, true) ||
       !make_map(&mb, a.qb, a.E * two_i, a.K / 2, BKB, BN, true) ||
-      !make_map(&msa, a.sfa, a.M, a.K / 16, 16, BM, false) ||
+      !make_map(&msa, a.sfa, a.M, a.K / 16, 16, kABox, false) ||
       !make_map(&msb, a.sfb, a.E * two_i, a.K / 16, 16, BN, false))
     return NVFP4_ERR_UNSUPPORTED;
   Params p;
