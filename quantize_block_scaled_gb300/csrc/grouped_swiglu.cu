@@ -70,15 +70,17 @@ constexpr int BM = 128;              // MMA M: rows of A per tile
 constexpr int BN = 256;              // MMA N: weight rows per slice
 constexpr int BKB = 128;             // bytes of a K tile per row = 256 FP4 elements
 constexpr int kThreads = 192;
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;        // 4 when the group tables leave room, else 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;  // scale factors after the 256-column accumulator
 constexpr uint32_t kSfChunk = 512;     // scales of 128 rows for one MMA (K = 64)
-constexpr uint32_t kCtrlBytes = 256;
+constexpr uint32_t kCtrlBytes = 256;  // barriers, then the TMEM address at byte 192
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
 
-// Stage layout: A codes, B codes, the scale boxes as loaded (row-major 16
-// bytes per row), then the same scales rearranged for tcgen05.cp.
+// Stage layout: A codes, B codes, then the scale boxes as loaded (row-major
+// 16 bytes per row), which the scale warps rearrange in place into the
+// layout tcgen05.cp reads (each 2 KB atom of 128 rows becomes four 512-byte
+// chunks, one per MMA step).
 constexpr uint32_t kA = BM * BKB;                  // 16 KB
 constexpr uint32_t kB = BN * BKB;                  // 32 KB
 constexpr uint32_t kSfaStage = BM * 16;
@@ -86,9 +88,7 @@ constexpr uint32_t kSfbStage = BN * 16;
 constexpr uint32_t offB = kA;
 constexpr uint32_t offSfaStage = kA + kB;
 constexpr uint32_t offSfbStage = offSfaStage + kSfaStage;
-constexpr uint32_t offSfaMma = offSfbStage + kSfbStage;
-constexpr uint32_t offSfbMma = offSfaMma + 4 * kSfChunk;
-constexpr uint32_t kStage = offSfbMma + 8 * kSfChunk;  // 60 KB
+constexpr uint32_t kStage = offSfbStage + kSfbStage;  // 54 KB
 constexpr uint32_t kSfTmemPerStage = 16 + 32;          // SFA: 4 x 4 columns, SFB: 4 x 8
 // A and its scales arrive in boxes of 32 rows, only as many as the item's
 // rows need (a decode-sized group fills one); the MMA still reads 128 rows,
@@ -98,8 +98,8 @@ constexpr uint32_t kABoxBytes = kABox * BKB;
 constexpr uint32_t kSfaBoxBytes = kABox * 16;
 static_assert(kStage % 1024 == 0, "stages keep the 1 KB alignment of the 128-byte swizzle");
 static_assert(kABoxBytes % 1024 == 0, "A boxes keep the 8-row swizzle pattern");
-static_assert(kSfTmemBase + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
-static_assert((4 * kStages + 4) * 8 <= 128, "barriers precede the TMEM slot");
+static_assert(kSfTmemBase + kMaxStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
+static_assert((4 * kMaxStages + 4) * 8 <= 192, "barriers precede the TMEM slot");
 
 struct Params {
   const float* gsa;
@@ -114,6 +114,7 @@ struct Params {
   int num_k_tiles;    // K / 256
   int n_tiles;        // 2I / 256
   int max_row_tiles;  // row tiles the item list may hold (a bound for valid offsets)
+  int stages;         // pipeline depth (3 or 4)
 };
 
 // Instruction descriptor of kind::mxf4nvf4: E2M1 A and B, E4M3 scales, both
@@ -132,6 +133,21 @@ __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32
   atomicOr(status, NVFP4_DEVICE_TIMEOUT);
 }
 
+// Named barrier 1 over the four scale/epilogue warps (128 threads); returns
+// whether any of them passed `fail`, so all four take the same branch.
+__device__ __forceinline__ bool bar_any_128(bool fail) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(fail ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -141,6 +157,54 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
+}
+
+// tcgen05.ld writes its registers asynchronously: after tcgen05.wait::ld,
+// this empty asm marks them as (re)defined, so no use of them can be
+// scheduled before the wait.
+__device__ __forceinline__ void regs_after_wait(uint32_t (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[i]));
+}
+
+// Clamp + SwiGLU of one 32-column accumulator chunk of row `orow` (TMEM
+// words v), then the bf16 store: 16 values h (layout 0) at output column
+// (n0 + c) / 2, or the chunk's 32 columns as a / h (layout 1) at n0 + c.
+// exp and the quotient use the fast hardware approximations (a few ulp;
+// far inside the epilogue's tolerance).
+template <int G>
+__device__ __forceinline__ void swiglu_chunk(const uint32_t (&v)[32], float gab, float limit, int layout,
+                                             uint16_t* orow, int col) {
+  float av[16], hv[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    // x-th (gate, up) pair of the chunk: run x / G, offset x % G
+    const int gi = (x / G) * 2 * G + (x % G);
+    const float gate = fminf(__uint_as_float(v[gi]) * gab, limit);
+    const float up = fminf(fmaxf(__uint_as_float(v[gi + G]) * gab, -limit), limit);
+    av[x] = __fdividef(gate, 1.0f + __expf(-gate));
+    hv[x] = av[x] * up;
+  }
+  if (layout == 0) {
+    uint16_t* dst = orow + col / 2;
+    st_global_v4(dst, pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
+                 pack_bf16x2(hv[6], hv[7]));
+    st_global_v4(dst + 8, pack_bf16x2(hv[8], hv[9]), pack_bf16x2(hv[10], hv[11]), pack_bf16x2(hv[12], hv[13]),
+                 pack_bf16x2(hv[14], hv[15]));
+  } else {
+    // column y of the chunk: run y / G (even: gate -> a, odd: up -> h)
+    float o[32];
+#pragma unroll
+    for (int y = 0; y < 32; ++y) {
+      const int x = (y / (2 * G)) * G + (y % G);
+      o[y] = ((y / G) & 1) ? hv[x] : av[x];
+    }
+    uint16_t* dst = orow + col;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_global_v4(dst + 8 * q, pack_bf16x2(o[8 * q], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
+                   pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+  }
 }
 
 // One work item: rows m0 .. m0 + vr - 1 of A against weight rows brow ..
@@ -179,24 +243,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  uint8_t* ctrl = smem + kStages * kStage;
+  const int S = p.stages;
+  uint8_t* ctrl = smem + S * kStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
   auto full_bar = [&](int s) { return smem_addr(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_addr(&bars[kStages + s]); };
-  auto sfready_bar = [&](int s) { return smem_addr(&bars[2 * kStages + s]); };
-  auto sffull_bar = [&](int s) { return smem_addr(&bars[3 * kStages + s]); };  // scale boxes landed
-  const uint32_t tfull_bar = smem_addr(&bars[4 * kStages]);       // accumulator complete
-  const uint32_t tempty_bar = smem_addr(&bars[4 * kStages + 1]);  // accumulator read out
-  const uint32_t drain_bar = smem_addr(&bars[4 * kStages + 2]);   // MMAs drained
-  const uint32_t xdrain_bar = smem_addr(&bars[4 * kStages + 3]);  // scale copies drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
-  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 132);
+  auto empty_bar = [&](int s) { return smem_addr(&bars[kMaxStages + s]); };
+  auto sfready_bar = [&](int s) { return smem_addr(&bars[2 * kMaxStages + s]); };
+  auto sffull_bar = [&](int s) { return smem_addr(&bars[3 * kMaxStages + s]); };  // scale boxes landed
+  const uint32_t tfull_bar = smem_addr(&bars[4 * kMaxStages]);       // accumulator complete
+  const uint32_t tempty_bar = smem_addr(&bars[4 * kMaxStages + 1]);  // accumulator read out
+  const uint32_t drain_bar = smem_addr(&bars[4 * kMaxStages + 2]);   // MMAs drained
+  const uint32_t xdrain_bar = smem_addr(&bars[4 * kMaxStages + 3]);  // scale copies drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 192);
+  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 196);
   int* tstart = reinterpret_cast<int*>(ctrl + kCtrlBytes);  // [E + 1] first row tile of each group
   int* glo = tstart + (p.E + 1);                              // [E] clamped first row
   int* ghi = glo + p.E;                                       // [E] clamped end row
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(sffull_bar(s), 1);
       mbar_init(empty_bar(s), 1);
@@ -263,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int brow = it.e * p.two_i + it.n0;
       const int na = (it.vr + kABox - 1) / kABox;  // A boxes holding the item's rows
       for (int kt = 0; kt < nk; ++kt, ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
         if (!warp_wait(empty_bar(s), ph ^ 1u, abort)) {
           if (lane == 0) record_timeout(p.status, abort);
           ok = false;
@@ -287,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {  // let every copy issued here land before the CTA can exit
       uint32_t never = 0;
       const int last = i - 1;
-      for (int s = 0; s < kStages; ++s) {
-        const int i_s = last - (((last - s) % kStages) + kStages) % kStages;
+      for (int s = 0; s < S; ++s) {
+        const int i_s = last - (((last - s) % S) + S) % S;
         if (last >= 0 && i_s >= 0 &&
-            (!mbar_wait_bounded(full_bar(s), (i_s / kStages) & 1, &never, kWaitLimit) ||
-             !mbar_wait_bounded(sffull_bar(s), (i_s / kStages) & 1, &never, kWaitLimit)))
+            (!mbar_wait_bounded(full_bar(s), (i_s / S) & 1, &never, kWaitLimit) ||
+             !mbar_wait_bounded(sffull_bar(s), (i_s / S) & 1, &never, kWaitLimit)))
           record_timeout(p.status, abort);
       }
     }
@@ -309,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       for (int kt = 0; kt < nk; ++kt, ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
         if (!warp_wait(full_bar(s), ph, abort) || !warp_wait(sfready_bar(s), ph, abort)) {
           if (lane == 0) record_timeout(p.status, abort);
           ok = false;
@@ -347,42 +412,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++t) {
       for (int kt = 0; kt < nk; ++kt, ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!warp_wait(sffull_bar(s), ph, abort)) {
-          if (lane == 0) record_timeout(p.status, abort);
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
+        // the four warps leave together when any of them gave up waiting
+        const bool failed = !warp_wait(sffull_bar(s), ph, abort);
+        if (bar_any_128(failed)) {
+          if (failed && lane == 0) record_timeout(p.status, abort);
           ok = false;
           break;
         }
         const uint32_t st = sbase + s * kStage;
         // Staged row r (16 bytes: MMA words 0..3) -> chunk u gets, at offset
-        // 16 * r0, word u of rows r0, r0 + 32, r0 + 64, r0 + 96.
+        // 16 * r0, word u of rows r0, r0 + 32, r0 + 64, r0 + 96.  Chunk u
+        // overwrites staged rows 32u .. 32u + 31 of the atom, so every warp
+        // reads its words before any writes (the barrier in between).
+        uint32_t sw[3][4];
 #pragma unroll
         for (int a = 0; a < 3; ++a) {
           const uint32_t src = a == 0 ? st + offSfaStage : st + offSfbStage + (a - 1) * 2048;
-          const uint32_t dst = a == 0 ? st + offSfaMma + u * kSfChunk : st + offSfbMma + (u * 2 + (a - 1)) * kSfChunk;
-          const uint32_t w0 = ld_shared_u32(src + (0 * 32 + lane) * 16 + u * 4);
-          const uint32_t w1 = ld_shared_u32(src + (1 * 32 + lane) * 16 + u * 4);
-          const uint32_t w2 = ld_shared_u32(src + (2 * 32 + lane) * 16 + u * 4);
-          const uint32_t w3 = ld_shared_u32(src + (3 * 32 + lane) * 16 + u * 4);
-          st_shared_v4(dst + lane * 16, w0, w1, w2, w3);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sw[a][q] = ld_shared_u32(src + (q * 32 + lane) * 16 + u * 4);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+          const uint32_t atom = a == 0 ? st + offSfaStage : st + offSfbStage + (a - 1) * 2048;
+          st_shared_v4(atom + u * kSfChunk + lane * 16, sw[a][0], sw[a][1], sw[a][2], sw[a][3]);
         }
         fence_proxy_async_smem();  // read by tcgen05.cp through the async proxy
         __syncwarp();
         if (lane == 0) {
           tc_fence_after();
           const uint32_t sf_col = tmem + kSfTmemBase + s * kSfTmemPerStage;
-          tc_cp_32x128b_warpx4(sf_col + u * 4, smem_desc(st + offSfaMma + u * kSfChunk, 0, 128, 0));
-          tc_cp_32x128b_warpx4(sf_col + 16 + u * 8, smem_desc(st + offSfbMma + (u * 2) * kSfChunk, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sf_col + u * 4, smem_desc(st + offSfaStage + u * kSfChunk, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sf_col + 16 + u * 8, smem_desc(st + offSfbStage + u * kSfChunk, 0, 128, 0));
           tc_cp_32x128b_warpx4(sf_col + 16 + u * 8 + 4,
-                               smem_desc(st + offSfbMma + (u * 2 + 1) * kSfChunk, 0, 128, 0));
+                               smem_desc(st + offSfbStage + 2048 + u * kSfChunk, 0, 128, 0));
           tc_commit(sfready_bar(s));
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (!warp_wait(tfull_bar, t & 1, abort)) {
-        if (lane == 0) record_timeout(p.status, abort);
+      const bool tfailed = !warp_wait(tfull_bar, t & 1, abort);
+      if (bar_any_128(tfailed)) {  // (uniform: the next item's barriers need all four warps)
+        if (tfailed && lane == 0) record_timeout(p.status, abort);
         break;
       }
       tc_fence_after();
@@ -392,44 +465,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float gab = gsa * __ldg(p.gsb + it.e);
         const bool live = row < it.vr;
         uint16_t* orow = p.out + static_cast<int64_t>(it.m0 + (live ? row : 0)) * p.ld_out;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + c + (static_cast<uint32_t>(quarter * 32) << 16), v);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        // two chunks in flight: the load of chunk c + 32 overlaps the math of chunk c
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32(taddr, va);
+#pragma unroll
+        for (int c = 0; c < BN; c += 64) {
           tmem_wait_ld();
-          if (live) {
-            float av[16], hv[16];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              // x-th (gate, up) pair of the chunk: run x / G, offset x % G
-              const int gi = (x / G) * 2 * G + (x % G);
-              const float gate = fminf(__uint_as_float(v[gi]) * gab, p.limit);
-              const float up = fminf(fmaxf(__uint_as_float(v[gi + G]) * gab, -p.limit), p.limit);
-              av[x] = gate / (1.0f + __expf(-gate));
-              hv[x] = av[x] * up;
-            }
-            if (p.layout == 0) {
-              uint16_t* dst = orow + (it.n0 + c) / 2;
-              st_global_v4(dst, pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
-                           pack_bf16x2(hv[6], hv[7]));
-              st_global_v4(dst + 8, pack_bf16x2(hv[8], hv[9]), pack_bf16x2(hv[10], hv[11]),
-                           pack_bf16x2(hv[12], hv[13]), pack_bf16x2(hv[14], hv[15]));
-            } else {
-              // column c + y of the chunk: run y / G (even: gate -> a, odd: up -> h)
-              float o[32];
-#pragma unroll
-              for (int y = 0; y < 32; ++y) {
-                const int x = (y / (2 * G)) * G + (y % G);
-                o[y] = ((y / G) & 1) ? hv[x] : av[x];
-              }
-              uint16_t* dst = orow + it.n0 + c;
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                st_global_v4(dst + 8 * q, pack_bf16x2(o[8 * q], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
-                             pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
-            }
-          }
+          regs_after_wait(va);
+          tmem_ld_32x32b_x32(taddr + c + 32, vb);
+          if (live) swiglu_chunk<G>(va, gab, p.limit, p.layout, orow, it.n0 + c);
+          tmem_wait_ld();
+          regs_after_wait(vb);
+          if (c + 64 < BN) tmem_ld_32x32b_x32(taddr + c + 64, va);
+          if (live) swiglu_chunk<G>(vb, gab, p.limit, p.layout, orow, it.n0 + c + 32);
         }
+        tmem_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
@@ -451,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t smem_bytes(int64_t E) {
-  return 1024 + static_cast<size_t>(kStages) * kStage + kCtrlBytes + static_cast<size_t>(3 * E + 1) * 4;
+size_t smem_bytes(int stages, int64_t E) {
+  return 1024 + static_cast<size_t>(stages) * kStage + kCtrlBytes + static_cast<size_t>(3 * E + 1) * 4;
 }
 
 template <int G>
@@ -508,7 +559,11 @@ int launch_grouped_swiglu(const GroupedSwigluArgs& a, cudaStream_t stream, cudaE
   p.max_row_tiles = static_cast<int>(row_tiles);
   const int64_t items = row_tiles * p.n_tiles;
   const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
-  const size_t smem = smem_bytes(a.E);
+  int smem_optin = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  p.stages = smem_bytes(kMaxStages, a.E) <= static_cast<size_t>(smem_optin) ? kMaxStages : kMaxStages - 1;
+  const size_t smem = smem_bytes(p.stages, a.E);
   cudaError_t e;
   switch (a.granularity) {
     case 1: e = launch_g<1>(ma, mb, msa, msb, p, grid, smem, stream); break;
