@@ -387,8 +387,71 @@ class MoeL1:
         return 2.0 * b["M"] * 2 * INTER * HIDDEN
 
 
+ROTATE_BYTES = int(2.2 * L2_BYTES)  # inputs rotated per timed pass: more than twice the L2 cache
+ROTATE_MAX_SETS = 2048
+
+
+def rotating_sets(bytes_per_call):
+    """Input copies a rotation needs so that one pass reads more than 2.2x L2, or
+    None when that takes more than ROTATE_MAX_SETS copies (then L2 is flushed)."""
+    n = -(-ROTATE_BYTES // max(1, bytes_per_call))
+    return max(2, n) if n <= ROTATE_MAX_SETS else None
+
+
+def time_rotating(fn, n_sets, reps=3):
+    """Average device time of fn(i) over one pass of i = 0 .. n_sets - 1 (each
+    call on its own input copy, so the inputs come from HBM while the
+    kernels' code stays in L2), replayed from a CUDA graph; eager replays if
+    the calls cannot be captured."""
+    import torch
+    cur = torch.cuda.current_stream()
+    s = torch.cuda.Stream()
+    s.wait_stream(cur)
+    with torch.cuda.stream(s):
+        for i in range(n_sets):  # eager warm-up (kernel attributes, tensor maps)
+            fn(i)
+    cur.wait_stream(s)
+    torch.cuda.synchronize()
+    g = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_sets):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+    except RuntimeError:
+        g = None
+        torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(n_sets):
+                fn(i)
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / (reps * n_sets), ("graph" if g is not None else "eager")
+
+
+def time_op(make_inputs, call, bytes_per_call, flush, iters=30):
+    """(seconds per call, how): rotating input copies when a pass over them can
+    exceed 2.2x L2 (make_inputs(i) builds copy i), else an L2 flush before each
+    call on copy 0."""
+    n = rotating_sets(bytes_per_call)
+    if n is None:
+        inp = make_inputs(0)
+        return time_op_flushed(lambda: call(inp), iters, flush), "l2 flushed before each call"
+    sets = [make_inputs(i) for i in range(n)]
+    t, how = time_rotating(lambda i: call(sets[i]), n)
+    return t, f"{n} rotating input copies ({n * bytes_per_call / 2**20:.0f} MiB), {how} replay"
+
+
 def secondary(nv, ws, pk, flush):
-    """Per-kernel figures on the other pages' shapes (L2 flushed before each call)."""
+    """Per-kernel figures on the other pages' shapes: inputs rotated over more
+    than twice the L2 cache where that is possible, else L2 flushed per call."""
     import torch
     out = {}
     hbm = pk["hbm_gbs"] * 1e9
@@ -396,30 +459,36 @@ def secondary(nv, ws, pk, flush):
     # quantize sweep
     sweep = {}
     for T in (1, 128, 2048, 16384):
-        x = torch.from_numpy(workloads.quantize_input(T).view(np.int16)).cuda()
-        q, sf, gs = nv.quantize(x, ws)
-        t = time_op_flushed(lambda: nv.nvfp4_quantize(x, q, sf, gs, ws), 10 if T > 2048 else 30, flush)
+        x0 = torch.from_numpy(workloads.quantize_input(T).view(np.int16)).cuda()
+        q, sf, gs = nv.quantize(x0, ws)
+        t, how = time_op(lambda i: x0 if i == 0 else x0.clone(), lambda x: nv.nvfp4_quantize(x, q, sf, gs, ws),
+                         T * HIDDEN * 2, flush, 10 if T > 2048 else 30)
         b = quantize_bytes(T, HIDDEN)
-        sweep[f"T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3))
-        del x, q, sf, gs
+        sweep[f"T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3), l2=how)
+        del x0, q, sf, gs
+        torch.cuda.empty_cache()
     hh = torch.from_numpy(workloads.swiglu_interleaved(2048).view(np.int16)).cuda()
     q, sf, gs = nv.deinterleave_quantize(hh, GRAN, ws)
-    t = time_op_flushed(lambda: nv.nvfp4_deinterleave_quantize(hh, GRAN, q, sf, gs, ws), 30, flush)
+    t, how = time_op(lambda i: hh if i == 0 else hh.clone(),
+                     lambda h: nv.nvfp4_deinterleave_quantize(h, GRAN, q, sf, gs, ws), hh.numel() * 2, flush)
     b = quantize_bytes(2048, 2 * INTER)
     sweep["deinterleave_T2048_g8"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1),
-                                          hbm_frac=round(b / t / hbm, 3))
+                                          hbm_frac=round(b / t / hbm, 3), l2=how)
     del hh, q, sf, gs
     # NEXT-2: RMSNorm fused into the quantize (the norm output never reaches HBM)
     rng = np.random.default_rng(7)
     wn = torch.from_numpy(workloads.bf16_bits((1.0 + 0.1 * rng.standard_normal(HIDDEN)).astype(np.float32))
                           .view(np.int16)).cuda()
     for T in (32, 2048):
-        x = torch.from_numpy(workloads.quantize_input(T).view(np.int16)).cuda()
-        q, sf, gs = nv.rmsnorm_quantize(x, wn, 1e-6, ws)
-        t = time_op_flushed(lambda: nv.nvfp4_rmsnorm_quantize(x, wn, 1e-6, q, sf, gs, ws), 30, flush)
+        x0 = torch.from_numpy(workloads.quantize_input(T).view(np.int16)).cuda()
+        q, sf, gs = nv.rmsnorm_quantize(x0, wn, 1e-6, ws)
+        t, how = time_op(lambda i: x0 if i == 0 else x0.clone(),
+                         lambda x: nv.nvfp4_rmsnorm_quantize(x, wn, 1e-6, q, sf, gs, ws), T * HIDDEN * 2, flush)
         b = quantize_bytes(T, HIDDEN) + HIDDEN * 2
-        sweep[f"rmsnorm_T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3))
-        del x, q, sf, gs
+        sweep[f"rmsnorm_T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3),
+                                      l2=how)
+        del x0, q, sf, gs
+    torch.cuda.empty_cache()
     out["quantize"] = sweep
     # router prefill T = 8192 (Student-t activations with outliers)
     d = workloads.router_prefill()
@@ -432,14 +501,19 @@ def secondary(nv, ws, pk, flush):
     idx = torch.empty(M, TOPK, dtype=torch.int32, device="cuda")
     sc = torch.empty(M, TOPK, dtype=torch.float32, device="cuda")
     wt = torch.empty(M, TOPK, dtype=torch.float32, device="cuda")
-    tq = time_op_flushed(lambda: nv.nvfp4_quantize(x, qa, sfa, gsa, ws), 10, flush)
-    tg = time_op_flushed(lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 1, bias, TOPK, idx, sc, wt,
-                                                   None, ws), 10, flush)
+    tq, how_q = time_op(lambda i: x if i == 0 else x.clone(), lambda xx: nv.nvfp4_quantize(xx, qa, sfa, gsa, ws),
+                        x.numel() * 2, flush, 10)
+    nv.nvfp4_quantize(x, qa, sfa, gsa, ws)
+    tg, how_g = time_op(lambda i: (qa, sfa) if i == 0 else (qa.clone(), sfa.clone()),
+                        lambda a: nv.nvfp4_gemm_topk(a[0], a[1], gsa, qb, sfb, gsb, 1, bias, TOPK, idx, sc, wt,
+                                                     None, ws),
+                        qa.numel() + sfa.numel(), flush, 10)
     fl, by = gemm_flops(M, EXPERTS, HIDDEN), gemm_bytes(M, EXPERTS, HIDDEN, TOPK)
     out["router_prefill_T8192"] = dict(
         quantize_us=round(tq * 1e6, 2), gemm_topk_us=round(tg * 1e6, 2),
         gemm_tflops=round(fl / tg / 1e12, 1), fp4_tensor_frac=round(fl / tg / fp4_peak, 3),
-        gemm_hbm_frac=round(by / tg / hbm, 3), rows_per_s=round(M / (tq + tg), 1))
+        gemm_hbm_frac=round(by / tg / hbm, 3), rows_per_s=round(M / (tq + tg), 1), l2_quantize=how_q, l2_gemm=how_g)
+    torch.cuda.empty_cache()
     del x, w, qa, sfa, qb, sfb, idx, sc, wt
     # indexer-shaped scoring
     d = workloads.indexer()
@@ -448,22 +522,25 @@ def secondary(nv, ws, pk, flush):
     M, N, K, k = 64, workloads.INDEXER_KEYS, workloads.INDEXER_DIM, workloads.INDEXER_TOPK
     idx = torch.empty(M, k, dtype=torch.int32, device="cuda")
     sc = torch.empty(M, k, dtype=torch.float32, device="cuda")
-    ti = time_op_flushed(lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, 0, None, k, idx, sc, None,
-                                                   None, ws), 30, flush)
+    keys = lambda i: (qb, sfb) if i == 0 else (qb.clone(), sfb.clone())  # the keys stream from HBM per call
+    ti, how = time_op(keys, lambda kk: nv.nvfp4_gemm_topk(qa, sfa, gsa, kk[0], kk[1], gsb, 0, None, k, idx, sc, None,
+                                                         None, ws), qb.numel() + sfb.numel(), flush)
     by = gemm_bytes(M, N, K, k, bias=False) - M * k * 4
     out["indexer_M64_N2048_k512"] = dict(us=round(ti * 1e6, 2), hbm_frac=round(by / ti / hbm, 4),
-                                         rows_per_s=round(M / ti, 1))
+                                         rows_per_s=round(M / ti, 1), l2=how)
     # NEXT-1: the indexer's weighted ReLU head sum fused in (one token, 64 heads x 128 dims)
     hw = torch.from_numpy((np.random.default_rng(64).standard_normal((1, 64)) / 8).astype(np.float32)).cuda()
     qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
     qb, sfb, gsb = nv.quantize(torch.from_numpy(d["w"].view(np.int16)).cuda(), ws)
     idx1 = torch.empty(1, k, dtype=torch.int32, device="cuda")
     sc1 = torch.empty(1, k, dtype=torch.float32, device="cuda")
-    th = time_op_flushed(lambda: nv.nvfp4_indexer_topk(qa, sfa, gsa, qb, sfb, gsb, 64, hw, k, idx1, sc1, None, ws),
-                         30, flush)
+    th, how = time_op(lambda i: (qb, sfb) if i == 0 else (qb.clone(), sfb.clone()),
+                      lambda kk: nv.nvfp4_indexer_topk(qa, sfa, gsa, kk[0], kk[1], gsb, 64, hw, k, idx1, sc1, None, ws),
+                      qb.numel() + sfb.numel(), flush)
     by = gemm_bytes(64, N, K, k, bias=False) - 64 * k * 12 + k * 8 + 64 * 4
     out["indexer_heads64_T1_N2048_k512"] = dict(us=round(th * 1e6, 2), hbm_frac=round(by / th / hbm, 4),
-                                                tokens_per_s=round(1 / th, 1))
+                                                tokens_per_s=round(1 / th, 1), l2=how)
+    torch.cuda.empty_cache()
     # router variant: 384 experts, top-6, normalised gating weights (decode, T = 32)
     rng = np.random.default_rng(384)
     E, kv = 384, 6
@@ -477,11 +554,13 @@ def secondary(nv, ws, pk, flush):
     idx = torch.empty(32, kv, dtype=torch.int32, device="cuda")
     sc = torch.empty(32, kv, dtype=torch.float32, device="cuda")
     wt = torch.empty(32, kv, dtype=torch.float32, device="cuda")
-    tv = time_op_flushed(lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, nv.EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM,
-                                                   bv, kv, idx, sc, wt, None, ws), 30, flush)
+    tv, how = time_op(lambda i: (qb, sfb) if i == 0 else (qb.clone(), sfb.clone()),
+                      lambda w_: nv.nvfp4_gemm_topk(qa, sfa, gsa, w_[0], w_[1], gsb, nv.EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM,
+                                                    bv, kv, idx, sc, wt, None, ws),
+                      qb.numel() + sfb.numel(), flush)
     by = gemm_bytes(32, E, HIDDEN, kv)
     out["router_E384_k6_norm_decode_T32"] = dict(us=round(tv * 1e6, 2), hbm_frac=round(by / tv / hbm, 4),
-                                                 rows_per_s=round(32 / tv, 1))
+                                                 rows_per_s=round(32 / tv, 1), l2=how)
     # NEXT-4: grouped NVFP4 GEMM + SwiGLU, MoE first projection (256 experts,
     # I = 2048, granularity 8, limit 10): decode (32 tokens x top-8) and
     # prefill (8192 tokens x top-8)
