@@ -201,3 +201,23 @@ def test_decode_shape_sampled(nv, ws):
         h, _ = oracle.grouped_swiglu(qa[lo:hi], sfa[lo:hi], gsa, qb[w], sfb[w], gsb[e:e + 1],
                                      np.array([0, hi - lo], np.int32), I, 8, 10.0)
         assert_swiglu(got[lo:hi], h, f"decode group {e}")
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_single_expert_ragged_rows(nv, ws, layout):
+    # one expert (the shared-expert case of the pages: num_groups = 1), 45 rows
+    # (one partial tile, not a multiple of the 32-row A boxes), K = 1024
+    case = make_case(45, [45], 256, 1024, seed=90)
+    check(nv, ws, case, 256, 8, 10.0, layout, f"single expert layout {layout}", ld_pad=8)
+
+
+def test_leading_empty_group_and_offset_start(nv, ws):
+    # the first group starts past row 0 (rows 0..9 belong to no group) and a
+    # group of exactly 128 rows sits between two empty ones
+    qa, sfa, gsa, qb, sfb, gsb, _ = make_case(300, [0, 0, 0, 0], 128, 256, seed=91)
+    offs = np.array([10, 10, 138, 138, 250], np.int32)
+    case = (qa, sfa, gsa, qb, sfb, gsb, offs)
+    got = run(nv, ws, case, 128, 4, 10.0, 0)
+    h, _ = oracle.grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offs, 128, 4, 10.0)
+    assert_swiglu(got[10:250], h[10:250], "offset groups")
+    assert np.all(got[:10] == 0xC0E0) and np.all(got[250:] == 0xC0E0)
