@@ -190,10 +190,16 @@ class RouterSets:
         rng = np.random.default_rng(seed)
         dev = "cuda"
         T = tokens
-        self.x = [torch.from_numpy(workloads.bf16_bits(rng.standard_normal((T, HIDDEN), np.float32))
-                                   .view(np.int16)).to(dev) for _ in range(n_sets)]
-        self.h = [torch.from_numpy(workloads.bf16_bits(rng.standard_normal((T, 2 * INTER), np.float32))
-                                   .view(np.int16)).to(dev) for _ in range(n_sets)]
+        # Each set's inputs sit in one arena ([x | h], bf16) and its outputs in
+        # another, so the end-to-end run moves one buffer each way per step.
+        self.xin = [torch.empty(T * HIDDEN + T * 2 * INTER, dtype=torch.int16, device=dev) for _ in range(n_sets)]
+        self.x = [a[:T * HIDDEN].view(T, HIDDEN) for a in self.xin]
+        self.h = [a[T * HIDDEN:].view(T, 2 * INTER) for a in self.xin]
+        for i in range(n_sets):
+            self.x[i].copy_(torch.from_numpy(workloads.bf16_bits(rng.standard_normal((T, HIDDEN), np.float32))
+                                             .view(np.int16)))
+            self.h[i].copy_(torch.from_numpy(workloads.bf16_bits(rng.standard_normal((T, 2 * INTER), np.float32))
+                                             .view(np.int16)))
         self.bias = [torch.from_numpy((rng.standard_normal(EXPERTS) * 0.01).astype(np.float32)).to(dev)
                      for _ in range(n_sets)]
         # gate weights: drawn as bf16 N(0, 0.02) and quantized once by the library (static per layer)
@@ -207,9 +213,17 @@ class RouterSets:
             self.gsb.append(gs)
         e = lambda *s, dt=torch.uint8: [torch.empty(*s, dtype=dt, device=dev) for _ in range(n_sets)]
         self.qa, self.sfa, self.gsa = e(T, HIDDEN // 2), e(T, HIDDEN // 16), e(1, dt=torch.float32)
-        self.idx, self.score, self.weight = e(T, TOPK, dt=torch.int32), e(T, TOPK, dt=torch.float32), \
-            e(T, TOPK, dt=torch.float32)
-        self.qh, self.sfh, self.gsh = e(T, INTER), e(T, INTER // 8), e(1, dt=torch.float32)
+        # output arena: idx | score | weight | qh | sfh | gsh (16-byte aligned pieces)
+        sizes = [T * TOPK * 4, T * TOPK * 4, T * TOPK * 4, T * INTER, T * INTER // 8, 4]
+        offs = np.concatenate([[0], np.cumsum([(z + 15) // 16 * 16 for z in sizes])])
+        self.out = [torch.empty(int(offs[-1]), dtype=torch.uint8, device=dev) for _ in range(n_sets)]
+        piece = lambda a, j, dt, shape: a[int(offs[j]):int(offs[j]) + sizes[j]].view(dt).view(*shape)
+        self.idx = [piece(a, 0, torch.int32, (T, TOPK)) for a in self.out]
+        self.score = [piece(a, 1, torch.float32, (T, TOPK)) for a in self.out]
+        self.weight = [piece(a, 2, torch.float32, (T, TOPK)) for a in self.out]
+        self.qh = [piece(a, 3, torch.uint8, (T, INTER)) for a in self.out]
+        self.sfh = [piece(a, 4, torch.uint8, (T, INTER // 8)) for a in self.out]
+        self.gsh = [piece(a, 5, torch.float32, (1,)) for a in self.out]
         # The SwiGLU-output quantize does not depend on the router: it runs on a
         # second stream (with its own workspace) beside quantize -> GEMM.
         self.side = torch.cuda.Stream()
@@ -629,41 +643,59 @@ def run_gpu(args, rank, world, local):
                     algorithmic_bytes=op_bytes[dominant], launch_us=round(op_times[dominant] * 1e6, 3),
                     peak_source=pk["source"])
 
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
-    e2e_sets = n_sets
-    hx = [torch.empty(T, HIDDEN, dtype=torch.int16, pin_memory=True) for _ in range(e2e_sets)]
-    hh = [torch.empty(T, 2 * INTER, dtype=torch.int16, pin_memory=True) for _ in range(e2e_sets)]
-    for i in range(e2e_sets):
-        hx[i].copy_(sets.x[i].cpu())
-        hh[i].copy_(sets.h[i].cpu())
-    o_idx = [torch.empty(T, TOPK, dtype=torch.int32, pin_memory=True) for _ in range(e2e_sets)]
-    o_sc = [torch.empty(T, TOPK, dtype=torch.float32, pin_memory=True) for _ in range(e2e_sets)]
-    o_wt = [torch.empty(T, TOPK, dtype=torch.float32, pin_memory=True) for _ in range(e2e_sets)]
-    o_qh = [torch.empty(T, INTER, dtype=torch.uint8, pin_memory=True) for _ in range(e2e_sets)]
-    o_sfh = [torch.empty(T, INTER // 8, dtype=torch.uint8, pin_memory=True) for _ in range(e2e_sets)]
-    o_gsh = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(e2e_sets)]
+    # End to end through the public API with host buffers (pinned), copies
+    # inside the timed region: every step copies its own inputs in (one
+    # arena, [x | h]) and its results out (one arena: router top-k and the
+    # SwiGLU-output codes, scales and global scale).  The copies run on
+    # their own streams, so step i + 1's inputs travel while step i computes
+    # and step i's results travel while step i + 1 computes; the timed region
+    # ends after the last step's results are on the host.
+    hin = [torch.empty(a.numel(), dtype=torch.int16, pin_memory=True) for a in sets.xin]
+    hout = [torch.empty(a.numel(), dtype=torch.uint8, pin_memory=True) for a in sets.out]
+    for i in range(n_sets):
+        hin[i].copy_(sets.xin[i].cpu())
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step(i):
-        sets.x[i].copy_(hx[i], non_blocking=True)
-        sets.h[i].copy_(hh[i], non_blocking=True)
-        sets.step(nv, ws, i)
-        o_idx[i].copy_(sets.idx[i], non_blocking=True)
-        o_sc[i].copy_(sets.score[i], non_blocking=True)
-        o_wt[i].copy_(sets.weight[i], non_blocking=True)
-        o_qh[i].copy_(sets.qh[i], non_blocking=True)
-        o_sfh[i].copy_(sets.sfh[i], non_blocking=True)
-        o_gsh[i].copy_(sets.gsh[i], non_blocking=True)
+    def e2e_steps(indices):
+        main = torch.cuda.current_stream()
+        h2d_s.wait_stream(main)
+        d2h_s.wait_stream(main)
+        for i in indices:
+            with torch.cuda.stream(h2d_s):
+                sets.xin[i].copy_(hin[i], non_blocking=True)
+            main.wait_stream(h2d_s)
+            sets.step(nv, ws, i)
+            d2h_s.wait_stream(main)
+            with torch.cuda.stream(d2h_s):
+                hout[i].copy_(sets.out[i], non_blocking=True)
+        main.wait_stream(h2d_s)
+        main.wait_stream(d2h_s)
 
-    ge, se = capture_chunks(e2e_step, e2e_sets, chunk)
-    replay_steps(ge, se, chunk, min(args.warmup, e2e_sets))
+    # eager warm-up, then graphs of chunk-sized runs and of single steps
+    e2e_steps(range(n_sets))
+    torch.cuda.synchronize()
+    ge, se = [], []
+    for c0 in range(0, n_sets, chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_steps(range(c0, min(c0 + chunk, n_sets)))
+        ge.append(g)
+    for i in range(chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_steps([i])
+        se.append(g)
+    replay_steps(ge, se, chunk, min(args.warmup, n_sets))
     e2e_secs, _, _ = time_graphs(ge, se, chunk, args.steps, world)
     e2e_secs = reduce_max(e2e_secs, world)
-    h2d = T * HIDDEN * 2 + T * 2 * INTER * 2
-    d2h = T * TOPK * 12 + T * INTER + T * INTER // 8 + 4
+    h2d = sets.xin[0].numel() * 2
+    d2h = sets.out[0].numel()
     e2e = dict(value=round(throughput(T, args.steps, e2e_secs, world), 1), unit="rows/s",
                h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h)
-    # check that the last step's outputs match the device results (copies really ran)
+    # the copies really ran: every set's host results equal its device results
     torch.cuda.synchronize()
+    for i in range(n_sets):
+        assert torch.equal(hout[i], sets.out[i].cpu()), "end-to-end results differ from the device results"
 
     status = nv.read_device_status(ws)
     detail = None
