@@ -76,3 +76,14 @@ def test_algorithmic_bytes():
     assert bench.quantize_bytes(1, 7168) == 14336 + 3584 + 448 + 4
     # router decode T=32: A and B codes + scales, gs, bias, top-8 outputs
     assert bench.gemm_bytes(32, 256, 7168, 8) == (32 + 256) * 4032 + 8 + 1024 + 32 * 8 * 12
+
+
+def test_rotating_sets_exceed_twice_l2():
+    # a rotation reads more than 2.2x L2 per pass, with at least two copies;
+    # inputs too small for a bounded number of copies fall back to a flush
+    for b in (1 << 20, 29 * (1 << 20), 235 * (1 << 20), 150 * 1024):
+        n = bench.rotating_sets(b)
+        assert n is not None and n >= 2 and n * b >= bench.ROTATE_BYTES
+        assert (n - 1) * b < bench.ROTATE_BYTES or n == 2
+    assert bench.rotating_sets(14 * 1024) is None  # 14 KB would need ~20k copies
+    assert bench.rotating_sets(bench.ROTATE_BYTES + 1) == 2
