@@ -248,15 +248,54 @@ class RouterSets:
     def op_deinterleave(self, nv, ws, i):
         nv.nvfp4_deinterleave_quantize(self.h[i], GRAN, self.qh[i], self.sfh[i], self.gsh[i], ws)
 
-    def step(self, nv, ws, i):
+    def steps(self, nv, ws, indices, ready=None, done=None):
+        """Steps on sets `indices`: quantize -> GEMM + top-k on the current
+        stream, the SwiGLU-output quantize of each step on the side stream
+        (forked once, joined once, so consecutive router kernels stay adjacent
+        on their stream).  ready(i) may return an event that step i's inputs
+        wait for, and done(i, main, side) is called once step i's work is
+        enqueued on both streams (end-to-end copies)."""
         import torch
         main = torch.cuda.current_stream()
-        self.side.wait_stream(main)  # fork after this step's inputs are in place
-        with torch.cuda.stream(self.side):
-            self.op_deinterleave(nv, self.ws2, i)
-        self.op_quantize(nv, ws, i)
-        self.op_gemm(nv, ws, i)
-        main.wait_stream(self.side)  # join
+        self.side.wait_stream(main)
+        for i in indices:
+            ev = ready(i) if ready is not None else None
+            with torch.cuda.stream(self.side):
+                if ev is not None:
+                    self.side.wait_event(ev)
+                self.op_deinterleave(nv, self.ws2, i)
+            if ev is not None:
+                main.wait_event(ev)
+            self.op_quantize(nv, ws, i)
+            self.op_gemm(nv, ws, i)
+            if done is not None:
+                done(i, main, self.side)
+        main.wait_stream(self.side)
+
+    def step(self, nv, ws, i):
+        self.steps(nv, ws, [i])
+
+
+def capture_runs(run, n_sets, chunk):
+    """CUDA graphs of run(indices) for chunk-sized runs of consecutive sets,
+    and of single sets (for a remainder)."""
+    import torch
+    run(range(n_sets))  # eager warm-up of every set (kernel attributes, tensor maps)
+    torch.cuda.synchronize()
+    graphs = []
+    for c0 in range(0, n_sets, chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run(range(c0, min(c0 + chunk, n_sets)))
+        graphs.append(g)
+    singles = []
+    for i in range(chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run([i])
+        singles.append(g)
+    torch.cuda.synchronize()
+    return graphs, singles
 
 
 def capture_chunks(fn, n_sets, chunk):
@@ -613,7 +652,7 @@ def run_gpu(args, rank, world, local):
     kernels_per_step = nv.kernel_launches() - before
     torch.cuda.synchronize()
 
-    graphs, singles = capture_chunks(lambda i: sets.step(nv, ws, i), n_sets, chunk)
+    graphs, singles = capture_runs(lambda idx: sets.steps(nv, ws, idx), n_sets, chunk)
     with ClockSampler(local) as clk:
         replay_steps(graphs, singles, chunk, args.warmup)
         secs, t0, t1 = time_graphs(graphs, singles, chunk, args.steps, world)
@@ -659,32 +698,27 @@ def run_gpu(args, rank, world, local):
     def e2e_steps(indices):
         main = torch.cuda.current_stream()
         h2d_s.wait_stream(main)
-        d2h_s.wait_stream(main)
-        for i in indices:
+        landed = {}
+        for i in indices:  # every step's inputs, in order, on the copy-in stream
             with torch.cuda.stream(h2d_s):
                 sets.xin[i].copy_(hin[i], non_blocking=True)
-            main.wait_stream(h2d_s)
-            sets.step(nv, ws, i)
-            d2h_s.wait_stream(main)
+                landed[i] = torch.cuda.Event()
+                landed[i].record(h2d_s)
+        d2h_s.wait_stream(main)
+
+        def results_out(i, m, side):  # step i's results leave once both its streams are done with it
+            for st in (m, side):
+                ev = torch.cuda.Event()
+                ev.record(st)
+                d2h_s.wait_event(ev)
             with torch.cuda.stream(d2h_s):
                 hout[i].copy_(sets.out[i], non_blocking=True)
+
+        sets.steps(nv, ws, indices, ready=lambda i: landed[i], done=results_out)
         main.wait_stream(h2d_s)
         main.wait_stream(d2h_s)
 
-    # eager warm-up, then graphs of chunk-sized runs and of single steps
-    e2e_steps(range(n_sets))
-    torch.cuda.synchronize()
-    ge, se = [], []
-    for c0 in range(0, n_sets, chunk):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            e2e_steps(range(c0, min(c0 + chunk, n_sets)))
-        ge.append(g)
-    for i in range(chunk):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            e2e_steps([i])
-        se.append(g)
+    ge, se = capture_runs(e2e_steps, n_sets, chunk)
     replay_steps(ge, se, chunk, min(args.warmup, n_sets))
     e2e_secs, _, _ = time_graphs(ge, se, chunk, args.steps, world)
     e2e_secs = reduce_max(e2e_secs, world)

@@ -856,6 +856,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int mma_n = min(BN, (ncols + 15) & ~15);
   constexpr int kUnits = 1 + L::kAtomsB;  // scale atoms per stage: SFA + SFB's
 
+  // The next kernel on the stream may set up while this one runs (it waits
+  // for our completion before touching memory); the tensor maps are kernel
+  // parameters, so their descriptors can be fetched before the previous
+  // kernel has finished.
+  pdl_launch_dependents();
+  if (threadIdx.x == 32) {
+    prefetch_tensormap(&tma_a);
+    prefetch_tensormap(&tma_b);
+    if (p.tma_sf) {
+      prefetch_tensormap(&tma_sfa);
+      prefetch_tensormap(&tma_sfb);
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), p.tma_sf ? 1 : 1 + 32);  // + one cp.async arrival per producer lane

@@ -260,6 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* glo = tstart + (p.E + 1);                              // [E] clamped first row
   int* ghi = glo + p.E;                                       // [E] clamped end row
 
+  if (threadIdx.x == 32) {  // descriptor fetches overlap the set-up
+    prefetch_tensormap(&tma_a);
+    prefetch_tensormap(&tma_b);
+    prefetch_tensormap(&tma_sfa);
+    prefetch_tensormap(&tma_sfb);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
