@@ -456,12 +456,17 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
       cta_max = __uint_as_float(m << 16);
     }
     ptx::cluster_sync();
-    if (threadIdx.x == 0) {
-      float mx = 0.0f;
-      for (uint32_t r = 0; r < gridDim.x; ++r) mx = fmaxf(mx, ptx::ld_cluster_f32(ptx::mapa_shared(ptx::smem_addr(&cta_max), r)));
-      const float gs = __fdiv_rn(fmaxf(mx, kAmaxFloor), kGsDivisor);
-      gs_sh = gs;
-      if (blockIdx.x == 0) gs_out[0] = gs;
+    if (threadIdx.x < 32) {
+      // lane r reads CTA r's maximum (the reads overlap), then a warp max
+      const uint32_t r = threadIdx.x;
+      float mx = r < gridDim.x ? ptx::ld_cluster_f32(ptx::mapa_shared(ptx::smem_addr(&cta_max), r)) : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      if (threadIdx.x == 0) {
+        const float gs = __fdiv_rn(fmaxf(mx, kAmaxFloor), kGsDivisor);
+        gs_sh = gs;
+        if (blockIdx.x == 0) gs_out[0] = gs;
+      }
     }
     ptx::cluster_sync();  // no CTA leaves while a peer may still read its maximum
   } else if (threadIdx.x == 0) {
@@ -808,13 +813,17 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
       cta_max = __uint_as_float(m << 16);
     }
     ptx::cluster_sync();
-    if (threadIdx.x == 0) {
-      float mx = 0.0f;
-      for (uint32_t r = 0; r < gridDim.x; ++r)
-        mx = fmaxf(mx, ptx::ld_cluster_f32(ptx::mapa_shared(ptx::smem_addr(&cta_max), r)));
-      const float gs = __fdiv_rn(fmaxf(mx, kAmaxFloor), kGsDivisor);
-      gs_sh = gs;
-      if (blockIdx.x == 0) gs_out[0] = gs;
+    if (threadIdx.x < 32) {
+      // lane r reads CTA r's maximum (the reads overlap), then a warp max
+      const uint32_t r = threadIdx.x;
+      float mx = r < gridDim.x ? ptx::ld_cluster_f32(ptx::mapa_shared(ptx::smem_addr(&cta_max), r)) : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      if (threadIdx.x == 0) {
+        const float gs = __fdiv_rn(fmaxf(mx, kAmaxFloor), kGsDivisor);
+        gs_sh = gs;
+        if (blockIdx.x == 0) gs_out[0] = gs;
+      }
     }
     ptx::cluster_sync();  // no CTA leaves while a peer may still read its maximum
   } else if (threadIdx.x == 0) {
