@@ -125,3 +125,37 @@ def test_indexer_topk_validation(L):
     assert call(k=0) == 1
     assert call(N=5000) == 2              # keys on chip: N <= 4096
     assert call(K=100) == 2               # K a multiple of 64
+
+
+def test_grouped_swiglu_validation(L):
+    P, f = _p, ctypes.c_float
+
+    def call(qa=FAKE, sfa=FAKE, offs=FAKE, out=FAKE, M=256, E=8, inter=2048, K=7168, g=8, limit=10.0,
+             layout=0, ld=2048, ws=FAKE, ws_bytes=256, gsb=FAKE):
+        return L.nvfp4_grouped_swiglu_gemm(P(qa) if qa else None, P(sfa) if sfa else None, P(FAKE), P(FAKE),
+                                           P(FAKE), P(gsb) if gsb else None, P(offs) if offs else None, M, E,
+                                           inter, K, g, f(limit), layout, P(out) if out else None, ld,
+                                           P(ws) if ws else None, ws_bytes, None)
+
+    assert call(offs=0) == 1                      # device offsets required when M > 0
+    assert call(out=0) == 1
+    assert call(gsb=0) == 1
+    assert call(E=0) == 1
+    assert call(E=1025) == 2                      # at most 1024 groups
+    assert call(layout=2) == 1
+    assert call(limit=0.0) == 1                   # limit > 0 (infinity allowed)
+    assert call(limit=float("nan")) == 1
+    assert call(g=3) == 2                         # granularity 1, 2, 4, 8, 16
+    assert call(inter=200) == 2                   # I a multiple of 128
+    assert call(K=7168 + 64) == 2                 # K a multiple of 256
+    assert call(ld=2040) == 2                     # ld >= I and a multiple of 8
+    assert call(layout=1, ld=2048) == 2           # layout 1 rows hold 2I values
+    assert call(ld=2052) == 2
+    assert call(qa=FAKE + 8) == 2                 # codes 16-byte aligned
+    assert call(sfa=FAKE + 4) == 2                # scales 16-byte aligned (TMA boxes)
+    assert call(out=FAKE + 2) == 2                # bf16 rows stored 16 bytes at a time
+    assert call(offs=FAKE + 2) == 2
+    assert call(ws=0) == 3
+    assert call(ws_bytes=64) == 3
+    # M == 0 launches nothing and accepts NULL activations, offsets and output
+    assert call(M=0, qa=0, sfa=0, offs=0, out=0) == 0
