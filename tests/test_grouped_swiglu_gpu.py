@@ -221,3 +221,34 @@ def test_leading_empty_group_and_offset_start(nv, ws):
     h, _ = oracle.grouped_swiglu(qa, sfa, gsa, qb, sfb, gsb, offs, 128, 4, 10.0)
     assert_swiglu(got[10:250], h[10:250], "offset groups")
     assert np.all(got[:10] == 0xC0E0) and np.all(got[250:] == 0xC0E0)
+
+
+def test_prefill_like_full_tiles_sampled(nv, ws):
+    # 1024 tokens x top-8 over 32 experts (about 256 rows per group: full
+    # 128-row tiles, several per group, every expert used), hidden 7168,
+    # I = 2048: the K ring runs 28 stages per item over many items per CTA.
+    # Rows at each sampled group's start, its first tile boundary (127, 128)
+    # and its end are checked against the oracle.
+    T, E, k, I, K = 1024, 32, 8, workloads.MOE_INTER, workloads.HIDDEN
+    tok, offs = workloads.moe_routing(T, E, k, seed=95)
+    x = workloads.quantize_input(T, seed=96)
+    qa, sfa, gsa = oracle.quantize(x[tok])
+    w_one = workloads.moe_l1_weights(4, I, K, seed=97)
+    qbs, sfbs, gsbs = quantize_experts(w_one, 4)
+    pick = np.arange(E) % 4
+    rows_per = 2 * I
+    qb = np.concatenate([qbs[p * rows_per:(p + 1) * rows_per] for p in pick])
+    sfb = np.concatenate([sfbs[p * rows_per:(p + 1) * rows_per] for p in pick])
+    gsb = gsbs[pick]
+    case = (qa, sfa, gsa, qb, sfb, gsb, offs)
+    got = run(nv, ws, case, I, 8, 10.0, 0)
+    sizes = offs[1:] - offs[:-1]
+    assert sizes.min() > 129, sizes.min()
+    for e in (0, 13, 31):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        rows = [lo, lo + 1, lo + 127, lo + 128, hi - 2, hi - 1]
+        w = slice(e * rows_per, (e + 1) * rows_per)
+        for r in rows:
+            h, _ = oracle.grouped_swiglu(qa[r:r + 1], sfa[r:r + 1], gsa, qb[w], sfb[w], gsb[e:e + 1],
+                                         np.array([0, 1], np.int32), I, 8, 10.0)
+            assert_swiglu(got[r:r + 1], h, f"group {e} row {r - lo}")
