@@ -20,8 +20,8 @@
 // Work split.  A work item is one 128-row tile of one group times one
 // 256-row slice of that group's weights (128 gate and 128 up columns).  The
 // group offsets live on the device (the router writes them), so the CTAs
-// derive the item list themselves: each stages the offsets in shared memory
-// and scans them into per-group tile starts.  Items are dealt round-robin
+// derive the item list themselves: one warp of each scans the offsets into
+// per-group tile starts in shared memory.  Items are dealt round-robin
 // with the weight slice varying fastest, so the CTAs that work at the same
 // time share each A tile through L2 and the row tiles of one group share its
 // weight slices.
@@ -29,21 +29,24 @@
 // Per CTA, 6 warps:
 //   warp 0     producer: TMA loads of the A and B code tiles (128-byte rows,
 //              128-byte swizzle) and the row-major E4M3 scale boxes into a
-//              3-stage ring that runs on across work items.  The scale boxes
-//              complete on a barrier of their own, so their rearrangement
-//              and copy into TMEM overlap the landing of the code tiles; A
-//              comes in 32-row boxes, only those holding the item's rows.
+//              ring of 4 stages of 54 KB (3 when the group tables of more than
+//              ~830 groups need the room) that runs on across work items.
+//              The scale boxes complete on a barrier of their own, so their
+//              rearrangement and copy into TMEM overlap the landing of the
+//              code tiles; A comes in 32-row boxes, only those holding the
+//              item's rows.
 //   warp 1     MMA issuer (one thread): four 128 x 256 x 64 kind::mxf4nvf4
 //              block-scaled MMAs per stage into one TMEM accumulator; before
 //              the first MMA of an item it waits until the epilogue has read
 //              the previous item's accumulator.
-//   warps 2-5  lay each stage's scale tiles out for tcgen05.cp and copy them
-//              into TMEM (one MMA step of every 128-row scale atom each);
+//   warps 2-5  rearrange each stage's scale boxes in place into the layout
+//              tcgen05.cp reads (all four read, a named barrier, then each
+//              writes the chunk of its MMA step) and copy them into TMEM;
 //              after an item's last stage they are its epilogue: the thread
-//              owning TMEM lane r reads row r 32 columns at a time, scales by
-//              gsa * gsb[e], applies the clamp and SwiGLU in registers and
-//              stores bf16 straight to global memory (rows past the group's
-//              end are not stored).
+//              owning TMEM lane r reads row r 32 columns at a time (two
+//              chunks in flight), scales by gsa * gsb[e], applies the clamp
+//              and SwiGLU in registers and stores bf16 straight to global
+//              memory (rows past the group's end are not stored).
 //
 // Every wait is bounded (~1 s of SM clock): on expiry the kernel records
 // NVFP4_DEVICE_TIMEOUT in the workspace, stops the CTA's other warps, lets
