@@ -2,12 +2,18 @@
 """Benchmark of the NVFP4 router hot path on GB300.
 
 One step = one pass of the whole path over one decode batch of T tokens:
-  1. nvfp4_quantize               X [T, 7168] bf16 -> NVFP4 (amax + quantize kernels)
+  1. nvfp4_quantize               X [T, 7168] bf16 -> NVFP4 (one launch: a cluster
+                                  meets on the global maximum in shared memory)
   2. nvfp4_gemm_topk              gate GEMM vs 256 NVFP4 experts, sqrt(softplus) + bias, top-8
-  3. nvfp4_deinterleave_quantize  SwiGLU output [T, 2*2048] (granularity 8) -> NVFP4
-Five kernel launches per step.  Inputs rotate over enough independent sets
-(activations, weights, biases) that the working set is more than twice the
-L2 cache, so every step reads HBM.  Steps are replayed from CUDA graphs.
+  3. nvfp4_deinterleave_quantize  SwiGLU output [T, 2*2048] (granularity 8) -> NVFP4,
+                                  on a side stream beside 1-2
+Three kernel launches per step (the library counts its own launches; the
+JSON line's gpu_launches is that count).  Inputs rotate over enough
+independent sets (activations, weights, biases) that the working set is more
+than twice the L2 cache, so every step reads HBM.  Steps are replayed from
+CUDA graphs.  Detail lines time the other shapes of the pages (quantize
+sweep, RMSNorm producer, prefill router, indexer, router variant, grouped MoE
+projection).
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
 only reference this path has) on a bounded sample instead.
