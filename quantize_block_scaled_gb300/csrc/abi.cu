@@ -225,7 +225,8 @@ int nvfp4_grouped_swiglu_gemm(const uint8_t* qa, const uint8_t* sfa, const float
   if (gsa == nullptr || qb == nullptr || sfb == nullptr || gsb == nullptr) return NVFP4_ERR_INVALID;
   if (M != 0 && (qa == nullptr || sfa == nullptr || offsets == nullptr || out == nullptr))
     return NVFP4_ERR_INVALID;
-  if (M < 0 || M > kInt32Max || E < 1 || inter < 1 || K < 1 || K > kInt32Max) return NVFP4_ERR_INVALID;
+  if (M < 0 || M > kInt32Max || E < 1 || inter < 1 || inter > kInt32Max || K < 1 || K > kInt32Max)
+    return NVFP4_ERR_INVALID;
   if (E > 1024) return NVFP4_ERR_UNSUPPORTED;
   if (layout != 0 && layout != 1) return NVFP4_ERR_INVALID;
   if (!(limit > 0.0f)) return NVFP4_ERR_INVALID;  // also rejects NaN

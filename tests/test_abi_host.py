@@ -147,6 +147,7 @@ def test_grouped_swiglu_validation(L):
     assert call(limit=float("nan")) == 1
     assert call(g=3) == 2                         # granularity 1, 2, 4, 8, 16
     assert call(inter=200) == 2                   # I a multiple of 128
+    assert call(inter=1 << 62) == 1               # sizes are checked before any product of them
     assert call(K=7168 + 64) == 2                 # K a multiple of 256
     assert call(ld=2040) == 2                     # ld >= I and a multiple of 8
     assert call(layout=1, ld=2048) == 2           # layout 1 rows hold 2I values
