@@ -182,7 +182,7 @@ int nvfp4_indexer_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa, 
     return NVFP4_ERR_INVALID;
   if (tokens < 0 || N < 1 || K < 1 || N > kInt32Max || K > kInt32Max) return NVFP4_ERR_INVALID;
   if (heads != 32 && heads != 64 && heads != 128) return NVFP4_ERR_UNSUPPORTED;
-  if (tokens * heads > kInt32Max) return NVFP4_ERR_INVALID;
+  if (tokens > kInt32Max || tokens * heads > kInt32Max) return NVFP4_ERR_INVALID;
   if (k < 1 || k > 1024) return NVFP4_ERR_INVALID;
   if (K % 64 != 0 || N > 4096) return NVFP4_ERR_UNSUPPORTED;
   if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sfa, 4) || !aligned(sfb, 4) || !aligned(gsa, 4) ||

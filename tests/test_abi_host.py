@@ -125,6 +125,9 @@ def test_indexer_topk_validation(L):
     assert call(k=0) == 1
     assert call(N=5000) == 2              # keys on chip: N <= 4096
     assert call(K=100) == 2               # K a multiple of 64
+    too_many = L.nvfp4_indexer_topk(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1 << 60, 64, 2048, 128,
+                                    P(FAKE), 512, P(FAKE), P(FAKE), None, ws, 256, None)
+    assert too_many == 1                  # tokens bounded before tokens * heads
 
 
 def test_grouped_swiglu_validation(L):
