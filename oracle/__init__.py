@@ -68,6 +68,7 @@ def _load():
             "orc_topk": (None, [P, P, I64, I64, ctypes.c_int, P, P, P]),
             "orc_normalize_topk_weights": (None, [P, P, I64, ctypes.c_int]),
             "orc_rmsnorm": (None, [P, I64, I64, I64, P, F, P]),
+            "orc_rms_sum_of_squares": (None, [P, I64, I64, I64, P]),
             "orc_indexer_scores": (None, [P, P, F, P, P, F, I64, I64, I64, I64, P, P]),
             "orc_rmsnorm_quantize": (None, [P, I64, I64, I64, P, F, P, P, P]),
             "orc_gemm_topk_rows": (None, [P, P, F, P, P, F, I64, I64, ctypes.c_int, P,
@@ -221,6 +222,15 @@ def indexer_scores(qa, sfa, gsa, qb, sfb, gsb, heads: int, head_w: np.ndarray) -
     out = np.zeros((T, N), np.float32)
     _load().orc_indexer_scores(_ptr(qa), _ptr(sfa), float(gsa), _ptr(qb), _ptr(sfb), float(gsb), T, heads, N, K,
                                _ptr(w), _ptr(out))
+    return out
+
+
+def rms_sum_of_squares(x: np.ndarray) -> np.ndarray:
+    """Per row of bf16 bits: the exact sum of squares rounded once to FP32."""
+    x = _c(x, np.uint16)
+    rows, cols = x.shape
+    out = np.zeros(rows, np.float32)
+    _load().orc_rms_sum_of_squares(_ptr(x), rows, cols, cols, _ptr(out))
     return out
 
 

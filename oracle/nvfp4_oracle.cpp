@@ -206,39 +206,73 @@ uint16_t bf16_round(float f) {
   return static_cast<uint16_t>(rounded >> 16);
 }
 
+// Sum of the squares of one bf16 row, exactly, rounded once to FP32 (round
+// to nearest, ties to even; inf when the exact sum is past FP32's range).
+// The pages write the norm's denominator as an FP32 sum (or mean) of x^2
+// over the row (x_f32.pow(2).sum(dim=-1) in mhc.py, _project_and_rms;
+// pow(2).mean(dim=-1) in _dynamic_params) without an order, so the order-
+// free reading is taken: the FP32 value nearest the exact sum.
+//
+// Every finite bf16 value is M * 2^q with an integer M < 256 and
+// q = max(E, 1) - 134 (E the 8-bit exponent field), so every square is the
+// integer M^2 times 2^(2q), 2q >= -266: the exact sum is an integer S times
+// 2^-266, accumulated here in 32-bit limbs, then rounded to the FP32 grid.
+float exact_sum_of_squares(const uint16_t* xr, int64_t cols) {
+  constexpr int kLimbs = 20;  // 640 bits: 2^16 * 2^506 * 2^14 < 2^537
+  uint32_t acc[kLimbs] = {};
+  for (int64_t c = 0; c < cols; ++c) {
+    const uint32_t e = (xr[c] >> 7) & 0xFFu;
+    const uint64_t m = (xr[c] & 0x7Fu) | (e != 0 ? 0x80u : 0u);
+    const int shift = 2 * ((e != 0 ? static_cast<int>(e) : 1) - 134) + 266;  // 0 .. 506
+    // add m^2 << shift
+    uint64_t carry = 0;
+    const int limb = shift / 32, off = shift % 32;
+    const uint64_t part = (m * m) << off;  // < 2^48
+    for (int i = limb; i < kLimbs; ++i) {
+      uint64_t add = carry;
+      if (i == limb) add += part & 0xFFFFFFFFu;
+      if (i == limb + 1) add += part >> 32;
+      const uint64_t t = static_cast<uint64_t>(acc[i]) + add;
+      acc[i] = static_cast<uint32_t>(t);
+      carry = t >> 32;
+      if (carry == 0 && i > limb) break;
+    }
+  }
+  auto bit = [&](int i) { return (acc[i / 32] >> (i % 32)) & 1u; };
+  int top = kLimbs * 32 - 1;
+  while (top >= 0 && !bit(top)) --top;
+  if (top < 0) return 0.0f;
+  // Keep the bits from position p up: 24 significant bits, but no finer than
+  // FP32's smallest step 2^-149 (position 266 - 149 = 117).
+  const int p = std::max(top - 23, 117);
+  uint64_t keep = 0;
+  for (int i = top; i >= p; --i) keep = (keep << 1) | bit(i);
+  if (p > 0) {
+    const bool half = bit(p - 1) != 0;
+    bool below = false;
+    for (int i = p - 2; i >= 0 && !below; --i) below = bit(i) != 0;
+    if (half && (below || (keep & 1u))) ++keep;  // round to nearest, ties to even
+  }
+  // keep * 2^(p - 266) is on the FP32 grid (or past its largest value)
+  const double v = std::ldexp(static_cast<double>(keep), p - 266);
+  return v > static_cast<double>(std::numeric_limits<float>::max())
+             ? std::numeric_limits<float>::infinity()
+             : static_cast<float>(v);
+}
+
 // RMSNorm of each row to bf16, as the producer of the quantize input (page
 // "compare ... v-official-encoding-path": fused RMSNorm + NVFP4 quantize,
 // PERFORMANCE_AUDIT.md P4; the norm is input * inv_rms * weight[c]).  The
-// pages fix neither epsilon nor the summation order; the readings taken:
-//   sum of squares: each 16-element block accumulated in order with fused
-//     multiply-adds from 0; the block sums combined pairwise, level by level
-//     (entry j of the next level is p[2j] + p[2j+1], or p[2j] alone at an
-//     odd end) down to one value;
+// pages fix no epsilon; the readings taken:
+//   sum of squares: exact, rounded once to FP32 (exact_sum_of_squares);
 //   inv_rms = 1 / sqrt(sum / cols + eps), each step one FP32 operation;
 //   y = (x * inv_rms) * weight[c] in FP32, rounded to bf16 (the model's
 //     hidden-state type), which is what gets quantized.
 void orc_rmsnorm(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const uint16_t* weight,
                  float eps, uint16_t* out) {
-  const int64_t nb = cols / 16;
-  std::vector<float> level(static_cast<size_t>(nb));
   for (int64_t r = 0; r < rows; ++r) {
     const uint16_t* xr = x + r * ld;
-    for (int64_t b = 0; b < nb; ++b) {
-      float acc = 0.0f;
-      for (int i = 0; i < 16; ++i) {
-        const float v = bf16_value(xr[b * 16 + i]);
-        acc = std::fma(v, v, acc);
-      }
-      level[b] = acc;
-    }
-    int64_t n = nb;
-    while (n > 1) {
-      const int64_t half = (n + 1) / 2;
-      for (int64_t j = 0; j < half; ++j)
-        level[j] = (2 * j + 1 < n) ? level[2 * j] + level[2 * j + 1] : level[2 * j];
-      n = half;
-    }
-    const float sum = nb > 0 ? level[0] : 0.0f;
+    const float sum = exact_sum_of_squares(xr, cols);
     const float mean = sum / static_cast<float>(cols);
     const float inv_rms = 1.0f / std::sqrt(mean + eps);
     for (int64_t c = 0; c < cols; ++c) {
@@ -246,6 +280,11 @@ void orc_rmsnorm(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, cons
       out[r * cols + c] = bf16_round(y);
     }
   }
+}
+
+// The FP32 sum of squares of each row, as orc_rmsnorm takes it.
+void orc_rms_sum_of_squares(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* out) {
+  for (int64_t r = 0; r < rows; ++r) out[r] = exact_sum_of_squares(x + r * ld, cols);
 }
 
 // RMSNorm, then quantize the [rows, cols] bf16 result as a whole.

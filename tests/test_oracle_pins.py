@@ -384,6 +384,67 @@ def _bf16(vals):
     return bf16_bits(np.asarray(vals, np.float32))
 
 
+def _nearest_f32(frac):
+    """The float32 nearest a non-negative Fraction (ties to the even
+    significand), found by comparing the exact value with its float32
+    neighbours; inf beyond float32's range."""
+    from fractions import Fraction
+    big = Fraction(np.finfo(np.float32).max.item()) + Fraction(2) ** 103  # max + half its step
+    if frac >= big:
+        return np.float32(np.inf)
+    c = np.float32(float(frac))  # within one step of the answer
+    best = None
+    for cand in (np.nextafter(c, np.float32(0)), c, np.nextafter(c, np.float32(np.inf))):
+        if not np.isfinite(cand) or cand < 0:
+            continue
+        d = abs(Fraction(cand.item()) - frac)
+        key = (d, int(np.float32(cand).view(np.uint32)) & 1)  # tie: even significand bit
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return np.float32(best[1])
+
+
+def _exact_sum_sq(row_bits):
+    from fractions import Fraction
+    return sum((Fraction(v.item()) ** 2 for v in bf16_to_f32(row_bits).astype(np.float64)), Fraction(0))
+
+
+def test_rms_sum_of_squares_is_nearest_float_of_exact_sum():
+    # rows over a wide range of magnitudes, with bf16 subnormals, zeros and
+    # negative values; the reference is Python's exact rational arithmetic
+    rng = np.random.default_rng(33)
+    rows = [rng.standard_normal(300) * 2.0 ** rng.integers(-30, 30) for _ in range(6)]
+    rows.append(np.concatenate([rng.standard_normal(150) * 1e3, rng.standard_normal(150) * 1e-30]))
+    rows.append(np.concatenate([rng.standard_normal(10) * 2.0 ** -128, np.zeros(290)]))  # bf16 subnormals
+    rows.append(rng.standard_normal(300) * 2.0 ** -70)  # squares below FP32's normal range
+    x = bf16_bits(np.array(rows, np.float32))
+    got = oracle.rms_sum_of_squares(x)
+    for r in range(x.shape[0]):
+        want = _nearest_f32(_exact_sum_sq(x[r]))
+        assert got[r].view(np.uint32) == want.view(np.uint32), (r, got[r], want)
+
+
+def test_rms_sum_of_squares_ties_and_limits():
+    # 2^24 + 1 is halfway between 2^24 and 2^24 + 2: ties to even (2^24);
+    # any positive term below it breaks the tie upwards; 2^24 + 9 -> 2^24 + 8
+    cases = [([4096.0, 1.0], 2.0 ** 24), ([4096.0, 1.0, 2.0 ** -20], 2.0 ** 24 + 2),
+             ([4096.0, 3.0], 2.0 ** 24 + 8), ([2.0 ** 100], np.inf), ([2.0 ** -80], 0.0),
+             ([2.0 ** -70, 2.0 ** -70], 2.0 ** -139), ([], 0.0)]
+    for vals, want in cases:
+        x = _bf16([list(vals) + [0.0] * (16 - len(vals))])
+        assert oracle.rms_sum_of_squares(x)[0] == np.float32(want), (vals, want)
+
+
+def test_rms_sum_of_squares_is_order_free():
+    # the reading has no summation order: any permutation of a row gives the same FP32 sum
+    rng = np.random.default_rng(34)
+    x = bf16_bits((rng.standard_normal((4, 7168)) * 2.0 ** rng.integers(-20, 20, (4, 7168))).astype(np.float32))
+    s0 = oracle.rms_sum_of_squares(x)
+    for seed in range(3):
+        perm = np.random.default_rng(seed).permutation(7168)
+        assert np.array_equal(oracle.rms_sum_of_squares(x[:, perm]), s0)
+
+
 def test_rmsnorm_worked_row():
     # x = [3, 4, 0 x 14], weight 1, eps 0: sum 25, mean 25/16, rms 1.25,
     # y = [2.4, 3.2, 0 ...] -> bf16 2.40625, 3.203125 (round to nearest even)
