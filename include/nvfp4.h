@@ -75,8 +75,26 @@ typedef enum nvfp4_epilogue {
 #define NVFP4_DEVICE_TIMEOUT 0x1u /* a bounded wait inside a kernel gave up */
 #define NVFP4_DEVICE_BAD_GROUPS 0x2u /* group offsets broke their contract (grouped GEMM) */
 
-/* Bytes of workspace every call needs (a small constant). */
-size_t nvfp4_workspace_bytes(void);
+/* Operations, for nvfp4_workspace_bytes. */
+typedef enum nvfp4_op {
+  NVFP4_OP_QUANTIZE = 0,
+  NVFP4_OP_DEINTERLEAVE_QUANTIZE = 1,
+  NVFP4_OP_GEMM_TOPK = 2,
+  NVFP4_OP_RMSNORM_QUANTIZE = 3,
+  NVFP4_OP_INDEXER_TOPK = 4,
+  NVFP4_OP_GROUPED_SWIGLU_GEMM = 5,
+  NVFP4_OP_MHC_RMSNORM_QUANTIZE = 6
+} nvfp4_op;
+
+/*
+ * Bytes of workspace a call of operation `op` needs for a problem of `rows`
+ * x `cols` (quantize ops: the input's shape; GEMM ops: rows = M, cols = K,
+ * n = N, k = top-k).  Every kernel keeps its cross-CTA state in a few
+ * counters, so today the answer is the same small constant (256) for every
+ * operation and shape, and one workspace serves every call of a stream.
+ * Returns 0 for an unknown op or a negative size.
+ */
+size_t nvfp4_workspace_bytes(int op, int64_t rows, int64_t cols, int64_t n, int k);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Needed once per buffer. */
 int nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -101,7 +119,12 @@ int nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
  *         x, q and sf may then be NULL).
  * q     : [rows, cols/2] bytes, 8-byte aligned.   sf : [rows, cols/16] bytes.
  * gs    : one float on the device, written by the call (4-byte aligned).
- * Two kernels: a grid-wide amax whose last block writes gs, then the
+ * Launches: inputs that fit in the SMs' shared memory (up to about 30 MB)
+ * take ONE launch: each CTA copies its slice on chip, the CTAs meet on the
+ * grid-wide maximum (one thread-block cluster in distributed shared memory
+ * up to 512 KB, else a cooperative grid at a bounded counter barrier), and
+ * quantize from shared memory, so x crosses HBM once.  Larger inputs take
+ * two kernels: a grid-wide amax whose last block writes gs, then the
  * quantize pass, which reads gs from device memory.
  */
 int nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -131,9 +154,10 @@ int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, 
  * PERFORMANCE_AUDIT.md P4, "fuse RMSNorm into the next NVFP4 quantize";
  * the norm is input * inv_rms * weight[c], as in the model notes' kv_norm):
  *
- *   per row: sum of squares in a fixed order (16-element blocks accumulated
- *            with fused multiply-adds, block sums combined pairwise level by
- *            level), inv_rms = 1 / sqrt(sum / cols + eps)          (FP32)
+ *   per row: sum = the exact sum of x^2 over the row rounded once to FP32
+ *            (round to nearest even; the pages give an FP32 sum of squares
+ *            without an order, mhc.py _project_and_rms),
+ *            inv_rms = 1 / sqrt(sum / cols + eps)                  (FP32)
  *   y[r, c] = bf16((x[r, c] * inv_rms) * weight[c])   (round to nearest even)
  *   then exactly nvfp4_quantize of the bf16 matrix y, which never reaches
  *   memory.
@@ -203,10 +227,13 @@ int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
  * kernels.  All calls on a device share the array: calls that can overlap on
  * the GPU (different streams without ordering between them) race and give
  * wrong results.  The first call on a device, with that device current,
- * looks up the array's device address (cudaGetSymbolAddress); make that
- * first call before any stream capture.  Device status bits of these calls
- * are not readable with nvfp4_read_device_status (the quantize kernels set
- * none).  Allocates nothing.
+ * looks up the array's device address (cudaGetSymbolAddress) and keeps it
+ * for that device (one CUDA context per device, the runtime's primary
+ * context, is assumed); make that first call before any stream capture.  A
+ * bounded wait that runs out inside the one-pass kernel records
+ * NVFP4_DEVICE_TIMEOUT in the static scratch, where no caller can read it
+ * (nvfp4_read_device_status takes a workspace): q, sf and gs are then
+ * undefined and nothing reports it.  Allocates nothing.
  */
 int nvfp4_quantize_noalloc(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                            uint8_t* q, uint8_t* sf, float* gs, cudaStream_t stream);

@@ -62,7 +62,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
         L.nvfp4_workspace_bytes.restype = SZ
-        L.nvfp4_workspace_bytes.argtypes = []
+        L.nvfp4_workspace_bytes.argtypes = [I, I64, I64, I64, I]
         L.nvfp4_workspace_init.restype = I
         L.nvfp4_workspace_init.argtypes = [P, SZ, P]
         L.nvfp4_quantize.restype = I
@@ -128,8 +128,12 @@ def _bf16_bits(x: torch.Tensor) -> torch.Tensor:
 
 # ---------------------------------------------------------------- raw entry points
 
-def workspace_bytes() -> int:
-    return int(lib().nvfp4_workspace_bytes())
+OP_QUANTIZE, OP_DEINTERLEAVE_QUANTIZE, OP_GEMM_TOPK, OP_RMSNORM_QUANTIZE, OP_INDEXER_TOPK, \
+    OP_GROUPED_SWIGLU_GEMM, OP_MHC_RMSNORM_QUANTIZE = range(7)
+
+
+def workspace_bytes(op: int = OP_QUANTIZE, rows: int = 0, cols: int = 0, n: int = 0, k: int = 0) -> int:
+    return int(lib().nvfp4_workspace_bytes(op, rows, cols, n, k))
 
 
 def workspace(device=None, stream=None) -> torch.Tensor:

@@ -51,7 +51,11 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 extern "C" {
 
-size_t nvfp4_workspace_bytes(void) { return nvfp4::kWorkspaceBytes; }
+size_t nvfp4_workspace_bytes(int op, int64_t rows, int64_t cols, int64_t n, int k) {
+  if (op < NVFP4_OP_QUANTIZE || op > NVFP4_OP_MHC_RMSNORM_QUANTIZE || rows < 0 || cols < 0 || n < 0 || k < 0)
+    return 0;
+  return nvfp4::kWorkspaceBytes;  // cross-CTA counters only, whatever the shape
+}
 
 int nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
   const int st = check_workspace(ws, ws_bytes);

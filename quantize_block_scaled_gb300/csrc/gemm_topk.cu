@@ -891,11 +891,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             per_row * static_cast<uint32_t>(owned * p.k_split));
     }
   }
+  pdl_wait();  // the previous kernel's outputs (our A operand, scales, ...) are complete
+  // Tensor memory is taken only once the previous kernel has finished, so a
+  // CTA that starts early never holds it while waiting; one CTA per SM (the
+  // host pads shared memory above half of the SM's) means the allocation
+  // never waits for another CTA of this grid.
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  pdl_wait();  // the previous kernel's outputs (our A operand, scales, ...) are complete
   if (threadIdx.x == 0) {
     if (p.tma_sf) {
       // The first stages need no empty-slot wait: start their loads now,
@@ -1469,8 +1473,8 @@ struct Plan {
 
 // Pick the split, epilogue and shared-memory layout of one problem; false if
 // it cannot be laid out.
-bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, int max_cluster,
-               int rpc, int heads, Plan* out) {
+bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, int smem_one_cta,
+               int max_cluster, int rpc, int heads, Plan* out) {
   Plan pl{};
   pl.rpc = rpc;
   pl.heads = heads;
@@ -1542,6 +1546,10 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
   pl.smem = total();
   if (pl.smem > static_cast<size_t>(smem_optin)) return false;
+  // Every CTA allocates all of tensor memory: keep two CTAs off one SM by
+  // asking for more than half of the SM's shared memory.
+  if (pl.smem < static_cast<size_t>(smem_one_cta)) pl.smem = static_cast<size_t>(smem_one_cta);
+  if (pl.smem > static_cast<size_t>(smem_optin)) return false;
   if (heads && !pl.bulk) return false;  // head reduction stages token rows for bulk copies
   *out = pl;
   return true;
@@ -1594,7 +1602,6 @@ cudaError_t configure(size_t smem, int cluster) {
 // at all (answers cached per device and configuration).
 template <int BN, int KMAX>
 int active_clusters(int cluster, size_t smem) {
-  if (cluster <= 1) return sm_count();  // one CTA per SM
   static std::mutex mu;
   static int cache_dev[64], cache_cluster[64];
   static size_t cache_smem[64];
@@ -1606,11 +1613,21 @@ int active_clusters(int cluster, size_t smem) {
   for (int i = 0; i < n_cache; ++i)
     if (cache_dev[i] == dev && cache_cluster[i] == cluster && cache_smem[i] == smem) return cache_ok[i];
   int ok = 0;
-  if (configure<BN, KMAX>(smem, cluster) == cudaSuccess) {
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(cluster, cluster, smem, nullptr, attr);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN, KMAX>, &cfg) == cudaSuccess && n > 0) ok = n;
+  // Every CTA takes all of tensor memory, so a second CTA on one SM would
+  // wait in its allocation: a footprint that lets two share an SM is refused.
+  int per_sm = 0;
+  if (configure<BN, KMAX>(smem, cluster) == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_topk_kernel<BN, KMAX>, kThreads, smem) ==
+          cudaSuccess &&
+      per_sm == 1) {
+    if (cluster <= 1) {
+      ok = sm_count();
+    } else {
+      cudaLaunchAttribute attr[2];
+      cudaLaunchConfig_t cfg = launch_config<BN, KMAX>(cluster, cluster, smem, nullptr, attr);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_topk_kernel<BN, KMAX>, &cfg) == cudaSuccess && n > 0) ok = n;
+    }
   }
   cudaGetLastError();  // a refused query leaves no error behind
   if (n_cache < 64) {
@@ -1668,13 +1685,18 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   if (a.M == 0) return NVFP4_OK;
   int dev = 0;
   cudaGetDevice(&dev);
-  int smem_optin = 0;
+  int smem_optin = 0, smem_sm = 0, smem_reserved = 0;
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  // the least dynamic shared memory that leaves no room for a second CTA
+  const int smem_one_cta = smem_sm / 2 - smem_reserved + 1;
   // Largest cluster (16, else 8, 4, ...) whose CTAs can be co-resident.
   Plan pl;
   int cap = kMaxCluster;
   for (;;) {
-    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, BM, a.heads, &pl)) return NVFP4_ERR_UNSUPPORTED;
+    if (!make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, smem_one_cta, cap, BM, a.heads, &pl))
+      return NVFP4_ERR_UNSUPPORTED;
     if (active(pl) > 0) break;
     const int c = pl.n_split * pl.k_split;
     if (c <= 1 || cap <= 1) return NVFP4_ERR_UNSUPPORTED;
@@ -1689,7 +1711,8 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
     rpc = (rpc + unit - 1) / unit * unit;
     Plan spread;
     if (rpc < BM &&
-        make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, cap, static_cast<int>(rpc), a.heads, &spread) &&
+        make_plan(a.M, a.N, a.K, a.k, sm_count(), smem_optin, smem_one_cta, cap, static_cast<int>(rpc), a.heads,
+                  &spread) &&
         spread.n_split == pl.n_split && spread.k_split == pl.k_split && active(spread) > 0)
       pl = spread;
   }

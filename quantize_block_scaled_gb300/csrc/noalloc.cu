@@ -36,7 +36,8 @@ std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of this device's copy of the array (set up on first use;
-// host code may not use the symbol itself as an address).
+// host code may not use the symbol itself as an address).  Cached per device
+// ordinal: the runtime's primary context is the one context per device.
 int scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -57,7 +58,7 @@ int scratch_for_current_device(void** out) {
 
 extern "C" int nvfp4_quantize_noalloc(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                                       uint8_t* q, uint8_t* sf, float* gs, cudaStream_t stream) {
-  if (nvfp4_workspace_bytes() > kNoallocScratchBytes) return NVFP4_ERR_WORKSPACE;
+  if (nvfp4_workspace_bytes(NVFP4_OP_QUANTIZE, rows, cols, 0, 0) > kNoallocScratchBytes) return NVFP4_ERR_WORKSPACE;
   // nvfp4_quantize's own argument checks, made here first so that a refused
   // call touches neither the scratch nor the stream.
   const auto misaligned = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; };

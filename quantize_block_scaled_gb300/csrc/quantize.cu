@@ -437,11 +437,15 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   }
   __syncthreads();  // the barrier is initialised before anyone waits on it
   uint32_t never = 0;
-  if (!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL) && threadIdx.x == 0)
-    atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+  // A slice that did not land in time is left alone: the CTA still meets the
+  // others (so none waits for it) but contributes no maximum and writes no
+  // outputs, and the recorded NVFP4_DEVICE_TIMEOUT marks q, sf and gs as
+  // undefined.
+  const bool late_load = __syncthreads_or(!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL)) != 0;
+  if (late_load && threadIdx.x == 0) atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
   // local max of |x| over the slice
   const uint4* sv = reinterpret_cast<const uint4*>(smem);
-  const int64_t n_vec = n_units * (kUnitBytes / 16);
+  const int64_t n_vec = late_load ? 0 : n_units * (kUnitBytes / 16);
   uint32_t m2 = 0;
   for (int64_t i = threadIdx.x; i < n_vec; i += kOnePassThreads) m2 = __vmaxu2(m2, absmax8(sv[i]));
   uint32_t m = fold16(m2);
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   sc.gs = gs_sh;
   sc.r_gs = __frcp_rn(sc.gs);
   sc.r_six = __frcp_rn(6.0f);
-  for (int64_t i = threadIdx.x; i < n_units; i += kOnePassThreads) {
+  for (int64_t i = threadIdx.x; i < (late_load ? 0 : n_units); i += kOnePassThreads) {
     const int64_t u = u0 + i;
     if constexpr (G == 0) {
       uint32_t sbyte;
@@ -531,6 +535,8 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
       srow[inter / 16 + c] = static_cast<uint8_t>(su);
     }
   }
+  // copies still in flight after a timeout get one more bounded wait
+  if (late_load && threadIdx.x == 0) ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL);
   if constexpr (kCluster) return;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -612,51 +618,134 @@ bool launch_onepass(const uint16_t* x, int64_t rows, int64_t upr, int64_t ld, ui
 // The quantize input produced by an RMSNorm: y = bf16((x * inv_rms) * w[c])
 // with inv_rms = 1 / sqrt(sum(x^2) / cols + eps), fused so that y never
 // reaches HBM (the compare view's PERFORMANCE_AUDIT.md P4).  The sum of
-// squares follows one fixed order: each 16-element block accumulated with
-// fused multiply-adds in element order, the block sums then combined
-// pairwise level by level (entry j of a level is the sum of entries 2j and
-// 2j + 1 of the level below, or entry 2j alone at an odd end).
-constexpr int kRmsMaxBlocks = 1024;  // 16-element blocks per row (cols <= 16384)
+// squares has no order: it is the exact sum rounded once to FP32.
+//
+// Exact sum.  A finite bf16 value is M * 2^q (M < 256 an integer, q =
+// max(E, 1) - 134 from its exponent field E), so relative to the row's
+// largest exponent Emax an element with d = Emax' - E' <= 17 (primes: at
+// least 1) is the integer a = M << (17 - d) < 2^25 in units of
+// 2^(qmax - 17), and its square a^2 < 2^50 is exact in a 64-bit sum of up to
+// 2^14 terms.  Window w >= 1 holds the elements with 17w < d <= 17w + 17 in
+// units 2^-17w smaller.  Windows 0 and 1 cover almost every row; what lies
+// below them can only set the sticky bit of the rounding, unless window 1's
+// low bits sit so close to a carry that the lower windows could cross it,
+// in which case every window is summed (a slow pass per window, rare).
+constexpr int kWinBits = 17;         // exponent steps per window; squares gain 34 bits
+constexpr uint64_t kLow34 = (1ull << 34) - 1;
 
-__device__ __forceinline__ float sq_block(uint4 a, uint4 b) {
-  float acc = 0.0f;
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float lo = lo_bf16(w[i]), hi = hi_bf16(w[i]);
-    acc = __fmaf_rn(lo, lo, acc);
-    acc = __fmaf_rn(hi, hi, acc);
-  }
-  return acc;
+// Add the square of one bf16 value (bits h, exponent field e) to windows 0
+// and 1, or flag it as lying below them.
+__device__ __forceinline__ void sq_windows(uint32_t h, int emax, uint64_t& w0, uint64_t& w1, uint32_t& below) {
+  const uint32_t e = (h >> 7) & 0xFFu;
+  const uint32_t m = (h & 0x7Fu) | (e != 0 ? 0x80u : 0u);
+  const int d = emax - max(static_cast<int>(e), 1);
+  const bool in0 = d <= kWinBits, in1 = !in0 && d <= 2 * kWinBits;
+  const uint32_t a = (in0 || in1) ? m << (in0 ? kWinBits - d : 2 * kWinBits - d) : 0u;
+  const uint64_t sq = static_cast<uint64_t>(a) * a;
+  w0 += in0 ? sq : 0ull;
+  w1 += in1 ? sq : 0ull;
+  below |= (in0 || in1) ? 0u : m;
 }
 
-// inv_rms of one bf16 row (global or shared memory), one warp; p is this
-// warp's scratch of at least cols / 16 floats.
-__device__ float warp_inv_rms(const uint16_t* xr, int nb, int64_t cols, float eps, float* p) {
+// Window w alone (slow pass): the squares of the elements with
+// 17w < d <= 17w + 17 (w = 0: d <= 17), in that window's units.
+__device__ __forceinline__ uint64_t sq_window(uint32_t h, int emax, int w) {
+  const uint32_t e = (h >> 7) & 0xFFu;
+  const uint32_t m = (h & 0x7Fu) | (e != 0 ? 0x80u : 0u);
+  const int d = emax - max(static_cast<int>(e), 1);
+  const int wd = d == 0 ? 0 : (d - 1) / kWinBits;
+  const uint32_t a = wd == w ? m << (kWinBits * (w + 1) - d) : 0u;
+  return static_cast<uint64_t>(a) * a;
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// v * 2^e for a v whose product is on the FP32 grid (or beyond its range,
+// giving inf), by multiplications with normal powers of two.
+__device__ __forceinline__ float scale_pow2(float v, int e) {
+  auto pow2 = [](int k) { return __int_as_float((k + 127) << 23); };  // -126 <= k <= 127
+  if (e > 127) {
+    v = __fmul_rn(v, pow2(127));
+    e -= 127;
+    if (e > 127) e = 127;  // the product is past FP32's range already
+  } else if (e < -126) {
+    v = __fmul_rn(v, pow2(-100));
+    e += 100;
+  }
+  return __fmul_rn(v, pow2(e));
+}
+
+// FP32 nearest (top + t) * 2^e0 for an integer top >= 2^34 and 0 <= t < 1,
+// where sticky says whether t > 0 (ties to even).
+__device__ __forceinline__ float round_sum(uint64_t top, bool sticky, int e0) {
+  const int h = 63 - __clzll(static_cast<long long>(top));
+  const int p = max(h - 23, -149 - e0);  // lowest kept bit: 24 bits, or FP32's 2^-149 step
+  if (p >= 64) return 0.0f;              // top * 2^e0 < 2^-150: nearest is zero
+  const uint64_t keep = top >> p;
+  const uint64_t rem = top & ((1ull << p) - 1ull);
+  const uint64_t half = 1ull << (p - 1);  // p >= 11 (h >= 34)
+  const bool up = rem > half || (rem == half && (sticky || (keep & 1ull)));
+  return scale_pow2(static_cast<float>(keep + (up ? 1ull : 0ull)), p + e0);
+}
+
+// The FP32 sum of squares of one bf16 row (global or shared memory), one
+// warp; every lane returns it.  cols is a multiple of 16.
+__device__ float warp_sum_sq_exact(const uint16_t* xr, int64_t cols) {
   const int lane = static_cast<int>(threadIdx.x & 31);
-  for (int b = lane; b < nb; b += 32) {
-    const uint4* v = reinterpret_cast<const uint4*>(xr + b * 16);
-    p[b] = sq_block(v[0], v[1]);
-  }
-  __syncwarp();
-  for (int n = nb; n > 1; n = (n + 1) / 2) {
-    const int half = (n + 1) / 2;
-    float s[kRmsMaxBlocks / 64];  // outputs of this lane at this level (read all, then write)
+  const uint4* v = reinterpret_cast<const uint4*>(xr);
+  const int nv = static_cast<int>(cols / 8);
+  uint32_t m2 = 0;
+  for (int i = lane; i < nv; i += 32) m2 = __vmaxu2(m2, absmax8(v[i]));
+  uint32_t mb = fold16(m2);
 #pragma unroll
-    for (int t = 0; t < kRmsMaxBlocks / 64; ++t) {
-      const int j = lane + 32 * t;
-      s[t] = j < half ? (2 * j + 1 < n ? __fadd_rn(p[2 * j], p[2 * j + 1]) : p[2 * j]) : 0.0f;
-    }
-    __syncwarp();
+  for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+  if (mb == 0) return 0.0f;
+  const int emax = max(static_cast<int>(mb >> 7), 1);
+  uint64_t w0 = 0, w1 = 0;
+  uint32_t below = 0;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 t = v[i];
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-    for (int t = 0; t < kRmsMaxBlocks / 64; ++t) {
-      const int j = lane + 32 * t;
-      if (j < half) p[j] = s[t];
+    for (int j = 0; j < 4; ++j) {
+      sq_windows(w[j] & 0xFFFFu, emax, w0, w1, below);
+      sq_windows(w[j] >> 16, emax, w0, w1, below);
     }
-    __syncwarp();
   }
-  const float sum = nb > 0 ? p[0] : 0.0f;
-  __syncwarp();  // the caller reuses p for its next row
+  w0 = warp_sum_u64(w0);
+  w1 = warp_sum_u64(w1);
+  below = __reduce_or_sync(0xFFFFFFFFu, below);
+  const int e0 = 2 * (emax - 134) - 2 * kWinBits;  // window 0's unit: 2^e0
+  // The windows below window 1 add less than 2^30 of window 1's units.
+  if (below == 0 || (w1 & kLow34) < kLow34 + 1 - (1ull << 30))
+    return round_sum(w0 + (w1 >> 34), (w1 & kLow34) != 0 || below != 0, e0);
+  // Every window, from the bottom up: carry the whole part, keep the rest as sticky.
+  const int n_win = (emax - 1) / kWinBits + 1;
+  uint64_t carry = 0;
+  bool sticky = false;
+  for (int wi = n_win - 1; wi >= 0; --wi) {
+    uint64_t acc = 0;
+    for (int i = lane; i < nv; i += 32) {
+      const uint4 t = v[i];
+      const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc += sq_window(w[j] & 0xFFFFu, emax, wi) + sq_window(w[j] >> 16, emax, wi);
+    }
+    const uint64_t tot = warp_sum_u64(acc) + carry;
+    if (wi == 0) return round_sum(tot, sticky, e0);
+    sticky = sticky || (tot & kLow34) != 0;
+    carry = tot >> 34;
+  }
+  return 0.0f;  // not reached
+}
+
+// inv_rms of one bf16 row, one warp (every lane gets it).
+__device__ float warp_inv_rms(const uint16_t* xr, int64_t cols, float eps) {
+  const float sum = warp_sum_sq_exact(xr, cols);
   const float mean = __fdiv_rn(sum, static_cast<float>(cols));
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 }
@@ -683,16 +772,14 @@ __global__ void __launch_bounds__(kRmsThreads)
                         const uint16_t* __restrict__ wt, float eps, float* __restrict__ gs_out,
                         Workspace* __restrict__ ws) {
   ptx::pdl_launch_dependents();
-  extern __shared__ __align__(16) float rms_scratch[];
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nb = static_cast<int>(cols / 16);
-  float* p = rms_scratch + warp * nb;
   uint32_t m2 = 0;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
   for (int64_t r = gw; r < rows; r += nw) {
     const uint16_t* xr = x + r * ld;
-    const float inv = warp_inv_rms(xr, nb, cols, eps, p);
+    const float inv = warp_inv_rms(xr, cols, eps);
     for (int b = lane; b < nb; b += 32) {
       const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
       const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
@@ -726,16 +813,14 @@ __global__ void __launch_bounds__(kRmsThreads)
                             const uint16_t* __restrict__ wt, float eps, uint8_t* __restrict__ q,
                             uint8_t* __restrict__ sf, const float* __restrict__ gs_ptr) {
   ptx::pdl_launch_dependents();
-  extern __shared__ __align__(16) float rms_scratch[];
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nb = static_cast<int>(cols / 16);
-  float* p = rms_scratch + warp * nb;
   const Scales sc = make_scales(gs_ptr);
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
   for (int64_t r = gw; r < rows; r += nw) {
     const uint16_t* xr = x + r * ld;
-    const float inv = warp_inv_rms(xr, nb, cols, eps, p);
+    const float inv = warp_inv_rms(xr, cols, eps);
     for (int b = lane; b < nb; b += 32) {
       const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
       const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
@@ -773,7 +858,6 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   const int64_t n_rows = r1 > r0 ? r1 - r0 : 0;
   const uint32_t row_bytes = static_cast<uint32_t>(cols * 2);
   uint16_t* data = reinterpret_cast<uint16_t*>(smem);
-  float* scratch = reinterpret_cast<float*>(smem + rows_per_cta * row_bytes) + warp * nb;
   const uint32_t bar_a = ptx::smem_addr(&bar);
   ptx::pdl_wait();
   if (threadIdx.x == 0) {
@@ -786,12 +870,14 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   }
   __syncthreads();
   uint32_t never = 0;
-  if (!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL) && threadIdx.x == 0)
-    atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+  // as in quantize_onepass_kernel: a late slice adds nothing and writes nothing
+  const bool late_load = __syncthreads_or(!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL)) != 0;
+  if (late_load && threadIdx.x == 0) atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
+  const int64_t n_rows_live = late_load ? 0 : n_rows;
   uint32_t m2 = 0;
-  for (int64_t rr = warp; rr < n_rows; rr += kWarpsOp) {
+  for (int64_t rr = warp; rr < n_rows_live; rr += kWarpsOp) {
     uint16_t* yr = data + rr * cols;
-    const float inv = warp_inv_rms(yr, nb, cols, eps, scratch);
+    const float inv = warp_inv_rms(yr, cols, eps);
     for (int b = lane; b < nb; b += 32) {
       uint4* v = reinterpret_cast<uint4*>(yr + b * 16);
       const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
@@ -853,7 +939,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   sc.r_gs = __frcp_rn(sc.gs);
   sc.r_six = __frcp_rn(6.0f);
   const uint4* sv = reinterpret_cast<const uint4*>(data);
-  const int64_t n_blocks = n_rows * nb;
+  const int64_t n_blocks = n_rows_live * nb;
   for (int64_t i = threadIdx.x; i < n_blocks; i += kOnePassThreads) {
     uint32_t sbyte;
     uint2 codes;
@@ -862,6 +948,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
     __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
     sf[blk] = static_cast<uint8_t>(sbyte);
   }
+  if (late_load && threadIdx.x == 0) ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL);
   if constexpr (kCluster) return;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -879,12 +966,10 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
 cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                                          const uint16_t* wt, float eps, uint8_t* q, uint8_t* sf, float* gs,
                                          Workspace* ws, cudaStream_t stream) {
-  const int nb = static_cast<int>(cols / 16);
   const int64_t row_bytes = cols * 2;
   const int sms = sm_count();
   if (rows > 0) {
-    const int64_t scratch = static_cast<int64_t>(kOnePassThreads / 32) * nb * 4;
-    const int64_t rows_cap = (static_cast<int64_t>(kOnePassMaxBytes) - scratch) / row_bytes;
+    const int64_t rows_cap = static_cast<int64_t>(kOnePassMaxBytes) / row_bytes;
     if (rows_cap >= 1 && rows <= rows_cap * sms) {
       const bool cluster = rows * row_bytes <= kClusterMaxBytes;
       const int64_t cap = cluster ? 16 : sms;
@@ -895,7 +980,7 @@ cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_
       if (per > rows_cap) per = rows_cap;
       grid = (rows + per - 1) / per;
       if (grid <= cap) {
-        const size_t smem = static_cast<size_t>(per * row_bytes + scratch);
+        const size_t smem = static_cast<size_t>(per * row_bytes);
         auto kernel = cluster ? rmsnorm_quantize_onepass_kernel<true> : rmsnorm_quantize_onepass_kernel<false>;
         bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)) == cudaSuccess;
@@ -932,25 +1017,17 @@ cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_
       }
     }
   }
-  const size_t scratch2 = static_cast<size_t>(kRmsThreads / 32) * nb * 4;
   cudaError_t e = cudaSuccess;
-  if (scratch2 > 48 * 1024)
-    e = cudaFuncSetAttribute(rmsnorm_amax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(scratch2));
-  if (e == cudaSuccess && scratch2 > 48 * 1024)
-    e = cudaFuncSetAttribute(rmsnorm_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(scratch2));
-  if (e != cudaSuccess) return e;
   const int64_t warps_needed = rows > 0 ? rows : 1;
   int64_t grid = (warps_needed + kRmsThreads / 32 - 1) / (kRmsThreads / 32);
   if (grid > 4ll * sms) grid = 4ll * sms;
   count_launch();
-  rmsnorm_amax_kernel<<<static_cast<unsigned>(grid), kRmsThreads, scratch2, stream>>>(x, rows, cols, ld, wt, eps,
+  rmsnorm_amax_kernel<<<static_cast<unsigned>(grid), kRmsThreads, 0, stream>>>(x, rows, cols, ld, wt, eps,
                                                                                        gs, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess || rows == 0) return e;
   count_launch();
-  rmsnorm_quantize_kernel<<<static_cast<unsigned>(grid), kRmsThreads, scratch2, stream>>>(x, rows, cols, ld, wt,
+  rmsnorm_quantize_kernel<<<static_cast<unsigned>(grid), kRmsThreads, 0, stream>>>(x, rows, cols, ld, wt,
                                                                                            eps, q, sf, gs);
   return cudaGetLastError();
 }

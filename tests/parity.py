@@ -1,4 +1,4 @@
-"""Comparison rules between the CUDA path and the oracle (numpy only).
+"""Comparison rules between the CUDA path and the oracle.
 
 * Quantize outputs (codes, scale bytes, global scale) must be bit-exact.
 * GEMM logits and scores: |gpu - oracle| <= ATOL + RTOL * |oracle| (FP32),
@@ -11,6 +11,8 @@
   beyond N hold index -1 and score -inf.
 """
 import numpy as np
+
+import oracle
 
 RTOL = 1e-3
 ATOL = 1e-4
@@ -35,7 +37,8 @@ def assert_topk(gpu_idx, gpu_score, gpu_weight, ref_score_rows, ref_weight_rows,
     """Check GPU top-k of each row against the oracle's full score rows.
 
     normalized: the weights are the router's normalised gating weights, so
-    the reference is the oracle's weights of the GPU's picks over their sum.
+    the reference is oracle.normalize_topk_weights applied to the oracle's
+    weights of the GPU's picks.
     """
     gpu_idx = np.asarray(gpu_idx)
     gpu_score = np.asarray(gpu_score)
@@ -59,7 +62,9 @@ def assert_topk(gpu_idx, gpu_score, gpu_weight, ref_score_rows, ref_weight_rows,
         if gpu_weight is not None and ref_weight_rows is not None:
             W = ref_weight_rows[r].astype(np.float64)
             gw = np.asarray(gpu_weight)[r][:take].astype(np.float64)
-            ref_w = W[gi] / W[gi].sum() if normalized else W[gi]
+            # normalised: the oracle's own normalisation of its weights of the GPU's picks
+            ref_w = (oracle.normalize_topk_weights(gi[None, :], W[gi][None, :].astype(np.float32))[0]
+                     .astype(np.float64) if normalized else W[gi])
             assert (np.abs(gw - ref_w) <= tol(ref_w)).all(), f"{what} row {r}: weight mismatch"
         # order: non-increasing, ties by increasing index
         assert (np.diff(gs) <= 0).all(), f"{what} row {r}: scores not descending"

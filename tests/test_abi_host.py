@@ -44,7 +44,14 @@ def test_library_exports_every_declared_symbol(L):
 def test_status_strings_and_workspace_size(L):
     assert L.nvfp4_status_string(0) == b"ok"
     assert L.nvfp4_status_string(2) == b"unsupported shape or alignment"
-    assert L.nvfp4_workspace_bytes() == 256
+    import quantize_block_scaled_gb300 as q
+    # one constant for every operation and shape (the kernels keep counters only)
+    for op in range(7):
+        assert L.nvfp4_workspace_bytes(op, 8192, 7168, 256, 8) == 256
+        assert q.workspace_bytes(op, 1, 16, 0, 0) == 256
+    assert L.nvfp4_workspace_bytes(7, 1, 16, 0, 0) == 0     # unknown operation
+    assert L.nvfp4_workspace_bytes(-1, 1, 16, 0, 0) == 0
+    assert L.nvfp4_workspace_bytes(0, -1, 16, 0, 0) == 0    # negative size
 
 
 FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first

@@ -2,10 +2,14 @@
 
 * The replica aggregation (barrier, max over ranks, whole-job throughput) on
   two gloo ranks on the CPU, as torchrun would launch them.
-* The clock-sample summary (throttle reasons, window selection).
+* The clock-sample summary (throttle reasons, window selection), the
+  parser of nvidia-smi's sample lines, and the sampler's pipe reader against
+  a stand-in nvidia-smi that prints samples until it is interrupted.
 """
 import os
 import socket
+import stat
+import time
 
 import pytest
 import torch.multiprocessing as mp
@@ -87,3 +91,33 @@ def test_rotating_sets_exceed_twice_l2():
         assert (n - 1) * b < bench.ROTATE_BYTES or n == 2
     assert bench.rotating_sets(14 * 1024) is None  # 14 KB would need ~20k copies
     assert bench.rotating_sets(bench.ROTATE_BYTES + 1) == 2
+
+
+SMI_LINE = ("2026/12/02 16:20:01.250, 0, 1965, 2070, 1012.55, 0x0000000000000004, Not Active, Not Active, "
+            "Not Active, Active")
+
+
+def test_smi_line_parser():
+    s = bench.parse_smi_line(SMI_LINE)
+    assert s["sm"] == 1965.0 and s["sm_max"] == 2070.0 and s["pcap"] == "Active" and s["hw"] == "Not Active"
+    assert s["t"] == time.mktime(time.strptime("2026/12/02 16:20:01", "%Y/%m/%d %H:%M:%S")) + 0.25
+    assert bench.parse_smi_line("timestamp, index, clocks.current.sm [MHz]") is None  # a header
+    assert bench.parse_smi_line("") is None
+    assert bench.parse_smi_line("2026/12/02 16:20:01.250, 0, [N/A], 2070, 1, 0x0, a, b, c, d") is None
+
+
+def test_clock_sampler_reads_samples_until_interrupted(tmp_path, monkeypatch):
+    # a stand-in nvidia-smi on PATH: one sample line (current time) every 10 ms, forever
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/bash\nwhile true; do\n"
+                    "  printf '%s, 0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active\\n' "
+                    "\"$(date '+%Y/%m/%d %H:%M:%S.%N' | cut -c1-23)\"\n  sleep 0.01\ndone\n")
+    fake.chmod(fake.stat().st_mode | stat.S_IEXEC)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ['PATH']}")
+    with bench.ClockSampler(0, period_ms=10) as clk:
+        t0 = time.time()
+        time.sleep(0.6)
+        t1 = time.time()
+    assert len(clk.samples) >= 10
+    s = clk.summary(t0 - 1.0, t1 + 1.0)
+    assert s["window"] == "timed" and s["sm_mhz"] == 2070.0 and s["reasons"] == []

@@ -1,4 +1,4 @@
-"""GPU parity of nvfp4_indexer_topk (the full indexer score):
+"""GPU parity of nvfp4_indexer_topk (the full indexer score with the head sum):
 I[t, s] = sum_h w[t, h] * ReLU(q[t, h] . K[s]) fused in the GEMM epilogue,
 then the top-k per token.  Scores within 1e-3 relative / 1e-4 absolute,
 index sets equal up to near-ties (tests/parity.py)."""

@@ -2,7 +2,9 @@
 with the oracle: bit-exact codes, scales and global scale.  Sizes cover the
 three kernel paths: one cluster (up to 512 KB of input), one cooperative
 grid (rows that fit in the SMs' shared memory), and the two row-parallel
-passes beyond.
+passes beyond.  The sum of squares is the exact sum rounded once, so rows
+of very wide range (bf16 subnormals, squares below FP32's normal range, a
+row whose low-order terms decide the rounding) are compared too.
 """
 import numpy as np
 import pytest
@@ -75,7 +77,8 @@ def test_rmsnorm_quantize_strided_and_outliers(nv, ws):
 
 def test_rmsnorm_quantize_two_calls_and_zero_rows(nv, ws):
     x1 = workloads.quantize_input(16, seed=91)
-    x2 = workloads.quantize_input(16, seed=92) // 2
+    # smaller values (scaled as floats): a stale maximum from the first call would show
+    x2 = workloads.bf16_bits(workloads.bf16_to_f32(workloads.quantize_input(16, seed=92)) * np.float32(0.25))
     w = norm_weight(7168, 5)
     for x in (x1, x2):
         check(run(nv, ws, x, w), oracle.rmsnorm_quantize(x, w, EPS), "repeat")
@@ -85,3 +88,44 @@ def test_rmsnorm_quantize_two_calls_and_zero_rows(nv, ws):
     q, sf, gs = nv.rmsnorm_quantize(xd, wd, EPS, ws)
     torch.cuda.synchronize()
     assert gs.item() == float(np.float32(1e-8) / np.float32(2688.0))
+
+
+def _bits(e, m):
+    """bf16 bit pattern with exponent field e and the 7 stored mantissa bits of m."""
+    return (e << 7) | (m & 0x7F)
+
+
+def wide_range_rows(cols):
+    """Rows whose sum of squares needs more than the two windows the kernel
+    sums by default: magnitudes over ~2^100 in one row, bf16 subnormals,
+    squares below FP32's normal range, and a crafted row whose window sums
+    sit right below a carry with a tiny term under them (the kernel then
+    sums every window)."""
+    rng = np.random.default_rng(77)
+    rows = []
+    for lo, hi in ((-50, 50), (-120, -60), (-133, -126), (0, 100)):
+        f = rng.standard_normal(cols) * np.exp2(rng.integers(lo, hi, cols).astype(np.float64))
+        rows.append(workloads.bf16_bits(f.astype(np.float32)))
+    crafted = [_bits(127, 128)] + [_bits(109, 129)] * 3 + [_bits(107, 129)] * 15 + [_bits(87, 128)]
+    crafted = np.array(crafted + [0] * (cols - len(crafted)), np.uint16)
+    rows.append(crafted)
+    rows.append(np.where(np.arange(cols) % 2 == 0, crafted[np.arange(cols) % 20], 0).astype(np.uint16))
+    tie = np.zeros(cols, np.uint16)  # 4096^2 + 1 = 2^24 + 1: halfway, ties to even
+    tie[0], tie[1] = _bits(139, 128), _bits(127, 128)
+    rows.append(tie)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("rows_rep", [1, 300])
+def test_rmsnorm_quantize_exact_sum_wide_range(nv, ws, rows_rep):
+    # rows_rep = 1: one cluster; 300 (2100 rows x 16 KB): the cooperative grid
+    x = np.tile(wide_range_rows(7168), (rows_rep, 1))
+    w = norm_weight(7168, 11)
+    check(run(nv, ws, x, w), oracle.rmsnorm_quantize(x, w, EPS), f"wide-range rows x{rows_rep}")
+
+
+def test_rmsnorm_quantize_exact_sum_wide_range_two_pass(nv, ws):
+    # enough rows that the row-parallel two-pass kernels run
+    x = np.tile(wide_range_rows(7168), (400, 1))
+    w = norm_weight(7168, 12)
+    check(run(nv, ws, x, w), oracle.rmsnorm_quantize(x, w, EPS), "wide-range rows, two passes")
