@@ -29,11 +29,12 @@ constexpr int kThreads = 256;
 constexpr float kGsDivisor = 2688.0f;  // 6 (E2M1 max) * 448 (E4M3 max)
 constexpr float kAmaxFloor = 1e-8f;
 
-// First pass (amax): ordinary loads, so a tensor that fits in L2 is still
-// there for the second pass; for a larger tensor the tail that the second
-// pass (which runs backwards) reads first is loaded with an L2 evict-last
-// policy and the rest with evict-first, so the tail survives in L2.
-// Second pass: streaming loads (last use).
+// First pass (amax): the tail of the tensor that the second pass (which runs
+// backwards) reads first, up to kL2KeepBytes, is loaded with an L2
+// evict-last policy and the rest with evict-first, so the tail survives in
+// L2.  Second pass: loads with an evict-first policy (last use: lines just
+// consumed leave before the ones still to come), ordinary stores (the codes
+// and scales stay in L2 for the GEMM that reads them next).
 __device__ __forceinline__ uint4 ld_keep(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
@@ -83,8 +84,10 @@ __global__ void __launch_bounds__(kThreads, 4)
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (ld == vpr * 8) {
     const uint4* xv = reinterpret_cast<const uint4*>(x);
-    const int64_t keep_from = total * 16 > 2 * kL2KeepBytes ? total - kL2KeepBytes / 16 : total;
-    if (keep_from < total) {  // larger than L2: keep the tail, stream the head
+    // Keep (at most) the last kL2KeepBytes in L2 for the quantize pass, which
+    // starts from the end; the head streams through.
+    const int64_t keep_from = total * 16 > kL2KeepBytes ? total - kL2KeepBytes / 16 : 0;
+    {
       const uint64_t pol_first = l2_policy_first(), pol_last = l2_policy_last();
       for (; i + (kAmaxUnroll - 1) * stride < total; i += kAmaxUnroll * stride) {
         uint4 v[kAmaxUnroll];
@@ -97,15 +100,6 @@ __global__ void __launch_bounds__(kThreads, 4)
         for (int u = 0; u < kAmaxUnroll; ++u) m2 = __vmaxu2(m2, absmax8(v[u]));
       }
       for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(ld_policy(xv + i, i >= keep_from ? pol_last : pol_first)));
-    } else {
-      for (; i + (kAmaxUnroll - 1) * stride < total; i += kAmaxUnroll * stride) {
-        uint4 v[kAmaxUnroll];
-#pragma unroll
-        for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(xv + i + u * stride);
-#pragma unroll
-        for (int u = 0; u < kAmaxUnroll; ++u) m2 = __vmaxu2(m2, absmax8(v[u]));
-      }
-      for (; i < total; i += stride) m2 = __vmaxu2(m2, absmax8(__ldg(xv + i)));
     }
   } else if (i < total) {
     int64_t r = i / vpr, c = i % vpr;
@@ -163,21 +157,6 @@ __device__ __forceinline__ float e4m3_decode(uint32_t c) {
   return f;
 }
 
-// Four E2M1 bytes (8 codes, element 0 in the low nibble) of 8 floats.
-__device__ __forceinline__ uint32_t cvt_e2m1x8(float f0, float f1, float f2, float f3, float f4,
-                                               float f5, float f6, float f7) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(out)
-      : "f"(f0), "f"(f1), "f"(f2), "f"(f3), "f"(f4), "f"(f5), "f"(f6), "f"(f7));
-  return out;
-}
-
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -195,48 +174,91 @@ __device__ __forceinline__ float div_rn(float a, float b, float r) {
   return __fmaf_rn(e, r, q);
 }
 
-// The same for b > 0, keeping the sign of a zero a (the correction's
-// (+0) + (-0) would otherwise turn -0 / b into +0; a nonzero quotient
-// already carries a's sign, so the OR changes nothing else).
-__device__ __forceinline__ float div_rn_signed(float a, float b, float r) {
-  const float d = div_rn(a, b, r);
-  return __uint_as_float(__float_as_uint(d) | (__float_as_uint(a) & 0x80000000u));
-}
-
-// Codes of 8 values x / den (correctly rounded quotients; den == 0 passes
-// r = 0 and gives signed zeros).  The E2M1 conversion rounds to nearest
-// even, saturates, and keeps the sign of values that round to zero.
-__device__ __forceinline__ uint32_t encode8(uint4 v, float r, float den) {
-  return cvt_e2m1x8(div_rn_signed(lo_bf16(v.x), den, r), div_rn_signed(hi_bf16(v.x), den, r),
-                    div_rn_signed(lo_bf16(v.y), den, r), div_rn_signed(hi_bf16(v.y), den, r),
-                    div_rn_signed(lo_bf16(v.z), den, r), div_rn_signed(hi_bf16(v.z), den, r),
-                    div_rn_signed(lo_bf16(v.w), den, r), div_rn_signed(hi_bf16(v.w), den, r));
-}
-
-struct Scales {
-  float gs;      // global scale
-  float r_gs;    // RN(1 / gs)
-  float r_six;   // RN(1 / 6)
+// Per-code divisors of one tensor: entry c holds den = e4m3(c) * gs (one
+// FP32 multiply) and RN(1 / den) (0 when den is 0).  One table per CTA in
+// shared memory, filled once gs is known, replaces a decode, a multiply and a
+// correctly rounded reciprocal per block with one shared-memory load.
+struct Codec {
+  float gs;            // global scale
+  float r_gs;          // RN(1 / gs)
+  float r_six;         // RN(1 / 6)
+  const float2* tab;   // [128] {den, RN(1/den)} by E4M3 code
 };
 
-__device__ __forceinline__ Scales make_scales(const float* gs_ptr) {
-  Scales sc;
-  sc.gs = __ldg(gs_ptr);
-  sc.r_gs = __frcp_rn(sc.gs);
-  sc.r_six = __frcp_rn(6.0f);
-  return sc;
+// Threads of the block fill the table (the caller then synchronises).
+__device__ __forceinline__ void fill_codec(float2* tab, float gs) {
+  for (int c = static_cast<int>(threadIdx.x); c < 128; c += static_cast<int>(blockDim.x)) {
+    const float den = __fmul_rn(e4m3_decode(static_cast<uint32_t>(c)), gs);
+    tab[c] = make_float2(den, den == 0.0f ? 0.0f : __frcp_rn(den));
+  }
+}
+
+__device__ __forceinline__ Codec make_codec(float gs, const float2* tab) {
+  Codec cd;
+  cd.gs = gs;
+  cd.r_gs = __frcp_rn(gs);
+  cd.r_six = __frcp_rn(6.0f);
+  cd.tab = tab;
+  return cd;
+}
+
+// Bits of the largest |x| over 16 bf16 values (two vectors): bf16x2 maxima
+// of magnitudes (the sign bits they leave are cleared at the end).
+__device__ __forceinline__ uint32_t absmax16(uint4 a, uint4 b) {
+  uint32_t m0, m1, m2, m3, m4, m5, m6;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m0) : "r"(a.x), "r"(a.y));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m1) : "r"(a.z), "r"(a.w));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(b.x), "r"(b.y));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m3) : "r"(b.z), "r"(b.w));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m4) : "r"(m0), "r"(m1));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m5) : "r"(m2), "r"(m3));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m6) : "r"(m4), "r"(m5));
+  return fold16(m6 & 0x7FFF7FFFu);
+}
+
+// E2M1 codes of the 8 bf16 values of v divided by den (element 0 in the low
+// nibble).  Per pair of values x (packed FP32 arithmetic) with nr = -RN(1/den):
+//   qn = RN(x nr) = -RN(x r),  e = RN(qn den + x) = x - q den (exact),
+//   vn = RN(e nr + qn) = -RN(q + e r) = -(x / den correctly rounded),
+// Markstein's correction carried out on the negated quotient.  The E2M1
+// conversion of vn rounds to nearest even, saturates and keeps the sign of
+// values that round to zero; flipping the four sign bits of each byte then
+// gives the codes of x / den.  Signed zeros come out right: x = -0 gives
+// vn = +0 (code 0x8 after the flip), x = +0 gives vn = -0 (code 0x0), and
+// den = 0 (r = 0) gives vn = -0 * sign(x), a zero code of x's sign.
+__device__ __forceinline__ uint32_t encode8(uint4 v, uint64_t nr2, uint64_t d2) {
+  uint32_t out;
+  asm("{\n\t.reg .b64 x, qn, e, vn;\n\t.reg .f32 lo, hi;\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b64 x, {%3, %4};\n\tmul.rn.f32x2 qn, x, %1;\n\tfma.rn.f32x2 e, qn, %2, x;\n\t"
+      "fma.rn.f32x2 vn, e, %1, qn;\n\tmov.b64 {lo, hi}, vn;\n\tcvt.rn.satfinite.e2m1x2.f32 c0, hi, lo;\n\t"
+      "mov.b64 x, {%5, %6};\n\tmul.rn.f32x2 qn, x, %1;\n\tfma.rn.f32x2 e, qn, %2, x;\n\t"
+      "fma.rn.f32x2 vn, e, %1, qn;\n\tmov.b64 {lo, hi}, vn;\n\tcvt.rn.satfinite.e2m1x2.f32 c1, hi, lo;\n\t"
+      "mov.b64 x, {%7, %8};\n\tmul.rn.f32x2 qn, x, %1;\n\tfma.rn.f32x2 e, qn, %2, x;\n\t"
+      "fma.rn.f32x2 vn, e, %1, qn;\n\tmov.b64 {lo, hi}, vn;\n\tcvt.rn.satfinite.e2m1x2.f32 c2, hi, lo;\n\t"
+      "mov.b64 x, {%9, %10};\n\tmul.rn.f32x2 qn, x, %1;\n\tfma.rn.f32x2 e, qn, %2, x;\n\t"
+      "fma.rn.f32x2 vn, e, %1, qn;\n\tmov.b64 {lo, hi}, vn;\n\tcvt.rn.satfinite.e2m1x2.f32 c3, hi, lo;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(out)
+      : "l"(nr2), "l"(d2), "f"(lo_bf16(v.x)), "f"(hi_bf16(v.x)), "f"(lo_bf16(v.y)),
+        "f"(hi_bf16(v.y)), "f"(lo_bf16(v.z)), "f"(hi_bf16(v.z)), "f"(lo_bf16(v.w)), "f"(hi_bf16(v.w)));
+  return out ^ 0x88888888u;
+}
+
+__device__ __forceinline__ uint64_t pair_f32(float a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(a));
+  return r;
 }
 
 // Quantize one 16-element block held in two vectors.
-__device__ __forceinline__ void quantize_block(uint4 a, uint4 b, const Scales& sc, uint32_t& sbyte,
+__device__ __forceinline__ void quantize_block(uint4 a, uint4 b, const Codec& cd, uint32_t& sbyte,
                                                uint2& codes) {
-  const uint32_t m = fold16(__vmaxu2(absmax8(a), absmax8(b)));
-  const float bamax = __uint_as_float(m << 16);
-  const float s = div_rn(div_rn(bamax, 6.0f, sc.r_six), sc.gs, sc.r_gs);  // (bamax / 6) / gs
+  const float bamax = __uint_as_float(absmax16(a, b) << 16);
+  const float s = div_rn(div_rn(bamax, 6.0f, cd.r_six), cd.gs, cd.r_gs);  // (bamax / 6) / gs
   sbyte = e4m3_encode(s);
-  const float den = __fmul_rn(e4m3_decode(sbyte), sc.gs);
-  const float r = den == 0.0f ? 0.0f : __frcp_rn(den);
-  codes = make_uint2(encode8(a, r, den), encode8(b, r, den));
+  const float2 t = cd.tab[sbyte];  // {den, RN(1 / den)}
+  const uint64_t nr2 = pair_f32(-t.y), d2 = pair_f32(t.x);
+  codes = make_uint2(encode8(a, nr2, d2), encode8(b, nr2, d2));
 }
 
 // ---------------------------------------------------------------- quantize
@@ -249,33 +271,41 @@ __global__ void __launch_bounds__(kThreads, 4)
                     uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                     const float* __restrict__ gs_ptr) {
   ptx::pdl_launch_dependents();
+  __shared__ float2 tab[128];
+  const float gs = __ldg(gs_ptr);
+  fill_codec(tab, gs);
+  __syncthreads();
   const int64_t total = rows * bpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t0 >= total) return;
-  const Scales sc = make_scales(gs_ptr);
+  const Codec sc = make_codec(gs, tab);
   if (ld == bpr * 16) {  // contiguous rows: one flat index
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     uint2* qv = reinterpret_cast<uint2*>(q);
+    const uint64_t pol = l2_policy_first();
     int64_t b = total - 1 - t0;
-    for (; b - stride >= 0; b -= 2 * stride) {
-      const int64_t b2 = b - stride;
-      const uint4 a0 = __ldcs(xv + 2 * b), a1 = __ldcs(xv + 2 * b + 1);
-      const uint4 c0 = __ldcs(xv + 2 * b2), c1 = __ldcs(xv + 2 * b2 + 1);
-      uint32_t s0, s1;
-      uint2 k0, k1;
-      quantize_block(a0, a1, sc, s0, k0);
-      quantize_block(c0, c1, sc, s1, k1);
-      __stcs(qv + b, k0);
-      __stcs(qv + b2, k1);
-      sf[b] = static_cast<uint8_t>(s0);
-      sf[b2] = static_cast<uint8_t>(s1);
+    for (; b - 3 * stride >= 0; b -= 4 * stride) {  // four blocks (8 loads) in flight
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        v[2 * u] = ld_policy(xv + 2 * (b - u * stride), pol);
+        v[2 * u + 1] = ld_policy(xv + 2 * (b - u * stride) + 1, pol);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t s0;
+        uint2 k0;
+        quantize_block(v[2 * u], v[2 * u + 1], sc, s0, k0);
+        qv[b - u * stride] = k0;
+        sf[b - u * stride] = static_cast<uint8_t>(s0);
+      }
     }
-    if (b >= 0) {
+    for (; b >= 0; b -= stride) {
       uint32_t s0;
       uint2 k0;
-      quantize_block(__ldcs(xv + 2 * b), __ldcs(xv + 2 * b + 1), sc, s0, k0);
-      __stcs(qv + b, k0);
+      quantize_block(ld_policy(xv + 2 * b, pol), ld_policy(xv + 2 * b + 1, pol), sc, s0, k0);
+      qv[b] = k0;
       sf[b] = static_cast<uint8_t>(s0);
     }
     return;
@@ -332,12 +362,16 @@ __global__ void __launch_bounds__(kThreads, 4)
                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                  const float* __restrict__ gs_ptr) {
   ptx::pdl_launch_dependents();
+  __shared__ float2 tab[128];
+  const float gs = __ldg(gs_ptr);
+  fill_codec(tab, gs);
+  __syncthreads();
   const int64_t cpr = inter / 16;  // 32-element input chunks per row
   const int64_t total = rows * cpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t0 >= total) return;
-  const Scales sc = make_scales(gs_ptr);
+  const Codec sc = make_codec(gs, tab);
   const int64_t b0 = total - 1 - t0;
   int64_t r = b0 / cpr, c = b0 % cpr;
   const int64_t sr = stride / cpr, scol = stride % cpr;
@@ -405,6 +439,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t red[kOnePassThreads / 32];
   __shared__ float gs_sh;
+  __shared__ float2 tab[128];
   const int64_t total = rows * upr;
   const int64_t u0 = static_cast<int64_t>(blockIdx.x) * units_per_cta;
   const int64_t u1 = u0 + units_per_cta < total ? u0 + units_per_cta : total;
@@ -496,10 +531,9 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
     if (blockIdx.x == 0) gs_out[0] = gs;
   }
   __syncthreads();
-  Scales sc;
-  sc.gs = gs_sh;
-  sc.r_gs = __frcp_rn(sc.gs);
-  sc.r_six = __frcp_rn(6.0f);
+  fill_codec(tab, gs_sh);
+  __syncthreads();
+  const Codec sc = make_codec(gs_sh, tab);
   for (int64_t i = threadIdx.x; i < (late_load ? 0 : n_units); i += kOnePassThreads) {
     const int64_t u = u0 + i;
     if constexpr (G == 0) {
@@ -815,7 +849,11 @@ __global__ void __launch_bounds__(kRmsThreads)
   ptx::pdl_launch_dependents();
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nb = static_cast<int>(cols / 16);
-  const Scales sc = make_scales(gs_ptr);
+  __shared__ float2 tab[128];
+  const float gs = __ldg(gs_ptr);
+  fill_codec(tab, gs);
+  __syncthreads();
+  const Codec sc = make_codec(gs, tab);
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
   for (int64_t r = gw; r < rows; r += nw) {
@@ -850,6 +888,7 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t red[kOnePassThreads / 32];
   __shared__ float gs_sh;
+  __shared__ float2 tab[128];
   constexpr int kWarpsOp = kOnePassThreads / 32;
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nb = static_cast<int>(cols / 16);
@@ -934,10 +973,9 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
     if (blockIdx.x == 0) gs_out[0] = gs;
   }
   __syncthreads();
-  Scales sc;
-  sc.gs = gs_sh;
-  sc.r_gs = __frcp_rn(sc.gs);
-  sc.r_six = __frcp_rn(6.0f);
+  fill_codec(tab, gs_sh);
+  __syncthreads();
+  const Codec sc = make_codec(gs_sh, tab);
   const uint4* sv = reinterpret_cast<const uint4*>(data);
   const int64_t n_blocks = n_rows_live * nb;
   for (int64_t i = threadIdx.x; i < n_blocks; i += kOnePassThreads) {
