@@ -134,6 +134,7 @@ struct Params {
   int large;              // reduce path: rows through shared-memory keys (k > 32 or N > 512)
   int cand_cap;           // large path: power of two >= k
   uint32_t row_bytes;     // large path: bytes of one warp's key buffer (16-byte multiple)
+  int vec_out;            // outputs 16-byte aligned (k == 8 rows take vector stores)
 };
 
 // Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1), E4M3
@@ -246,12 +247,36 @@ __device__ __forceinline__ void list_store(const Params& p, int64_t grow, const 
     for (int i = 0; i < KMAX; ++i)
       if (i < p.k && ti[i] >= 0) sum += tw[i];
   }
+  float wv[KMAX];
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) wv[i] = tw[i];
+  if (p.epilogue == NVFP4_EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM && sum > 0.0f) {
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i)
+      if (ti[i] >= 0) wv[i] = tw[i] / sum;
+  }
+  if (KMAX == 8 && p.k == 8 && p.vec_out) {
+    // a row's eight outputs of each kind are 32 contiguous bytes: two
+    // 16-byte stores each instead of eight scalar ones
+    int4* ip = reinterpret_cast<int4*>(p.topk_idx + o);
+    float4* sp = reinterpret_cast<float4*>(p.topk_score + o);
+    ip[0] = make_int4(ti[0], ti[1], ti[2], ti[3]);
+    ip[1] = make_int4(ti[4], ti[5], ti[6], ti[7]);
+    sp[0] = make_float4(tv[0], tv[1], tv[2], tv[3]);
+    sp[1] = make_float4(tv[4], tv[5], tv[6], tv[7]);
+    if (p.topk_weight) {
+      float4* wp = reinterpret_cast<float4*>(p.topk_weight + o);
+      wp[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
+      wp[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) {
     if (i < p.k) {  // empty slots hold -1 / -inf / 0 already
       p.topk_idx[o + i] = ti[i];
       p.topk_score[o + i] = tv[i];
-      if (p.topk_weight) p.topk_weight[o + i] = sum > 0.0f && ti[i] >= 0 ? tw[i] / sum : tw[i];
+      if (p.topk_weight) p.topk_weight[o + i] = wv[i];
     }
   }
 }
@@ -1076,10 +1101,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(xdrain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
     }
     __syncwarp();
-    if (!p.direct && p.epilogue != NVFP4_EPILOGUE_IDENTITY) {
-      // The row phase reads every bias of the row: stage them while the MMAs run.
+    if (p.epilogue != NVFP4_EPILOGUE_IDENTITY) {
+      // The epilogue reads every bias of its columns (the row phase of the
+      // reduce path: all N; the direct path: this CTA's): stage them while
+      // the MMAs run.
       float* bias_s = reinterpret_cast<float*>(rowmem + p.bias_off);
-      for (int n = (warp - 2) * 32 + static_cast<int>(lane); n < p.N; n += 128) bias_s[n] = __ldg(p.bias + n);
+      if (p.direct) {
+        for (int c = (warp - 2) * 32 + static_cast<int>(lane); c < ncols; c += 128) bias_s[c] = __ldg(p.bias + n0 + c);
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four scale warps read all of them
+      } else {
+        for (int n = (warp - 2) * 32 + static_cast<int>(lane); n < p.N; n += 128) bias_s[n] = __ldg(p.bias + n);
+      }
     }
     if (warp_wait(tfull_bar, 0, abort)) {
       acc_ready = true;
@@ -1100,82 +1132,212 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ti[KMAX];
       list_init<KMAX>(tv, ti, tw);
       const bool router = p.epilogue != NVFP4_EPILOGUE_IDENTITY;
-      // This warp's copy of the bias of the CTA's columns (stage region is free now).
-      float* bias_s = reinterpret_cast<float*>(smem) + (warp - 2) * BN;
-      if (router)
-        for (int c = lane; c < ncols; c += 32) bias_s[c] = __ldg(p.bias + n0 + c);
-      __syncwarp();
+      const float* bias_s = reinterpret_cast<const float*>(rowmem + p.bias_off);  // staged during the main loop
       const bool live = row < vr;
       if constexpr (KMAX == 8) {
-        // Branch-free: 32-bit keys (the score key's top 24 bits | 255 - local
-        // column), each 32-column chunk sorted in groups of 8 and merged into
-        // the running best 8.  The logits stay in shared memory (row stride
-        // BN + 4 floats) so the picks get their exact scores afterwards; keys
-        // closer than 2^-15 relative may trade places at the boundary (a
-        // near-tie), equal scores still go to the lower column.
+        // The logits stay in shared memory (row stride BN + 4 floats).
         float* zrow = reinterpret_cast<float*>(smem) + 4 * BN + row * (BN + 4);
-        uint32_t top[8];
+        if (router) {
+          // Router: only the top 8 of f(z) + bias[n], f = sqrt(softplus),
+          // matter, and f is increasing.  At least 8 columns have a logit
+          // >= zlo = the 8th largest of the two largest logits of each
+          // 16-column group, so the 8th best score is >= f(zlo) + min(bias);
+          // a column can reach it only if f(z) >= f(zlo) - (max(bias) -
+          // min(bias)).  That bound (less a safety margin for the
+          // approximate functions) gives a logit threshold; the few columns
+          // above it are scored exactly, eight at a time (independent
+          // exponentials and logarithms overlap), and kept in a sorted list
+          // in column order, so equal scores keep the lower column.  No
+          // column that can be selected is skipped, so the result equals
+          // scoring every column.
+          float blo = __int_as_float(0x7F800000), bhi = -__int_as_float(0x7F800000);
+          for (int c = lane; c < ncols; c += 32) {
+            blo = fminf(blo, bias_s[c]);
+            bhi = fmaxf(bhi, bias_s[c]);
+          }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) top[i] = 0u;
-        if (acc_ready) {
-          for (int c0 = 0; c0 < mma_n; c0 += 32) {
-            float b[32];  // the chunk's biases (one broadcast vector load per 4)
+          for (int o = 16; o > 0; o >>= 1) {
+            blo = fminf(blo, __shfl_xor_sync(0xFFFFFFFFu, blo, o));
+            bhi = fmaxf(bhi, __shfl_xor_sync(0xFFFFFFFFu, bhi, o));
+          }
+          float gtop[8];  // the 8 largest of the groups' two largest logits, descending
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 b4 = router ? *reinterpret_cast<const float4*>(bias_s + c0 + 4 * q4)
-                                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-              b[4 * q4] = b4.x;
-              b[4 * q4 + 1] = b4.y;
-              b[4 * q4 + 2] = b4.z;
-              b[4 * q4 + 3] = b4.w;
-            }
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
-            tmem_wait_ld();
-            uint32_t key[4][8];
+          for (int i = 0; i < 8; ++i) gtop[i] = -__int_as_float(0x7F800000);
+          if (acc_ready) {
+            for (int c0 = 0; c0 < mma_n; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+              tmem_wait_ld();
+              float h[2][2];  // per 16-column group: largest, second largest
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float z = __uint_as_float(v[j]) * gab;
-              v[j] = __float_as_uint(z);
-              if (p.logits != nullptr && live && c0 + j < ncols)
-                p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
-              const float sc = router ? router_weight(z) + b[j] : z;
-              key[j >> 3][j & 7] = (live && c0 + j < ncols)
-                                       ? ((float_key(sc) & 0xFFFFFF00u) | (255u - static_cast<uint32_t>(c0 + j)))
-                                       : 0u;
-            }
+              for (int g = 0; g < 2; ++g) h[g][0] = h[g][1] = -__int_as_float(0x7F800000);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              sort8_desc(key[g]);
-              merge_top8(top, key[g]);
-            }
-            if (live) {
-              const uint32_t dst = smem_addr(zrow + c0);
+              for (int j = 0; j < 32; ++j) {
+                const float z = __uint_as_float(v[j]) * gab;
+                v[j] = __float_as_uint(z);
+                if (p.logits != nullptr && live && c0 + j < ncols)
+                  p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
+                const float zv = c0 + j < ncols ? z : -__int_as_float(0x7F800000);
+                float(&hg)[2] = h[j >> 4];
+                hg[1] = fmaxf(hg[1], fminf(hg[0], zv));
+                hg[0] = fmaxf(hg[0], zv);
+              }
+              // insert the four into the running 8 (a compare-exchange chain each)
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                st_shared_v4(dst + 16 * q4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+              for (int g = 0; g < 4; ++g) {
+                float x = h[g >> 1][g & 1];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float hi = fmaxf(gtop[i], x);
+                  x = fminf(gtop[i], x);
+                  gtop[i] = hi;
+                }
+              }
+              if (live) {
+                const uint32_t dst = smem_addr(zrow + c0);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                  st_shared_v4(dst + 16 * q4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+              }
             }
           }
-        }
-        // exact score and weight of each pick, then an exact sort (score
-        // descending, lower column first)
-        uint64_t e[8];
-        float ew[8];
+          // logit threshold: f^-1(y) = softplus^-1(y^2) = log(exp(y^2) - 1), with
+          // margins far above the functions' approximation error (a lower
+          // threshold only admits more candidates)
+          float zthr = -__int_as_float(0x7F800000);
+          const float zlo = gtop[7];
+          if (zlo > -__int_as_float(0x7F800000) && zlo < __int_as_float(0x7F800000)) {
+            const float y = router_weight(zlo) - (bhi - blo);
+            if (y > 0.0f) {
+              const float ym = y - (1e-3f * y + 1e-6f);
+              const float t = ym * ym;
+              const float zt = t > 15.0f ? t : __logf(fmaxf(__expf(t) - 1.0f, 1e-30f));
+              zthr = zt - (1e-3f * fabsf(zt) + 1e-3f);
+            }
+          }
+          // candidate columns, one mask word per 32-column chunk
+          constexpr int kChunks = BN / 32;
+          uint32_t cm[kChunks];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = 255 - static_cast<int>(top[i] & 0xFFu);
-          const float z = top[i] != 0u ? zrow[c] : 0.0f;
-          const float w = router ? router_weight(z) : z;
-          const float sc = router ? w + bias_s[c] : z;
-          e[i] = top[i] != 0u ? entry(sc, n0 + c) : 0ull;
-          ew[i] = top[i] != 0u ? w : 0.0f;
-        }
-        sort8_pay(e, ew);
+          for (int ci = 0; ci < kChunks; ++ci) {
+            const int c0 = 32 * ci;
+            uint32_t m = 0u;
+            if (acc_ready && live && c0 < mma_n) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          tv[i] = e[i] != 0ull ? entry_score(e[i]) : -__int_as_float(0x7F800000);
-          ti[i] = e[i] != 0ull ? entry_col(e[i]) : -1;
-          tw[i] = ew[i];
+              for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 z4 = *reinterpret_cast<const float4*>(zrow + c0 + 4 * q4);
+                m |= (z4.x >= zthr ? 1u : 0u) << (4 * q4);
+                m |= (z4.y >= zthr ? 1u : 0u) << (4 * q4 + 1);
+                m |= (z4.z >= zthr ? 1u : 0u) << (4 * q4 + 2);
+                m |= (z4.w >= zthr ? 1u : 0u) << (4 * q4 + 3);
+              }
+              if (c0 + 32 > ncols) m &= ncols - c0 >= 32 ? 0xFFFFFFFFu : ((1u << (ncols - c0)) - 1u);
+            }
+            cm[ci] = m;
+          }
+          // rounds of up to eight candidates: exact scores as (score, column)
+          // keys, sorted and merged into the best eight by networks
+          uint64_t best[8];
+          float bw[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            best[i] = 0ull;
+            bw[i] = 0.0f;
+          }
+          auto any_left = [&]() {
+            uint32_t o = 0u;
+#pragma unroll
+            for (int ci = 0; ci < kChunks; ++ci) o |= cm[ci];
+            return o != 0u;
+          };
+          while (any_left()) {
+            int cb[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              // lowest set bit of the first non-empty word (selects only: the
+              // words stay in registers)
+              int sel = -1;
+#pragma unroll
+              for (int ci = kChunks - 1; ci >= 0; --ci) sel = cm[ci] != 0u ? ci : sel;
+              uint32_t w = 0u;
+#pragma unroll
+              for (int ci = 0; ci < kChunks; ++ci) w = ci == sel ? cm[ci] : w;
+              cb[q] = sel >= 0 ? 32 * sel + __ffs(w) - 1 : -1;
+#pragma unroll
+              for (int ci = 0; ci < kChunks; ++ci) cm[ci] = ci == sel ? (cm[ci] & (cm[ci] - 1u)) : cm[ci];
+            }
+            uint64_t e[8];
+            float ew[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int c = cb[q] >= 0 ? cb[q] : 0;
+              const float w = router_weight(zrow[c]);
+              e[q] = cb[q] >= 0 ? entry(w + bias_s[c], n0 + c) : 0ull;
+              ew[q] = cb[q] >= 0 ? w : 0.0f;
+            }
+            sort8_pay(e, ew);
+            merge_top8_pay(best, bw, e, ew);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            tv[i] = best[i] != 0ull ? entry_score(best[i]) : -__int_as_float(0x7F800000);
+            ti[i] = best[i] != 0ull ? entry_col(best[i]) : -1;
+            tw[i] = best[i] != 0ull ? bw[i] : 0.0f;
+          }
+        } else {
+          // Identity: branch-free 32-bit keys (the score key's top 24 bits |
+          // 255 - local column), each 32-column chunk sorted in groups of 8
+          // and merged into the running best 8; the picks then get their
+          // exact scores from the stored logits (keys closer than 2^-15
+          // relative may trade places at the boundary, a near-tie; equal
+          // scores still go to the lower column).
+          uint32_t top[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) top[i] = 0u;
+          if (acc_ready) {
+            for (int c0 = 0; c0 < mma_n; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tmem + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+              tmem_wait_ld();
+              uint32_t key[4][8];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float z = __uint_as_float(v[j]) * gab;
+                v[j] = __float_as_uint(z);
+                if (p.logits != nullptr && live && c0 + j < ncols)
+                  p.logits[static_cast<int64_t>(m0 + row) * p.N + n0 + c0 + j] = z;
+                key[j >> 3][j & 7] = (live && c0 + j < ncols)
+                                         ? ((float_key(z) & 0xFFFFFF00u) | (255u - static_cast<uint32_t>(c0 + j)))
+                                         : 0u;
+              }
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                sort8_desc(key[g]);
+                merge_top8(top, key[g]);
+              }
+              if (live) {
+                const uint32_t dst = smem_addr(zrow + c0);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                  st_shared_v4(dst + 16 * q4, v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+              }
+            }
+          }
+          // exact score of each pick, then an exact sort (score descending,
+          // lower column first)
+          uint64_t e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = 255 - static_cast<int>(top[i] & 0xFFu);
+            e[i] = top[i] != 0u ? entry(zrow[c], n0 + c) : 0ull;
+          }
+          sort8_desc(e);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            tv[i] = e[i] != 0ull ? entry_score(e[i]) : -__int_as_float(0x7F800000);
+            ti[i] = e[i] != 0ull ? entry_col(e[i]) : -1;
+            tw[i] = e[i] != 0ull ? tv[i] : 0.0f;
+          }
         }
       } else {
         const bool full_list = p.k == KMAX;  // k-th score is simply the last slot
@@ -1212,13 +1374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.n_split == 1) {
         if (row < vr) list_store<KMAX>(p, m0 + row, tv, ti, tw);
       } else if (row < vr) {
-        // push the row's list to its owner: [n slice][owned row][KMAX] x 16 bytes
+        // push the row's list to its owner: [n slice][slot][owned row] x 16
+        // bytes (consecutive rows at consecutive addresses, so the owner's
+        // threads read a slot without bank conflicts)
         const int owner = row / p.ro;
         const uint32_t dst = mapa_shared(smem_addr(rowmem), static_cast<uint32_t>(owner)) +
-                             static_cast<uint32_t>(((n_idx * p.ro + (row - owner * p.ro)) * KMAX) * 16);
+                             static_cast<uint32_t>((n_idx * KMAX * p.ro + (row - owner * p.ro)) * 16);
 #pragma unroll
         for (int i = 0; i < KMAX; ++i)
-          st_cluster_v4(dst + i * 16, __float_as_uint(tv[i]), static_cast<uint32_t>(ti[i]),
+          st_cluster_v4(dst + i * p.ro * 16, __float_as_uint(tv[i]), static_cast<uint32_t>(ti[i]),
                         __float_as_uint(tw[i]), 0u);
       }
     }
@@ -1238,7 +1402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ni = 0; ni < p.n_split; ++ni) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const uint4 q = *reinterpret_cast<const uint4*>(lists + ((ni * p.ro + t) * 8 + i) * 4);
+            const uint4 q = *reinterpret_cast<const uint4*>(lists + ((ni * 8 + i) * p.ro + t) * 4);
             const int col = static_cast<int>(q.y);
             g[i] = col >= 0 ? entry(__uint_as_float(q.x), col) : 0ull;
             gw[i] = __uint_as_float(q.z);
@@ -1271,7 +1435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ni = 0; ni < p.n_split; ++ni) {  // slices in column order: ties stay by lower n
 #pragma unroll
           for (int i = 0; i < KMAX; ++i) {
-            const uint32_t* e = lists + ((ni * p.ro + t) * KMAX + i) * 4;
+            const uint32_t* e = lists + ((ni * KMAX + i) * p.ro + t) * 4;
             const float s = __uint_as_float(e[0]);
             if (s > kth) {
               list_insert<KMAX>(tv, ti, tw, s, static_cast<int>(e[1]), __uint_as_float(e[2]));
@@ -1534,7 +1698,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
     if (pl.large)
       extra += pl.row_bytes + static_cast<size_t>(pl.cand_cap) * 8 + 256;  // keys, candidates, block scratch
     pl.bias_off = static_cast<uint32_t>(extra);
-    if (!pl.direct) extra += static_cast<size_t>((N * 4 + 15) & ~15);  // staged biases
+    extra += pl.direct ? static_cast<size_t>(pl.bn) * 4 : static_cast<size_t>((N * 4 + 15) & ~15);  // staged biases
     return 1024 + static_cast<size_t>(region) + kCtrlBytes + extra;
   };
   pl.bulk = pl.direct ? 0 : 1;
@@ -1764,6 +1928,10 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.large = pl.large;
   p.cand_cap = pl.cand_cap;
   p.row_bytes = pl.row_bytes;
+  {
+    const auto a16 = [](const void* q) { return q == nullptr || reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    p.vec_out = (a.k == 8 && a16(a.topk_idx) && a16(a.topk_score) && a16(a.topk_weight)) ? 1 : 0;
+  }
   const int grid = static_cast<int>((a.M + pl.rpc - 1) / pl.rpc) * pl.n_split * pl.k_split;
   const cudaError_t e = launch(pl, ma, mb, msa, msb, p, grid, stream);
   if (e != cudaSuccess) {

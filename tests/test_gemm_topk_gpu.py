@@ -215,3 +215,48 @@ def test_empty_rows_is_a_no_op(nv, ws):
     idx, score, _, _ = nv.gemm_topk(z8, zs, g, qb, sfb, g, 0, None, 4, ws)
     torch.cuda.synchronize()
     assert idx.shape == (0, 4)
+
+
+# The router epilogue of the direct path scores only the columns whose logit
+# can still reach the top 8 (a threshold from the logits and the spread of
+# the biases).  These cases drive that threshold to its ends: biases wide
+# enough that nothing is filtered, biases so narrow that only the top logits
+# survive, a ragged last column tile, logits far into both tails of softplus,
+# and exact ties (duplicate gate rows with equal biases).
+FILTER = [
+    # M, N, K, bias_std, weight_std
+    (5120, 256, 256, 1.0, 0.05),
+    (5120, 256, 256, 1e-4, 0.05),
+    (5120, 200, 512, 0.01, 0.05),
+    (5120, 256, 256, 0.01, 3.0),
+]
+
+
+@pytest.mark.parametrize("M,N,K,bstd,wstd", FILTER)
+def test_router_candidate_filter(nv, ws, M, N, K, bstd, wstd):
+    rng = np.random.default_rng(M + N + int(K * wstd))
+    xa = workloads.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    xb = workloads.bf16_bits((rng.standard_normal((N, K)) * wstd).astype(np.float32))
+    bias = (rng.standard_normal(N) * bstd).astype(np.float32)
+    qa, sfa, gsa = quantized(xa)
+    qb, sfb, gsb = quantized(xb)
+    rows = sorted(set(range(0, 64)) | set(range(M - 64, M)) | set(rng.integers(0, M, 128).tolist()))
+    check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, 1, bias, 8, rows=rows,
+               what=f"filter {M}x{N}x{K} bias {bstd} w {wstd}")
+
+
+def test_router_candidate_filter_exact_ties(nv, ws):
+    rng = np.random.default_rng(17)
+    M, K = 5120, 256
+    base = workloads.bf16_bits((rng.standard_normal((32, K)) * 0.05).astype(np.float32))
+    xb = np.concatenate([base] * 8)  # N = 256: each gate row 8 times
+    bias = np.tile((rng.standard_normal(32) * 0.01).astype(np.float32), 8)
+    xa = workloads.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    qa, sfa, gsa = quantized(xa)
+    qb, sfb, gsb = quantized(xb)
+    rows = list(range(0, 48)) + list(range(M - 16, M))
+    idx, score = check_case(nv, ws, qa, sfa, gsa, qb, sfb, gsb, 1, bias, 8, rows=rows, what="router ties")
+    for r in rows:
+        same = np.diff(score[r]) == 0
+        assert same.any()
+        assert (np.diff(idx[r])[same] > 0).all()
