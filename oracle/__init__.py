@@ -69,6 +69,8 @@ def _load():
             "orc_normalize_topk_weights": (None, [P, P, I64, ctypes.c_int]),
             "orc_rmsnorm": (None, [P, I64, I64, I64, P, F, P]),
             "orc_rms_sum_of_squares": (None, [P, I64, I64, I64, P]),
+            "orc_mhc_mix": (None, [P, I64, I64, I64, I64, P, P]),
+            "orc_mhc_rmsnorm_quantize": (None, [P, I64, I64, I64, I64, P, P, F, P, P, P]),
             "orc_indexer_scores": (None, [P, P, F, P, P, F, I64, I64, I64, I64, P, P]),
             "orc_rmsnorm_quantize": (None, [P, I64, I64, I64, P, F, P, P, P]),
             "orc_gemm_topk_rows": (None, [P, P, F, P, P, F, I64, I64, ctypes.c_int, P,
@@ -253,6 +255,30 @@ def rmsnorm_quantize(x: np.ndarray, weight: np.ndarray, eps: float):
     sf = np.zeros((rows, cols // 16), np.uint8)
     gs = np.zeros(1, np.float32)
     _load().orc_rmsnorm_quantize(_ptr(x), rows, cols, cols, _ptr(w), float(eps), _ptr(q), _ptr(sf), _ptr(gs))
+    return q, sf, gs[0]
+
+
+def mhc_mix(x: np.ndarray, a: np.ndarray) -> np.ndarray:
+    """bf16 bits of the mHC layer input: x [T, n_hc, d] bf16 bits, a [T, n_hc] bf16 bits."""
+    x = _c(x, np.uint16)
+    a = _c(a, np.uint16)
+    T, n, d = x.shape
+    out = np.zeros((T, d), np.uint16)
+    _load().orc_mhc_mix(_ptr(x), T, n, d, n * d, _ptr(a), _ptr(out))
+    return out
+
+
+def mhc_rmsnorm_quantize(x: np.ndarray, a: np.ndarray, weight: np.ndarray, eps: float):
+    """The fused op: mHC pre-mix, RMSNorm * weight, NVFP4 quantize -> (codes, scales, gs)."""
+    x = _c(x, np.uint16)
+    a = _c(a, np.uint16)
+    w = _c(weight, np.uint16)
+    T, n, d = x.shape
+    q = np.zeros((T, d // 2), np.uint8)
+    sf = np.zeros((T, d // 16), np.uint8)
+    gs = np.zeros(1, np.float32)
+    _load().orc_mhc_rmsnorm_quantize(_ptr(x), T, n, d, n * d, _ptr(a), _ptr(w), float(eps), _ptr(q), _ptr(sf),
+                                     _ptr(gs))
     return q, sf, gs[0]
 
 

@@ -295,6 +295,40 @@ void orc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t
   orc_quantize(tmp.data(), rows, cols, cols, q, sf, gs_out);
 }
 
+// The mHC layer input of each token: the mix of its n_hc residual streams
+// by the token's input mapping A_l (compare view: mhc.py, the mHCLayer
+// docstring "x_in, ctx = mhc.pre_block(X_l)" with X_l of shape (T, n_hc, d),
+// and _dynamic_params, "A_l: (T, n_hc) sigmoid-constrained input mapping",
+// returned as bf16; FINAL_STRETCH.md / PERFORMANCE_AUDIT.md P5 fuse this
+// pre_block with the RMSNorm and the NVFP4 quantize).  The pages do not print
+// pre_block's body; the reading taken: x_in[t, c] = sum_i A[t, i] X[t, i, c]
+// accumulated in FP32 over the streams in index order (each bf16 x bf16
+// product is exact in FP32, so only the additions round), rounded to bf16.
+// x: token t's stream i is the row of cols elements at x + t * ld + i * cols.
+void orc_mhc_mix(const uint16_t* x, int64_t rows, int64_t n_hc, int64_t cols, int64_t ld,
+                 const uint16_t* a, uint16_t* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      float acc = 0.0f;
+      for (int64_t i = 0; i < n_hc; ++i) {
+        const float prod = bf16_value(a[r * n_hc + i]) * bf16_value(x[r * ld + i * cols + c]);  // exact
+        acc = (i == 0) ? prod : acc + prod;
+      }
+      out[r * cols + c] = bf16_round(acc);
+    }
+}
+
+// mHC pre-mix, then RMSNorm (orc_rmsnorm), then quantize: the fused op.
+void orc_mhc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t n_hc, int64_t cols, int64_t ld,
+                              const uint16_t* a, const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf,
+                              float* gs_out) {
+  std::vector<uint16_t> mixed(static_cast<size_t>(rows * cols));
+  orc_mhc_mix(x, rows, n_hc, cols, ld, a, mixed.data());
+  std::vector<uint16_t> normed(static_cast<size_t>(rows * cols));
+  orc_rmsnorm(mixed.data(), rows, cols, cols, weight, eps, normed.data());
+  orc_quantize(normed.data(), rows, cols, cols, q, sf, gs_out);
+}
+
 // Deinterleave one [rows, 2I] matrix whose gate/up columns alternate in
 // groups of g: output column j < I is gate column j, taken from input column
 // 2g*floor(j/g) + (j mod g); output column I + j is up column j, taken from

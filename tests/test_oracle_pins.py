@@ -644,3 +644,55 @@ def test_grouped_swiglu_interleaved_layout():
     assert np.all(np.abs(got - h) <= 2.0 ** -8 * np.abs(h) + 1e-300)
     got_a = bf16_to_f32(de[:, :I]).astype(np.float64)
     assert np.all(np.abs(got_a - a) <= 2.0 ** -8 * np.abs(a) + 1e-300)
+
+
+# ---- mHC pre-mix of the residual streams, fused with RMSNorm + quantize
+
+def test_mhc_single_stream_with_unit_mapping_is_rmsnorm_quantize():
+    # n_hc = 1 and A = 1: the mix is the stream itself, so the fused op is
+    # exactly the pinned RMSNorm + quantize
+    rng = np.random.default_rng(51)
+    x = bf16_bits(rng.standard_normal((5, 1, 512)).astype(np.float32))
+    a = _bf16(np.ones((5, 1)))
+    w = bf16_bits((1.0 + 0.1 * rng.standard_normal(512)).astype(np.float32))
+    got = oracle.mhc_rmsnorm_quantize(x, a, w, 1e-6)
+    want = oracle.rmsnorm_quantize(x[:, 0, :], w, 1e-6)
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1]) and got[2] == want[2]
+
+
+def test_mhc_mix_on_an_exact_grid():
+    # streams and mapping on a grid where every partial sum is exact: the mix
+    # is the exact sum_i A[t, i] X[t, i, c] (numpy float64), for any stream order
+    rng = np.random.default_rng(52)
+    T, n, d = 6, 4, 64
+    xf = rng.integers(-3, 4, (T, n, d)).astype(np.float64)
+    af = np.array([0.25, 0.5, 1.0, 2.0])[rng.integers(0, 4, (T, n))]
+    mix = bf16_to_f32(oracle.mhc_mix(_bf16(xf), _bf16(af))).astype(np.float64)
+    assert np.array_equal(mix, np.einsum("ti,tic->tc", af, xf))
+    perm = rng.permutation(n)
+    assert np.array_equal(oracle.mhc_mix(_bf16(xf[:, perm]), _bf16(af[:, perm])), oracle.mhc_mix(_bf16(xf), _bf16(af)))
+
+
+def test_mhc_mix_rounds_in_stream_order():
+    # the reading: FP32 accumulation over the streams in index order, then bf16.
+    # 2^24 + 1 rounds to 2^24 (ties to even), so the sum of (2^24, 1, -2^24)
+    # is 0 in that order, although the exact sum is 1
+    x = _bf16(np.array([[[2.0 ** 24] * 16, [1.0] * 16, [-(2.0 ** 24)] * 16]]))
+    a = _bf16(np.ones((1, 3)))
+    assert (bf16_to_f32(oracle.mhc_mix(x, a)) == 0.0).all()
+    a2 = _bf16(np.array([[1.0, 1.0, 0.0]]))  # (2^24 + 1) alone rounds to 2^24 in FP32, stays 2^24 in bf16
+    assert (bf16_to_f32(oracle.mhc_mix(x, a2)) == 2.0 ** 24).all()
+
+
+def test_mhc_mapping_scaled_by_a_power_of_two_gives_the_same_codes():
+    # scaling A by 2^k scales the mix exactly; with eps = 0 RMSNorm divides the
+    # scale out exactly (the FP32 sum, mean, root and reciprocal all scale
+    # exactly), so codes, scales and the global scale are identical
+    rng = np.random.default_rng(53)
+    x = bf16_bits(rng.standard_normal((7, 4, 256)).astype(np.float32))
+    af = rng.uniform(0.2, 1.0, (7, 4))
+    w = bf16_bits((1.0 + 0.1 * rng.standard_normal(256)).astype(np.float32))
+    base = oracle.mhc_rmsnorm_quantize(x, _bf16(af), w, 0.0)
+    for k in (-3, 5):
+        got = oracle.mhc_rmsnorm_quantize(x, _bf16(af * 2.0 ** k), w, 0.0)
+        assert np.array_equal(got[0], base[0]) and np.array_equal(got[1], base[1]) and got[2] == base[2]
