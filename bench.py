@@ -594,6 +594,21 @@ def secondary(nv, ws, pk, flush):
         sweep[f"rmsnorm_T{T}"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1), hbm_frac=round(b / t / hbm, 3),
                                       l2=how)
         del x0, q, sf, gs
+    # mHC pre-mix of the 4 residual streams + RMSNorm + quantize (x_in and the
+    # normalised rows never reach HBM)
+    for T in (1, 32, 2048):
+        n_hc = 4
+        x0 = torch.from_numpy(workloads.quantize_input(T * n_hc).view(np.int16)).cuda().view(T, n_hc, HIDDEN)
+        a0 = torch.from_numpy(workloads.bf16_bits(rng.uniform(0.05, 1.0, (T, n_hc)).astype(np.float32))
+                              .view(np.int16)).cuda()
+        q, sf, gs = nv.mhc_rmsnorm_quantize(x0, a0, wn, 1e-6, ws)
+        t, how = time_op(lambda i: x0 if i == 0 else x0.clone(),
+                         lambda x: nv.nvfp4_mhc_rmsnorm_quantize(x, a0, wn, 1e-6, q, sf, gs, ws),
+                         T * n_hc * HIDDEN * 2, flush)
+        b = T * n_hc * HIDDEN * 2 + T * n_hc * 2 + HIDDEN * 2 + T * HIDDEN // 2 + T * HIDDEN // 16 + 4
+        sweep[f"mhc_rmsnorm_T{T}_nhc4"] = dict(us=round(t * 1e6, 2), gbs=round(b / t / 1e9, 1),
+                                               hbm_frac=round(b / t / hbm, 3), l2=how)
+        del x0, a0, q, sf, gs
     torch.cuda.empty_cache()
     out["quantize"] = sweep
     # indexer-shaped scoring

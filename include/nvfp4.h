@@ -11,6 +11,8 @@
  *                                output, deinterleaved to [gate | up] first
  *   nvfp4_rmsnorm_quantize       the same for RMSNorm(x) * weight, the
  *                                norm fused in
+ *   nvfp4_mhc_rmsnorm_quantize   the same for the mHC pre-mix of n_hc
+ *                                residual streams, mix and norm fused in
  *   nvfp4_gemm_topk              block-scaled FP4 GEMM with a fused scoring
  *                                epilogue and per-row top-k
  *   nvfp4_indexer_topk           the same GEMM with the indexer's weighted
@@ -171,6 +173,32 @@ int nvfp4_deinterleave_quantize(const uint16_t* x, int64_t rows, int64_t inter, 
 int nvfp4_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                            const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * mHC pre-mix, RMSNorm and the activation quantize in one op (the compare
+ * view's FINAL_STRETCH.md / PERFORMANCE_AUDIT.md P5, "fuse mHC pre_block +
+ * RMSNorm + NVFP4 quantize"; mhc.py: the layer input x_in = pre_block(X_l)
+ * of the (T, n_hc, d) residual state, with the per-token input mapping A_l
+ * of shape (T, n_hc) in bf16):
+ *
+ *   x_in[t, c] = bf16(sum_i A[t, i] * X[t, i, c])   FP32 accumulation over
+ *                the streams in index order (each product is exact in FP32;
+ *                the pages do not print pre_block's body: this is the reading)
+ *   then exactly nvfp4_rmsnorm_quantize of the [rows, cols] bf16 matrix x_in
+ *   (x_in and the normalised rows never reach memory).
+ *
+ * x      : bf16, token t's stream i is the row of cols elements at
+ *          x + t * ld_x + i * cols (streams of a token contiguous); 16-byte
+ *          aligned, ld_x a multiple of 8 and >= n_hc * cols.
+ * a      : bf16 [rows, n_hc] (2-byte aligned).   n_hc: 1 .. 8.
+ * weight : bf16 [cols], 16-byte aligned.  cols: multiple of 16, at most 8192.
+ * eps, q, sf, gs: as for nvfp4_rmsnorm_quantize.  One launch when the tokens'
+ *          streams fit in the SMs' shared memory (about 30 MB), else two
+ *          row-parallel passes (each mixes its rows again).
+ */
+int nvfp4_mhc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int n_hc, int64_t cols, int64_t ld_x,
+                               const uint16_t* a, const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf,
+                               float* gs, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Block-scaled FP4 GEMM + fused epilogue + per-row top-k.  Sources: the

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_last_cuda_error.argtypes = []
         L.nvfp4_indexer_topk.restype = I
         L.nvfp4_indexer_topk.argtypes = [P, P, P, P, P, P, I64, I, I64, I64, P, I, P, P, P, P, SZ, P]
+        L.nvfp4_mhc_rmsnorm_quantize.restype = I
+        L.nvfp4_mhc_rmsnorm_quantize.argtypes = [P, I64, I, I64, I64, P, P, ctypes.c_float, P, P, P, P, SZ, P]
         L.nvfp4_rmsnorm_quantize.restype = I
         L.nvfp4_rmsnorm_quantize.argtypes = [P, I64, I64, I64, P, ctypes.c_float, P, P, P, P, SZ, P]
         L.nvfp4_kernel_launches.restype = ctypes.c_uint64
@@ -96,7 +98,7 @@ EXPORTED_SYMBOLS = ("nvfp4_workspace_bytes", "nvfp4_workspace_init", "nvfp4_quan
                     "nvfp4_deinterleave_quantize", "nvfp4_gemm_topk", "nvfp4_read_device_status",
                     "nvfp4_status_string", "nvfp4_last_cuda_error", "nvfp4_quantize_noalloc",
                     "nvfp4_kernel_launches", "nvfp4_rmsnorm_quantize", "nvfp4_indexer_topk",
-                    "nvfp4_grouped_swiglu_gemm")
+                    "nvfp4_grouped_swiglu_gemm", "nvfp4_mhc_rmsnorm_quantize")
 
 
 def _check(fn: str, status: int):
@@ -167,6 +169,30 @@ def rmsnorm_quantize(x, weight, eps, ws, stream=None):
     sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=x.device)
     gs = torch.empty(1, dtype=torch.float32, device=x.device)
     nvfp4_rmsnorm_quantize(x, weight, eps, q, sf, gs, ws, stream)
+    return q, sf, gs
+
+
+def nvfp4_mhc_rmsnorm_quantize(x, a, weight, eps, q, sf, gs, ws, stream=None):
+    """x: bf16 [rows, n_hc, cols] (the token's streams contiguous; any token
+    stride), a: bf16 [rows, n_hc]; the mixed, normalised rows are quantized."""
+    x = _bf16_bits(x)
+    a = _bf16_bits(a)
+    weight = _bf16_bits(weight)
+    rows, n_hc, cols = x.shape
+    if x.stride(2) != 1 or x.stride(1) != cols or not a.is_contiguous():
+        raise ValueError("x must have contiguous streams of cols elements and a must be contiguous")
+    _check("nvfp4_mhc_rmsnorm_quantize", lib().nvfp4_mhc_rmsnorm_quantize(
+        _ptr(x), rows, int(n_hc), cols, x.stride(0), _ptr(a), _ptr(weight), float(eps), _ptr(q), _ptr(sf),
+        _ptr(gs), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def mhc_rmsnorm_quantize(x, a, weight, eps, ws, stream=None):
+    """Allocating convenience: (q, sf, gs) of RMSNorm(sum_i a[:, i] x[:, i]) * weight."""
+    rows, _, cols = x.shape
+    q = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=x.device)
+    gs = torch.empty(1, dtype=torch.float32, device=x.device)
+    nvfp4_mhc_rmsnorm_quantize(x, a, weight, eps, q, sf, gs, ws, stream)
     return q, sf, gs
 
 

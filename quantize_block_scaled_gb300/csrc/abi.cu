@@ -85,6 +85,24 @@ int nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, 
   return NVFP4_OK;
 }
 
+int nvfp4_mhc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int n_hc, int64_t cols, int64_t ld_x,
+                               const uint16_t* a, const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf,
+                               float* gs, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (gs == nullptr || weight == nullptr ||
+      (rows != 0 && (x == nullptr || a == nullptr || q == nullptr || sf == nullptr)))
+    return NVFP4_ERR_INVALID;
+  if (rows < 0 || n_hc < 1 || n_hc > 8 || cols <= 0 || ld_x < n_hc * cols || !(eps >= 0.0f) || eps > 3.4e38f)
+    return NVFP4_ERR_INVALID;
+  if (cols % 16 != 0 || cols > 8192 || ld_x % 8 != 0 || !aligned(x, 16) || !aligned(a, 2) ||
+      !aligned(weight, 16) || !aligned(q, 8) || !aligned(gs, 4))
+    return NVFP4_ERR_UNSUPPORTED;
+  const int st = check_workspace(ws, ws_bytes);
+  if (st != NVFP4_OK) return st;
+  const cudaError_t e = nvfp4::launch_mhc_rmsnorm_quantize(x, rows, n_hc, cols, ld_x, a, weight, eps, q, sf, gs,
+                                                           static_cast<nvfp4::Workspace*>(ws), stream);
+  return e == cudaSuccess ? NVFP4_OK : cuda_failure(e);
+}
+
 int nvfp4_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                            const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs, void* ws,
                            size_t ws_bytes, cudaStream_t stream) {

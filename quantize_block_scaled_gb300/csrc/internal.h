@@ -42,6 +42,12 @@ cudaError_t launch_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t col
                                     const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs,
                                     Workspace* ws, cudaStream_t stream);
 
+// mHC pre-mix of n_hc streams per token (x: token stride ld, streams cols
+// apart) by amap [rows, n_hc], then the same RMSNorm + quantize.
+cudaError_t launch_mhc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int n_hc, int64_t cols, int64_t ld,
+                                        const uint16_t* amap, const uint16_t* weight, float eps, uint8_t* q,
+                                        uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream);
+
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* gs,
                         Workspace* ws, cudaStream_t stream);
 

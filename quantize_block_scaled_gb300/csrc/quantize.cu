@@ -797,15 +797,59 @@ __device__ __forceinline__ uint4 rms_vec(uint4 x, uint4 w, float inv) {
                     rms_word(x.w, w.w, inv));
 }
 
+// mHC pre-mix of one token (the layer input before the norm): x_in[c] =
+// bf16(sum_i A[i] X_i[c]), FP32 accumulation over the streams in index order
+// (each bf16 product is exact in FP32).  One warp, 8 elements per lane step;
+// streams i at src + i * cols, result to dst (may alias stream 0: each lane
+// reads its own vector of every stream before it writes it).
+__device__ __forceinline__ void warp_mhc_mix(const uint16_t* src, int64_t cols, int n_hc, const uint16_t* a,
+                                             uint16_t* dst) {
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  float av[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    av[i] = 0.0f;
+    if (i < n_hc) av[i] = lo_bf16(static_cast<uint32_t>(__ldg(a + i)));
+  }
+  const int nv = static_cast<int>(cols / 8);
+  for (int v = lane; v < nv; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < n_hc) {
+        const uint4 w = reinterpret_cast<const uint4*>(src + i * cols)[v];
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p0 = __fmul_rn(av[i], lo_bf16(ww[j])), p1 = __fmul_rn(av[i], hi_bf16(ww[j]));
+          acc[2 * j] = i == 0 ? p0 : __fadd_rn(acc[2 * j], p0);
+          acc[2 * j + 1] = i == 0 ? p1 : __fadd_rn(acc[2 * j + 1], p1);
+        }
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j]))) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j + 1]))) << 16);
+    reinterpret_cast<uint4*>(dst)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  __syncwarp();
+}
+
 constexpr int kRmsThreads = 256;  // 8 warps, one row per warp at a time
 
 // Pass 1 (inputs larger than the SMs' shared memory): y's maximum |.|, then
 // gs by the last block, exactly as the amax kernel does.
+// kMix: the row is first mixed from the token's n_hc streams (mHC pre-mix)
+// into this warp's shared-memory buffer.
+template <bool kMix>
 __global__ void __launch_bounds__(kRmsThreads)
     rmsnorm_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-                        const uint16_t* __restrict__ wt, float eps, float* __restrict__ gs_out,
-                        Workspace* __restrict__ ws) {
+                        const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap, int n_hc,
+                        float* __restrict__ gs_out, Workspace* __restrict__ ws) {
   ptx::pdl_launch_dependents();
+  extern __shared__ __align__(16) uint16_t mixbuf[];
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nb = static_cast<int>(cols / 16);
   uint32_t m2 = 0;
@@ -813,6 +857,10 @@ __global__ void __launch_bounds__(kRmsThreads)
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
   for (int64_t r = gw; r < rows; r += nw) {
     const uint16_t* xr = x + r * ld;
+    if constexpr (kMix) {
+      warp_mhc_mix(xr, cols, n_hc, amap + r * n_hc, mixbuf + warp * cols);
+      xr = mixbuf + warp * cols;
+    }
     const float inv = warp_inv_rms(xr, cols, eps);
     for (int b = lane; b < nb; b += 32) {
       const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
@@ -842,11 +890,14 @@ __global__ void __launch_bounds__(kRmsThreads)
 }
 
 // Pass 2: recompute each row's inv_rms (same order, same value) and quantize y.
+template <bool kMix>
 __global__ void __launch_bounds__(kRmsThreads)
     rmsnorm_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-                            const uint16_t* __restrict__ wt, float eps, uint8_t* __restrict__ q,
-                            uint8_t* __restrict__ sf, const float* __restrict__ gs_ptr) {
+                            const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap,
+                            int n_hc, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                            const float* __restrict__ gs_ptr) {
   ptx::pdl_launch_dependents();
+  extern __shared__ __align__(16) uint16_t mixbuf[];
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nb = static_cast<int>(cols / 16);
   __shared__ float2 tab[128];
@@ -858,6 +909,10 @@ __global__ void __launch_bounds__(kRmsThreads)
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
   for (int64_t r = gw; r < rows; r += nw) {
     const uint16_t* xr = x + r * ld;
+    if constexpr (kMix) {
+      warp_mhc_mix(xr, cols, n_hc, amap + r * n_hc, mixbuf + warp * cols);
+      xr = mixbuf + warp * cols;
+    }
     const float inv = warp_inv_rms(xr, cols, eps);
     for (int b = lane; b < nb; b += 32) {
       const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
@@ -877,12 +932,15 @@ __global__ void __launch_bounds__(kRmsThreads)
 // CTAs exchange maxima as in quantize_onepass_kernel (one cluster, or a
 // cooperative grid meeting at the workspace counter), then each CTA
 // quantizes its rows from shared memory.
-template <bool kCluster>
+// kMix: each token's n_hc streams are copied on chip and mixed (mHC
+// pre-mix) into the first stream's buffer before the norm.
+template <bool kCluster, bool kMix>
 __global__ void __launch_bounds__(kOnePassThreads, 1)
     rmsnorm_quantize_onepass_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-                                    const uint16_t* __restrict__ wt, float eps, int64_t rows_per_cta,
-                                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                    float* __restrict__ gs_out, Workspace* __restrict__ ws) {
+                                    const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap,
+                                    int n_hc, int64_t rows_per_cta, uint8_t* __restrict__ q,
+                                    uint8_t* __restrict__ sf, float* __restrict__ gs_out,
+                                    Workspace* __restrict__ ws) {
   ptx::pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar;
@@ -895,7 +953,8 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
   const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
   const int64_t n_rows = r1 > r0 ? r1 - r0 : 0;
-  const uint32_t row_bytes = static_cast<uint32_t>(cols * 2);
+  const int64_t row_elems = kMix ? n_hc * cols : cols;  // shared-memory row: the token's streams
+  const uint32_t row_bytes = static_cast<uint32_t>(row_elems * 2);
   uint16_t* data = reinterpret_cast<uint16_t*>(smem);
   const uint32_t bar_a = ptx::smem_addr(&bar);
   ptx::pdl_wait();
@@ -915,7 +974,8 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   const int64_t n_rows_live = late_load ? 0 : n_rows;
   uint32_t m2 = 0;
   for (int64_t rr = warp; rr < n_rows_live; rr += kWarpsOp) {
-    uint16_t* yr = data + rr * cols;
+    uint16_t* yr = data + rr * row_elems;
+    if constexpr (kMix) warp_mhc_mix(yr, cols, n_hc, amap + (r0 + rr) * n_hc, yr);
     const float inv = warp_inv_rms(yr, cols, eps);
     for (int b = lane; b < nb; b += 32) {
       uint4* v = reinterpret_cast<uint4*>(yr + b * 16);
@@ -981,7 +1041,9 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   for (int64_t i = threadIdx.x; i < n_blocks; i += kOnePassThreads) {
     uint32_t sbyte;
     uint2 codes;
-    quantize_block(sv[2 * i], sv[2 * i + 1], sc, sbyte, codes);
+    const int64_t rr = kMix ? i / nb : 0;
+    const int64_t vi = kMix ? rr * (row_elems / 8) + 2 * (i - rr * nb) : 2 * i;  // the normalised row's block i
+    quantize_block(sv[vi], sv[vi + 1], sc, sbyte, codes);
     const int64_t blk = r0 * nb + i;
     __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
     sf[blk] = static_cast<uint8_t>(sbyte);
@@ -1001,10 +1063,13 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
 // Launch RMSNorm + quantize: one pass when whole rows fit in the SMs'
 // shared memory (one cluster up to 512 KB, else a cooperative grid of one
 // CTA per SM), otherwise the two row-parallel passes.
-cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                                         const uint16_t* wt, float eps, uint8_t* q, uint8_t* sf, float* gs,
-                                         Workspace* ws, cudaStream_t stream) {
-  const int64_t row_bytes = cols * 2;
+// n_hc == 0: plain RMSNorm of the rows; n_hc >= 1: each row is first the
+// mHC pre-mix of the token's n_hc streams (contiguous, cols apart) by amap.
+template <bool kMix>
+cudaError_t launch_rmsnorm_quantize_t(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                      const uint16_t* wt, float eps, const uint16_t* amap, int n_hc, uint8_t* q,
+                                      uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream) {
+  const int64_t row_bytes = (kMix ? n_hc : 1) * cols * 2;  // on chip per token
   const int sms = sm_count();
   if (rows > 0) {
     const int64_t rows_cap = static_cast<int64_t>(kOnePassMaxBytes) / row_bytes;
@@ -1019,7 +1084,7 @@ cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_
       grid = (rows + per - 1) / per;
       if (grid <= cap) {
         const size_t smem = static_cast<size_t>(per * row_bytes);
-        auto kernel = cluster ? rmsnorm_quantize_onepass_kernel<true> : rmsnorm_quantize_onepass_kernel<false>;
+        auto kernel = cluster ? rmsnorm_quantize_onepass_kernel<true, kMix> : rmsnorm_quantize_onepass_kernel<false, kMix>;
         bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)) == cudaSuccess;
         if (ok && cluster)
@@ -1049,24 +1114,35 @@ cudaError_t launch_rmsnorm_quantize_impl(const uint16_t* x, int64_t rows, int64_
         }
         if (ok) {
           count_launch();
-          return cudaLaunchKernelEx(&cfg, kernel, x, rows, cols, ld, wt, eps, per, q, sf, gs, ws);
+          return cudaLaunchKernelEx(&cfg, kernel, x, rows, cols, ld, wt, eps, amap, n_hc, per, q, sf, gs, ws);
         }
         cudaGetLastError();  // fall through to the two passes
       }
     }
   }
+  // two row-parallel passes; with the mix, each warp's row goes through its
+  // own shared-memory buffer
+  const size_t mix_smem = kMix ? static_cast<size_t>(kRmsThreads / 32) * cols * 2 : 0;
   cudaError_t e = cudaSuccess;
+  if (mix_smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(rmsnorm_amax_kernel<kMix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(mix_smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(rmsnorm_quantize_kernel<kMix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(mix_smem));
+    if (e != cudaSuccess) return e;
+  }
   const int64_t warps_needed = rows > 0 ? rows : 1;
   int64_t grid = (warps_needed + kRmsThreads / 32 - 1) / (kRmsThreads / 32);
   if (grid > 4ll * sms) grid = 4ll * sms;
   count_launch();
-  rmsnorm_amax_kernel<<<static_cast<unsigned>(grid), kRmsThreads, 0, stream>>>(x, rows, cols, ld, wt, eps,
-                                                                                       gs, ws);
+  rmsnorm_amax_kernel<kMix><<<static_cast<unsigned>(grid), kRmsThreads, mix_smem, stream>>>(
+      x, rows, cols, ld, wt, eps, amap, n_hc, gs, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess || rows == 0) return e;
   count_launch();
-  rmsnorm_quantize_kernel<<<static_cast<unsigned>(grid), kRmsThreads, 0, stream>>>(x, rows, cols, ld, wt,
-                                                                                           eps, q, sf, gs);
+  rmsnorm_quantize_kernel<kMix><<<static_cast<unsigned>(grid), kRmsThreads, mix_smem, stream>>>(
+      x, rows, cols, ld, wt, eps, amap, n_hc, q, sf, gs);
   return cudaGetLastError();
 }
 
@@ -1082,7 +1158,13 @@ int grid_for(int64_t work_items, int blocks_per_sm) {
 cudaError_t launch_rmsnorm_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                                     const uint16_t* weight, float eps, uint8_t* q, uint8_t* sf, float* gs,
                                     Workspace* ws, cudaStream_t stream) {
-  return launch_rmsnorm_quantize_impl(x, rows, cols, ld, weight, eps, q, sf, gs, ws, stream);
+  return launch_rmsnorm_quantize_t<false>(x, rows, cols, ld, weight, eps, nullptr, 0, q, sf, gs, ws, stream);
+}
+
+cudaError_t launch_mhc_rmsnorm_quantize(const uint16_t* x, int64_t rows, int n_hc, int64_t cols, int64_t ld,
+                                        const uint16_t* amap, const uint16_t* weight, float eps, uint8_t* q,
+                                        uint8_t* sf, float* gs, Workspace* ws, cudaStream_t stream) {
+  return launch_rmsnorm_quantize_t<true>(x, rows, cols, ld, weight, eps, amap, n_hc, q, sf, gs, ws, stream);
 }
 
 bool launch_quantize_onepass(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,

@@ -170,3 +170,15 @@ def test_grouped_swiglu_validation(L):
     assert call(ws_bytes=64) == 3
     # M == 0 launches nothing and accepts NULL activations, offsets and output
     assert call(M=0, qa=0, sfa=0, offs=0, out=0) == 0
+
+
+def test_mhc_rmsnorm_quantize_validation(L):
+    P = _p(FAKE)
+    ws = _p(FAKE)
+    args = lambda rows, n, cols, ld: (P, rows, n, cols, ld, P, P, ctypes.c_float(1e-6), P, P, P, ws, 256, None)
+    assert L.nvfp4_mhc_rmsnorm_quantize(*args(4, 0, 64, 64)) == 1       # no streams
+    assert L.nvfp4_mhc_rmsnorm_quantize(*args(4, 9, 64, 9 * 64)) == 1   # more than 8 streams
+    assert L.nvfp4_mhc_rmsnorm_quantize(*args(4, 4, 64, 200)) == 1      # token stride shorter than the streams
+    assert L.nvfp4_mhc_rmsnorm_quantize(*args(4, 4, 24, 96)) == 2       # cols not a multiple of 16
+    assert L.nvfp4_mhc_rmsnorm_quantize(*args(4, 1, 8208, 8208)) == 2   # cols beyond 8192
+    assert L.nvfp4_mhc_rmsnorm_quantize(*args(4, 4, 64, 260)) == 2      # token stride not a multiple of 8
