@@ -888,6 +888,28 @@ def run_profile(kind: str, iters: int):
         wn = torch.ones(HIDDEN, dtype=torch.bfloat16, device="cuda")
         q, sf, gs = nv.rmsnorm_quantize(x, wn, 1e-6, ws)
         fns = [lambda: nv.nvfp4_rmsnorm_quantize(x, wn, 1e-6, q, sf, gs, ws)]
+    elif kind == "deinterleave2048":
+        hh = torch.from_numpy(workloads.swiglu_interleaved(2048).view(np.int16)).cuda()
+        q, sf, gs = nv.deinterleave_quantize(hh, GRAN, ws)
+        fns = [lambda: nv.nvfp4_deinterleave_quantize(hh, GRAN, q, sf, gs, ws)]
+    elif kind in ("mhc32", "mhc2048"):
+        T = 32 if kind == "mhc32" else 2048
+        x = torch.from_numpy(workloads.quantize_input(T * 4).view(np.int16)).cuda().view(T, 4, HIDDEN)
+        a = torch.full((T, 4), 0.5, dtype=torch.bfloat16, device="cuda")
+        wn = torch.ones(HIDDEN, dtype=torch.bfloat16, device="cuda")
+        q, sf, gs = nv.mhc_rmsnorm_quantize(x, a, wn, 1e-6, ws)
+        fns = [lambda: nv.nvfp4_mhc_rmsnorm_quantize(x, a, wn, 1e-6, q, sf, gs, ws)]
+    elif kind == "router384":
+        rng = np.random.default_rng(384)
+        xv = torch.from_numpy(workloads.bf16_bits(rng.standard_normal((32, HIDDEN), np.float32)).view(np.int16)).cuda()
+        wv = torch.from_numpy(workloads.bf16_bits(rng.standard_normal((384, HIDDEN), np.float32) * np.float32(0.02))
+                              .view(np.int16)).cuda()
+        bv = torch.from_numpy((rng.standard_normal(384) * 0.01).astype(np.float32)).cuda()
+        qa, sfa, gsa = nv.quantize(xv, ws)
+        qb, sfb, gsb = nv.quantize(wv, ws)
+        out = [torch.empty(32, 6, dtype=dt, device="cuda") for dt in (torch.int32, torch.float32, torch.float32)]
+        fns = [lambda: nv.nvfp4_gemm_topk(qa, sfa, gsa, qb, sfb, gsb, nv.EPILOGUE_SQRT_SOFTPLUS_BIAS_NORM, bv, 6,
+                                          *out, None, ws)]
     elif kind == "indexer_heads":
         d = workloads.indexer()
         qa, sfa, gsa = nv.quantize(torch.from_numpy(d["x"].view(np.int16)).cuda(), ws)
@@ -950,7 +972,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no decode or per-shape detail)")
     ap.add_argument("--profile", choices=("decode", "prefill", "quantize", "quantize2048", "indexer",
-                                          "indexer_heads", "rmsnorm2048", "moe_decode", "moe_prefill", "moe_small"),
+                                          "indexer_heads", "rmsnorm2048", "moe_decode", "moe_prefill", "moe_small",
+                                          "deinterleave2048", "mhc32", "mhc2048", "router384"),
                     help="run --warmup eager iterations of one workload in an NVTX range and exit")
     args = ap.parse_args()
     if args.profile:
