@@ -24,11 +24,10 @@
 //              128-byte swizzle) and of the E4M3 scale tiles (row-major
 //              boxes, K % 256 == 0) or cp.async of the scale words scattered
 //              straight into MMA layout (other K); multi-stage mbarrier ring.
-//   warp 1     MMA issuer (one thread): tcgen05.cp of the scale factors into
-//              tensor memory, then four 128 x BN x 64 kind::mxf4nvf4
+//   warp 1     MMA issuer (one thread): four 128 x BN x 64 kind::mxf4nvf4
 //              block-scaled MMAs per stage into one TMEM accumulator.
-//   warps 2-5  rearrange each stage's scale tiles into the layout
-//              tcgen05.cp 32x128b.warpx4 reads (one 128-row atom per warp).
+//   warps 2-5  write each stage's scale factors into tensor memory with
+//              tcgen05.st, each warp the lanes of its own sub-partition.
 //
 // Then one of two epilogues.
 //  Direct (no K split, k <= 32): the thread that owns TMEM lane r owns row
@@ -73,14 +72,15 @@ constexpr int BM = 128;              // MMA M: rows of A per tile
 constexpr int BKB = 128;             // bytes of a K tile per row = 256 FP4 elements
 constexpr int kThreads = 192;        // 6 warps
 constexpr int kWarps = 6;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;  // scale factors live after the (<= 256-column) accumulator
-constexpr uint32_t kSfChunk = 512;     // scales of 128 rows for one MMA (K = 64)
 constexpr uint32_t kCtrlBytes = 256;
-// control block: 3 barriers per stage and 4 more, then the TMEM address at byte 128
-static_assert((3 * kMaxStages + 4) * 8 <= 128, "barriers precede the TMEM slot");
+// control block: 3 barriers per stage and 4 more, then the TMEM address and
+// the abort flag at byte 224
+constexpr uint32_t kCtrlSlot = 224;
+static_assert((3 * kMaxStages + 4) * 8 <= kCtrlSlot, "barriers precede the TMEM slot");
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
 constexpr int kSmallCols = 16;       // reduce path, small rows: <= 16 columns per lane (N <= 512)
 
@@ -89,19 +89,18 @@ struct Layout {
   static constexpr int kAtomsB = BN / 128;
   static constexpr uint32_t kA = BM * BKB;
   static constexpr uint32_t kB = BN * BKB;
-  static constexpr uint32_t kSfaStage = BM * 16;  // TMA box of scale bytes, row-major
+  static constexpr uint32_t kSfaStage = BM * 16;  // scale bytes of the K tile, row-major (16 per row)
   static constexpr uint32_t kSfbStage = BN * 16;
-  static constexpr uint32_t kSfaMma = 4 * kSfChunk;
-  static constexpr uint32_t kSfbMma = 4 * kAtomsB * kSfChunk;
   static constexpr uint32_t offB = kA;
   static constexpr uint32_t offSfaStage = kA + kB;
   static constexpr uint32_t offSfbStage = offSfaStage + kSfaStage;
-  static constexpr uint32_t offSfaMma = offSfbStage + kSfbStage;
-  static constexpr uint32_t offSfbMma = offSfaMma + kSfaMma;
-  static constexpr uint32_t kStage = offSfbMma + kSfbMma;  // 40 KB (BN 128) / 60 KB (BN 256)
+  static constexpr uint32_t kStage = offSfbStage + kSfbStage;  // 36 KB (BN 128) / 54 KB (BN 256)
   static constexpr uint32_t kSfTmemPerStage = 16 + 16 * kAtomsB;
+  // stages whose scale columns fit in TMEM after the accumulator
+  static constexpr int kStagesMax = static_cast<int>((kTmemCols - kSfTmemBase) / kSfTmemPerStage) < kMaxStages
+                                        ? static_cast<int>((kTmemCols - kSfTmemBase) / kSfTmemPerStage)
+                                        : kMaxStages;
   static_assert(kStage % 1024 == 0, "stages must keep 1 KB alignment for the 128-byte swizzle");
-  static_assert(kSfTmemBase + kMaxStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
 };
 
 struct Params {
@@ -859,9 +858,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sfready_bar = [&](int s) { return smem_addr(&bars[2 * kMaxStages + s]); };
   const uint32_t tfull_bar = smem_addr(&bars[3 * kMaxStages]);
   const uint32_t drain_bar = smem_addr(&bars[3 * kMaxStages + 1]);
-  const uint32_t xdrain_bar = smem_addr(&bars[3 * kMaxStages + 3]);  // scale copies drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 128);
-  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + 132);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + kCtrlSlot);
+  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(ctrl + kCtrlSlot + 4);
   uint8_t* rowmem = ctrl + kCtrlBytes;
 
   const int csize = p.n_split * p.k_split;
@@ -898,11 +896,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), p.tma_sf ? 1 : 1 + 32);  // + one cp.async arrival per producer lane
       mbar_init(empty_bar(s), 1);
-      mbar_init(sfready_bar(s), 4);  // one tcgen05.commit per scale-layout warp
+      mbar_init(sfready_bar(s), 4);  // one arrival per scale warp
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
-    mbar_init(xdrain_bar, 4);
     mbar_init(smem_addr(&bars[3 * kMaxStages + 2]), 1);  // rows received by bulk copy
     *abort = 0u;
     fence_mbar_init();
@@ -978,24 +975,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!p.tma_sf) {
-        // Scale word (row r, MMA kk) goes to byte (r % 32) * 16 + (r / 32) * 4
-        // of the row's 128-row atom in chunk kk.
+        // Scale word (row r, MMA step kk) goes to byte 16 r + 4 kk, the
+        // layout of the TMA-staged scales.
         const int kw = kt * 4 + kk;
         const bool kvalid = kw < kwords;
         for (int j = 0; j < BM / 8; ++j) {
           const int r = rsub + 8 * j;
           const int ra = m0 + r;
           const bool va = kvalid && ra < p.M;
-          cp_async_4(st + L::offSfaMma + kk * kSfChunk + (r & 31) * 16 + (r >> 5) * 4,
+          cp_async_4(st + L::offSfaStage + r * 16 + kk * 4,
                      va ? p.sfa + static_cast<int64_t>(ra) * sf_ld + kw * 4 : p.sfa, va ? 4u : 0u);
         }
         for (int j = 0; j < BN / 8; ++j) {
           const int r = rsub + 8 * j;
-          const int rr = r & 127;
           const int rb = n0 + r;
           const bool vb = kvalid && rb < p.N;
-          cp_async_4(st + L::offSfbMma + kk * (L::kAtomsB * kSfChunk) + (r >> 7) * kSfChunk +
-                         (rr & 31) * 16 + (rr >> 5) * 4,
+          cp_async_4(st + L::offSfbStage + r * 16 + kk * 4,
                      vb ? p.sfb + static_cast<int64_t>(rb) * sf_ld + kw * 4 : p.sfb, vb ? 4u : 0u);
         }
         cp_async_arrive_noinc(full_bar(s));
@@ -1046,12 +1041,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ scale layout
-    // Warp 2 + u owns MMA step kk = u of every 128-row scale atom (SFA, then
-    // the SFB atoms): it lays that chunk out for tcgen05.cp, copies it into
-    // TMEM and signals the stage with a tcgen05.commit.  Four warps share the
-    // copies because each tcgen05 instruction holds its issuing warp.
-    const int u = warp - 2;
+    // ------------------------------------------------------------ scale factors
+    // The block-scaled MMA reads the scales of MMA step kk (K = 64) of a
+    // 128-row atom from 4 TMEM columns: lane l (in every 32-lane
+    // sub-partition alike) holds, in column 4 kk + c, the scale word kk of
+    // row 32 c + l.  Each of the four warps writes that pattern into its own
+    // sub-partition with tcgen05.st from registers, so the tensor pipe
+    // spends no instructions on copying scales; the MMA warp waits for the
+    // four arrivals.
+    const uint32_t lane_sel = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int i = 0; i < nk; ++i) {
       const int s = i % S;
       const uint32_t ph = (i / S) & 1;
@@ -1059,46 +1057,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) record_timeout(p.status, abort);
         break;
       }
+      // (the MMAs that read this stage's TMEM columns in the previous round
+      // have completed: full(s) of this round follows empty(s))
+      tc_fence_after();
       const uint32_t st = sbase + s * L::kStage;
-      if (p.tma_sf) {
-        // Staged row r (16 bytes: MMA words 0..3) -> chunk u gets, at offset
-        // 16 * r0, word u of rows r0, r0 + 32, r0 + 64, r0 + 96.
+      const uint32_t sf_col = tmem + lane_sel + kSfTmemBase + s * L::kSfTmemPerStage;
+      uint32_t ra[16], rb[16 * L::kAtomsB];  // in TMEM column order: SFA, then SFB
+      // staged row-major: the 16 bytes of row 32 c + l of atom a hold its
+      // scale words kk = 0..3 (SFA: column 4 kk + c; SFB atom a - 1: column
+      // 16 + 4 (kk kAtomsB + a - 1) + c)
 #pragma unroll
-        for (int a = 0; a < kUnits; ++a) {
-          const uint32_t src = a == 0 ? st + L::offSfaStage : st + L::offSfbStage + (a - 1) * 2048;
-          const uint32_t dst = a == 0 ? st + L::offSfaMma + u * kSfChunk
-                                      : st + L::offSfbMma + (u * L::kAtomsB + (a - 1)) * kSfChunk;
-          const uint32_t w0 = ld_shared_u32(src + (0 * 32 + lane) * 16 + u * 4);
-          const uint32_t w1 = ld_shared_u32(src + (1 * 32 + lane) * 16 + u * 4);
-          const uint32_t w2 = ld_shared_u32(src + (2 * 32 + lane) * 16 + u * 4);
-          const uint32_t w3 = ld_shared_u32(src + (3 * 32 + lane) * 16 + u * 4);
-          st_shared_v4(dst + lane * 16, w0, w1, w2, w3);
-        }
-        fence_proxy_async_smem();  // read by tcgen05.cp through the async proxy
-      }
-      __syncwarp();
-      if (lane == 0) {
-        // (the copies of a stage run once the MMAs of its previous round have
-        // completed: full(s) of this round follows empty(s))
-        fence_proxy_async_smem();  // scales written through the generic proxy (cp.async path)
-        tc_fence_after();
-        const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
+      for (int a = 0; a < kUnits; ++a)
 #pragma unroll
-        for (int a = 0; a < kUnits; ++a) {
-          if (a == 0)
-            tc_cp_32x128b_warpx4(sf_col + u * 4, smem_desc(st + L::offSfaMma + u * kSfChunk, 0, 128, 0));
-          else
-            tc_cp_32x128b_warpx4(sf_col + 16 + u * 4 * L::kAtomsB + (a - 1) * 4,
-                                 smem_desc(st + L::offSfbMma + (u * L::kAtomsB + (a - 1)) * kSfChunk, 0, 128, 0));
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
+          ld_shared_v4((a == 0 ? st + L::offSfaStage : st + L::offSfbStage + (a - 1) * 2048) +
+                           (c * 32 + lane) * 16, w);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (a == 0) ra[kk * 4 + c] = w[kk];
+            else rb[(kk * L::kAtomsB + (a - 1)) * 4 + c] = w[kk];
+          }
         }
-        tc_commit(sfready_bar(s));
-      }
+      tmem_st_32x32b_x16(sf_col, ra);
+      if constexpr (L::kAtomsB == 1) tmem_st_32x32b_x16(sf_col + 16, rb);
+      else tmem_st_32x32b_x32(sf_col + 16, rb);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
-    }
-    if (lane == 0) {  // every copy of this warp has completed before TMEM can be freed
-      uint32_t never = 0;
-      tc_commit(xdrain_bar);
-      if (!mbar_wait_bounded(xdrain_bar, 0, &never, kWaitLimit)) record_timeout(p.status, abort);
+      if (lane == 0) mbar_arrive(sfready_bar(s));
     }
     __syncwarp();
     if (p.epilogue != NVFP4_EPILOGUE_IDENTITY) {
@@ -1679,7 +1666,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   const uint32_t staging =
       heads ? static_cast<uint32_t>(vrow_cap_floats(pl.bn) + 4 * pl.bn) * 4u  // token rows + quarter sums
             : static_cast<uint32_t>(vr_max) * static_cast<uint32_t>(pl.bn + 4) * 4u;
-  pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
+  const int smax = pl.bn == 128 ? Layout<128>::kStagesMax : Layout<256>::kStagesMax;
+  pl.stages = nk_max < smax ? nk_max : smax;
   // After the main loop the stage region holds the direct epilogue's bias
   // copies, or the reduce epilogue's staged tile (bulk) / received partials.
   auto total = [&]() {
@@ -1705,8 +1693,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   while (pl.bulk && total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
   if (pl.bulk && total() > static_cast<size_t>(smem_optin)) {  // receive in the stage region
     pl.bulk = 0;
-    pl.stages = nk_max < kMaxStages ? nk_max : kMaxStages;
-    }
+    pl.stages = nk_max < smax ? nk_max : smax;
+  }
   while (total() > static_cast<size_t>(smem_optin) && pl.stages > 1) --pl.stages;
   pl.smem = total();
   if (pl.smem > static_cast<size_t>(smem_optin)) return false;
