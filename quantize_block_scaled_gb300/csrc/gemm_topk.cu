@@ -21,13 +21,14 @@
 //
 // Per CTA, 6 warps during the main loop:
 //   warp 0     producer: TMA loads of the A and B code tiles (128-byte rows,
-//              128-byte swizzle) and of the E4M3 scale tiles (row-major
-//              boxes, K % 256 == 0) or cp.async of the scale words scattered
-//              straight into MMA layout (other K); multi-stage mbarrier ring.
-//   warp 1     MMA issuer (one thread): four 128 x BN x 64 kind::mxf4nvf4
-//              block-scaled MMAs per stage into one TMEM accumulator.
-//   warps 2-5  write each stage's scale factors into tensor memory with
-//              tcgen05.st, each warp the lanes of its own sub-partition.
+//              128-byte swizzle) into a ring of stages of K = 512.
+//   warp 1     MMA issuer (one thread): eight 128 x BN x 64 kind::mxf4nvf4
+//              block-scaled MMAs per stage into one TMEM accumulator, one
+//              commit per stage.
+//   warps 2-5  load each stage's E4M3 scale words from global memory and
+//              write them into tensor memory with tcgen05.st, each warp the
+//              lanes of its own sub-partition, as soon as the stage's
+//              columns are free.
 //
 // Then one of two epilogues.
 //  Direct (no K split, k <= 32): the thread that owns TMEM lane r owns row
@@ -69,10 +70,12 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128;              // MMA M: rows of A per tile
-constexpr int BKB = 128;             // bytes of a K tile per row = 256 FP4 elements
+constexpr int BKB = 128;             // bytes of a K sub-tile per row = 256 FP4 elements (one TMA box, one swizzle atom)
+constexpr int kSub = 2;              // K sub-tiles per pipeline stage: K = 512 per stage
+constexpr int kMmaPerStage = 4 * kSub;  // MMAs of K = 64 per stage
 constexpr int kThreads = 192;        // 6 warps
 constexpr int kWarps = 6;
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 4;
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;  // scale factors live after the (<= 256-column) accumulator
@@ -84,18 +87,25 @@ static_assert((3 * kMaxStages + 4) * 8 <= kCtrlSlot, "barriers precede the TMEM 
 constexpr long long kWaitLimit = 2000000000LL;  // SM cycles (~1 s)
 constexpr int kSmallCols = 16;       // reduce path, small rows: <= 16 columns per lane (N <= 512)
 
+// One stage: A and B code tiles of kSub sub-tiles each (sub-tile u of A at
+// u * BM * BKB, a 128-byte-swizzled box), then (scales by TMA) the stage's
+// scale bytes, SFA rows then SFB rows, 16 kSub bytes each.  Tensor memory
+// per stage: the SFA words of the kMmaPerStage MMAs (4 columns each), then
+// the SFB words (4 columns per MMA and 128-row atom).
 template <int BN>
 struct Layout {
   static constexpr int kAtomsB = BN / 128;
-  static constexpr uint32_t kA = BM * BKB;
-  static constexpr uint32_t kB = BN * BKB;
-  static constexpr uint32_t kSfaStage = BM * 16;  // scale bytes of the K tile, row-major (16 per row)
-  static constexpr uint32_t kSfbStage = BN * 16;
+  static constexpr uint32_t kSubA = BM * BKB;
+  static constexpr uint32_t kSubB = BN * BKB;
+  static constexpr uint32_t kA = kSub * kSubA;
+  static constexpr uint32_t kB = kSub * kSubB;
   static constexpr uint32_t offB = kA;
-  static constexpr uint32_t offSfaStage = kA + kB;
-  static constexpr uint32_t offSfbStage = offSfaStage + kSfaStage;
-  static constexpr uint32_t kStage = offSfbStage + kSfbStage;  // 36 KB (BN 128) / 54 KB (BN 256)
-  static constexpr uint32_t kSfTmemPerStage = 16 + 16 * kAtomsB;
+  static constexpr uint32_t kSfRow = 16 * kSub;
+  static constexpr uint32_t offSf = kA + kB;
+  static constexpr uint32_t kSf = (BM + BN) * kSfRow;
+  static constexpr uint32_t kStage = offSf + kSf;  // 72 KB (BN 128) / 108 KB (BN 256)
+  static constexpr uint32_t kSfbCol = 4 * kMmaPerStage;
+  static constexpr uint32_t kSfTmemPerStage = kSfbCol + 4 * kMmaPerStage * kAtomsB;
   // stages whose scale columns fit in TMEM after the accumulator
   static constexpr int kStagesMax = static_cast<int>((kTmemCols - kSfTmemBase) / kSfTmemPerStage) < kMaxStages
                                         ? static_cast<int>((kTmemCols - kSfTmemBase) / kSfTmemPerStage)
@@ -120,7 +130,8 @@ struct Params {
   int num_k_tiles;
   int n_split, k_split;
   int stages;
-  int tma_sf;             // scale tiles by TMA (needs K % 256 == 0)
+  int sf_tma;             // scales by TMA with the stage's tiles (rows and base 16-byte aligned, K % 256 == 0);
+                          // else the scale warps load them from global memory
   uint32_t region_bytes;  // pipeline ring, reused after the main loop (1 KB multiple)
   int direct;             // direct epilogue (k_split == 1, k <= 32)
   int ro;                 // rows of a tile owned by each CTA of the cluster
@@ -841,8 +852,8 @@ template <int BN, int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_topk_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b,
-                     const __grid_constant__ CUtensorMap tma_sfa,
-                     const __grid_constant__ CUtensorMap tma_sfb, const __grid_constant__ Params p) {
+                     const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
+                     const __grid_constant__ Params p) {
   using L = Layout<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -887,14 +898,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     prefetch_tensormap(&tma_a);
     prefetch_tensormap(&tma_b);
-    if (p.tma_sf) {
+    if (p.sf_tma) {
       prefetch_tensormap(&tma_sfa);
       prefetch_tensormap(&tma_sfb);
     }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), p.tma_sf ? 1 : 1 + 32);  // + one cp.async arrival per producer lane
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sfready_bar(s), 4);  // one arrival per scale warp
     }
@@ -923,18 +934,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    if (p.tma_sf) {
-      // The first stages need no empty-slot wait: start their loads now,
-      // ahead of the block barrier.
-      const int pre = min(S, nk);
-      const uint32_t tx = L::kA + L::kB + L::kSfaStage + L::kSfbStage;
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t st = sbase + i * L::kStage;
-        mbar_arrive_expect_tx(full_bar(i), tx);
-        tma_load_2d(st, &tma_a, full_bar(i), (kt0 + i) * BKB, m0);
-        tma_load_2d(st + L::offB, &tma_b, full_bar(i), (kt0 + i) * BKB, n0);
-        tma_load_2d(st + L::offSfaStage, &tma_sfa, full_bar(i), (kt0 + i) * 16, m0);
-        tma_load_2d(st + L::offSfbStage, &tma_sfb, full_bar(i), (kt0 + i) * 16, n0);
+    // The first stages need no empty-slot wait: start their loads now,
+    // ahead of the block barrier.
+    const int pre = min(S, nk);
+    for (int i = 0; i < pre; ++i) {
+      const uint32_t st = sbase + i * L::kStage;
+      mbar_arrive_expect_tx(full_bar(i), p.sf_tma ? L::kStage : L::offSf);
+#pragma unroll
+      for (int u = 0; u < kSub; ++u) {
+        tma_load_2d(st + u * L::kSubA, &tma_a, full_bar(i), ((kt0 + i) * kSub + u) * BKB, m0);
+        tma_load_2d(st + L::offB + u * L::kSubB, &tma_b, full_bar(i), ((kt0 + i) * kSub + u) * BKB, n0);
+      }
+      if (p.sf_tma) {
+        tma_load_2d(st + L::offSf, &tma_sfa, full_bar(i), (kt0 + i) * L::kSfRow, m0);
+        tma_load_2d(st + L::offSf + BM * L::kSfRow, &tma_sfb, full_bar(i), (kt0 + i) * L::kSfRow, n0);
       }
     }
   }
@@ -949,12 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const int kwords = p.K / 64;
-    const int sf_ld = p.K / 16;
-    const int kk = lane & 3;
-    const int rsub = lane >> 2;
-    const uint32_t tx = L::kA + L::kB + (p.tma_sf ? L::kSfaStage + L::kSfbStage : 0u);
-    const int pre = p.tma_sf ? min(S, nk) : 0;  // stages already loaded during set-up
+    const int pre = min(S, nk);  // stages already loaded during set-up
     int last = pre - 1;
     for (int i = pre; i < nk; ++i) {
       const int s = i % S;
@@ -966,34 +974,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sbase + s * L::kStage;
       const int kt = kt0 + i;
       if (lane == 0) {
-        mbar_arrive_expect_tx(full_bar(s), tx);
-        tma_load_2d(st, &tma_a, full_bar(s), kt * BKB, m0);
-        tma_load_2d(st + L::offB, &tma_b, full_bar(s), kt * BKB, n0);
-        if (p.tma_sf) {
-          tma_load_2d(st + L::offSfaStage, &tma_sfa, full_bar(s), kt * 16, m0);
-          tma_load_2d(st + L::offSfbStage, &tma_sfb, full_bar(s), kt * 16, n0);
+        mbar_arrive_expect_tx(full_bar(s), p.sf_tma ? L::kStage : L::offSf);
+#pragma unroll
+        for (int u = 0; u < kSub; ++u) {
+          tma_load_2d(st + u * L::kSubA, &tma_a, full_bar(s), (kt * kSub + u) * BKB, m0);
+          tma_load_2d(st + L::offB + u * L::kSubB, &tma_b, full_bar(s), (kt * kSub + u) * BKB, n0);
         }
-      }
-      if (!p.tma_sf) {
-        // Scale word (row r, MMA step kk) goes to byte 16 r + 4 kk, the
-        // layout of the TMA-staged scales.
-        const int kw = kt * 4 + kk;
-        const bool kvalid = kw < kwords;
-        for (int j = 0; j < BM / 8; ++j) {
-          const int r = rsub + 8 * j;
-          const int ra = m0 + r;
-          const bool va = kvalid && ra < p.M;
-          cp_async_4(st + L::offSfaStage + r * 16 + kk * 4,
-                     va ? p.sfa + static_cast<int64_t>(ra) * sf_ld + kw * 4 : p.sfa, va ? 4u : 0u);
+        if (p.sf_tma) {
+          tma_load_2d(st + L::offSf, &tma_sfa, full_bar(s), kt * L::kSfRow, m0);
+          tma_load_2d(st + L::offSf + BM * L::kSfRow, &tma_sfb, full_bar(s), kt * L::kSfRow, n0);
         }
-        for (int j = 0; j < BN / 8; ++j) {
-          const int r = rsub + 8 * j;
-          const int rb = n0 + r;
-          const bool vb = kvalid && rb < p.N;
-          cp_async_4(st + L::offSfbStage + r * 16 + kk * 4,
-                     vb ? p.sfb + static_cast<int64_t>(rb) * sf_ld + kw * 4 : p.sfb, vb ? 4u : 0u);
-        }
-        cp_async_arrive_noinc(full_bar(s));
       }
       last = i;
     }
@@ -1014,7 +1004,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nk; ++i) {
       const int s = i % S;
       const uint32_t ph = (i / S) & 1;
-      if (!warp_wait(full_bar(s), ph, abort) || !warp_wait(sfready_bar(s), ph, abort)) {
+      // (with the scales in the stage, the scale warps arrive on sfready(s)
+      // only after full(s) has completed, which then covers A and B too)
+      if ((!p.sf_tma && !warp_wait(full_bar(s), ph, abort)) || !warp_wait(sfready_bar(s), ph, abort)) {
         if (lane == 0) record_timeout(p.status, abort);
         ok = false;
         break;
@@ -1023,11 +1015,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t st = sbase + s * L::kStage;
         const uint32_t sf_col = tmem + kSfTmemBase + s * L::kSfTmemPerStage;
+        // MMAs that lie wholly past K (a short last stage) are skipped
+        const int nmma = min(kMmaPerStage, (p.K - (kt0 + i) * kMmaPerStage * 64 + 63) / 64);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc_mma_nvf4(tmem, smem_desc(st + kk * 32, 16, 1024, 2),
-                      smem_desc(st + L::offB + kk * 32, 16, 1024, 2), idesc, sf_col + kk * 4,
-                      sf_col + 16 + kk * 4 * L::kAtomsB, (i | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < kMmaPerStage; ++kk) {
+          if (kk < nmma)
+            tc_mma_nvf4(tmem, smem_desc(st + (kk / 4) * L::kSubA + (kk % 4) * 32, 16, 1024, 2),
+                        smem_desc(st + L::offB + (kk / 4) * L::kSubB + (kk % 4) * 32, 16, 1024, 2), idesc,
+                        sf_col + kk * 4, sf_col + L::kSfbCol + kk * 4 * L::kAtomsB, (i | kk) != 0 ? 1u : 0u);
         }
         tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
       }
@@ -1045,43 +1040,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The block-scaled MMA reads the scales of MMA step kk (K = 64) of a
     // 128-row atom from 4 TMEM columns: lane l (in every 32-lane
     // sub-partition alike) holds, in column 4 kk + c, the scale word kk of
-    // row 32 c + l.  Each of the four warps writes that pattern into its own
-    // sub-partition with tcgen05.st from registers, so the tensor pipe
-    // spends no instructions on copying scales; the MMA warp waits for the
-    // four arrivals.
+    // row 32 c + l.  Each of the four warps writes the words of its lanes
+    // into its own sub-partition with tcgen05.st, so the tensor pipe carries
+    // no scales.  The words come with the stage's tiles (TMA), or, when the
+    // scale rows are not 16-byte aligned, straight from global memory.
     const uint32_t lane_sel = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int64_t sf_ld = p.K / 16;  // scale bytes per row
+    const int kwords = p.K / 64;     // scale words per row
     for (int i = 0; i < nk; ++i) {
       const int s = i % S;
       const uint32_t ph = (i / S) & 1;
-      if (!warp_wait(full_bar(s), ph, abort)) {
-        if (lane == 0) record_timeout(p.status, abort);
-        break;
-      }
-      // (the MMAs that read this stage's TMEM columns in the previous round
-      // have completed: full(s) of this round follows empty(s))
-      tc_fence_after();
-      const uint32_t st = sbase + s * L::kStage;
-      const uint32_t sf_col = tmem + lane_sel + kSfTmemBase + s * L::kSfTmemPerStage;
-      uint32_t ra[16], rb[16 * L::kAtomsB];  // in TMEM column order: SFA, then SFB
-      // staged row-major: the 16 bytes of row 32 c + l of atom a hold its
-      // scale words kk = 0..3 (SFA: column 4 kk + c; SFB atom a - 1: column
-      // 16 + 4 (kk kAtomsB + a - 1) + c)
-#pragma unroll
-      for (int a = 0; a < kUnits; ++a)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[4];
-          ld_shared_v4((a == 0 ? st + L::offSfaStage : st + L::offSfbStage + (a - 1) * 2048) +
-                           (c * 32 + lane) * 16, w);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if (a == 0) ra[kk * 4 + c] = w[kk];
-            else rb[(kk * L::kAtomsB + (a - 1)) * 4 + c] = w[kk];
-          }
+      // SFA: column 4 kk + c; SFB atom a - 1: column kSfbCol + 4 (kk kAtomsB + a - 1) + c
+      uint32_t ra[4 * kMmaPerStage], rb[4 * kMmaPerStage * L::kAtomsB];
+      if (p.sf_tma) {
+        // the stage has landed; then the MMAs that read this slot's TMEM
+        // columns in the previous round have completed (full(s) of this
+        // round follows empty(s))
+        if (!warp_wait(full_bar(s), ph, abort)) {
+          if (lane == 0) record_timeout(p.status, abort);
+          break;
         }
-      tmem_st_32x32b_x16(sf_col, ra);
-      if constexpr (L::kAtomsB == 1) tmem_st_32x32b_x16(sf_col + 16, rb);
-      else tmem_st_32x32b_x32(sf_col + 16, rb);
+        const uint32_t sst = sbase + s * L::kStage + L::offSf;
+#pragma unroll
+        for (int a = 0; a < kUnits; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int h = 0; h < kSub; ++h) {
+              uint32_t w[4];
+              ld_shared_v4(sst + ((a == 0 ? 0 : BM + (a - 1) * 128) + c * 32 + static_cast<int>(lane)) * L::kSfRow +
+                               h * 16, w);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int kk = h * 4 + j;
+                if (a == 0) ra[kk * 4 + c] = w[j];
+                else rb[(kk * L::kAtomsB + (a - 1)) * 4 + c] = w[j];
+              }
+            }
+      } else {
+        const int kw0 = (kt0 + i) * kMmaPerStage;  // first scale word of the stage
+#pragma unroll
+        for (int a = 0; a < kUnits; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = (a == 0 ? m0 : n0 + (a - 1) * 128) + 32 * c + static_cast<int>(lane);
+            const bool row_ok = r < (a == 0 ? p.M : p.N);
+            const uint32_t* rowp = reinterpret_cast<const uint32_t*>(
+                (a == 0 ? p.sfa : p.sfb) + (row_ok ? static_cast<int64_t>(r) * sf_ld : 0));
+#pragma unroll
+            for (int kk = 0; kk < kMmaPerStage; ++kk) {
+              const uint32_t w = (row_ok && kw0 + kk < kwords) ? __ldg(rowp + kw0 + kk) : 0u;
+              if (a == 0) ra[kk * 4 + c] = w;
+              else rb[(kk * L::kAtomsB + (a - 1)) * 4 + c] = w;
+            }
+          }
+        // the MMAs that read this slot's TMEM columns S stages ago have completed
+        if (i >= S && !warp_wait(empty_bar(s), ph ^ 1u, abort)) {
+          if (lane == 0) record_timeout(p.status, abort);
+          break;
+        }
+      }
+      tc_fence_after();
+      const uint32_t sf_col = tmem + lane_sel + kSfTmemBase + s * L::kSfTmemPerStage;
+      static_assert(4 * kMmaPerStage == 32, "one 32-column store per 128-row atom");
+      tmem_st_32x32b_x32(sf_col, ra);
+      tmem_st_32x32b_x32(sf_col + L::kSfbCol, *reinterpret_cast<uint32_t(*)[32]>(rb));
+      if constexpr (L::kAtomsB == 2)
+        tmem_st_32x32b_x32(sf_col + L::kSfbCol + 32, *reinterpret_cast<uint32_t(*)[32]>(rb + 32));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -1111,6 +1136,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float gab = __ldg(p.gsa) * __ldg(p.gsb);
   const int quarter = warp & 3;  // epilogue warps read TMEM lanes 32*quarter .. +31
   const int row = quarter * 32 + static_cast<int>(lane);
+  // Direct path with an N split: the per-row lists go to their owners' stage
+  // regions (after the logits), free once every CTA of the cluster has left
+  // its main loop (copies landed, MMAs complete): arrive here, wait just
+  // before the pushes.
+  const bool list_barrier = p.direct && p.n_split > 1;
+  constexpr uint32_t kListOff = (4 * BN + (KMAX == 8 ? BM * (BN + 4) : 0)) * 4;
+  if (list_barrier) {
+    cluster_arrive();
+    if (warp < 2) cluster_wait();
+  }
 
   if (p.direct) {
     // ------------------------------------------------------------ direct epilogue
@@ -1358,6 +1393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (list_barrier) cluster_wait();
       if (p.n_split == 1) {
         if (row < vr) list_store<KMAX>(p, m0 + row, tv, ti, tw);
       } else if (row < vr) {
@@ -1365,7 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bytes (consecutive rows at consecutive addresses, so the owner's
         // threads read a slot without bank conflicts)
         const int owner = row / p.ro;
-        const uint32_t dst = mapa_shared(smem_addr(rowmem), static_cast<uint32_t>(owner)) +
+        const uint32_t dst = mapa_shared(sbase + kListOff, static_cast<uint32_t>(owner)) +
                              static_cast<uint32_t>((n_idx * KMAX * p.ro + (row - owner * p.ro)) * 16);
 #pragma unroll
         for (int i = 0; i < KMAX; ++i)
@@ -1383,7 +1419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (KMAX == 8 && t < owned) {
         // sorted lists of 8 entries, merged slice by slice (slices in column
         // order; the entry order already puts the lower column first on ties)
-        const uint32_t* lists = reinterpret_cast<const uint32_t*>(rowmem);
+        const uint32_t* lists = reinterpret_cast<const uint32_t*>(smem + kListOff);
         uint64_t r[8], g[8];
         float rw[8], gw[8];
         for (int ni = 0; ni < p.n_split; ++ni) {
@@ -1418,7 +1454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ti[KMAX];
         list_init<KMAX>(tv, ti, tw);
         float kth = -__int_as_float(0x7F800000);
-        const uint32_t* lists = reinterpret_cast<const uint32_t*>(rowmem);
+        const uint32_t* lists = reinterpret_cast<const uint32_t*>(smem + kListOff);
         for (int ni = 0; ni < p.n_split; ++ni) {  // slices in column order: ties stay by lower n
 #pragma unroll
           for (int i = 0; i < KMAX; ++i) {
@@ -1630,7 +1666,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   pl.rpc = rpc;
   pl.heads = heads;
   const int64_t m_tiles = (M + rpc - 1) / rpc;
-  const int kt = static_cast<int>((K / 2 + BKB - 1) / BKB);
+  const int kt = static_cast<int>((K / 2 + BKB * kSub - 1) / (BKB * kSub));  // pipeline stages of K
   if (N <= 128) {
     pl.bn = 128;
   } else if (N <= 256 && m_tiles * 2 >= sms / 2) {
@@ -1672,17 +1708,17 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int k, int sms, int smem_optin, 
   // copies, or the reduce epilogue's staged tile (bulk) / received partials.
   auto total = [&]() {
     // direct: four bias copies, and for k <= 8 the tile's logits (BM rows of BN + 4 floats)
+    // direct, N split: then the per-row lists pushed by the cluster's CTAs
     const uint32_t reuse =
         pl.direct ? 4u * static_cast<uint32_t>(pl.bn) * 4u +
-                        (pl.kmax == 8 ? static_cast<uint32_t>(BM) * static_cast<uint32_t>(pl.bn + 4) * 4u : 0u)
+                        (pl.kmax == 8 ? static_cast<uint32_t>(BM) * static_cast<uint32_t>(pl.bn + 4) * 4u : 0u) +
+                        (pl.n_split > 1 ? static_cast<uint32_t>(pl.n_split * pl.ro * pl.kmax) * 16u : 0u)
                   : (pl.bulk ? staging : recv);
     uint32_t region = pl.stages * sb > reuse ? pl.stages * sb : reuse;
     region = (region + 1023u) & ~1023u;
     pl.region = region;
     pl.recv_bytes = (!pl.direct && pl.bulk) ? recv : 0u;
     size_t extra = pl.recv_bytes;
-    if (pl.direct && pl.n_split > 1)
-      extra = static_cast<size_t>(pl.n_split) * pl.ro * pl.kmax * 16;  // merged per-row lists
     if (pl.large)
       extra += pl.row_bytes + static_cast<size_t>(pl.cand_cap) * 8 + 256;  // keys, candidates, block scratch
     pl.bias_off = static_cast<uint32_t>(extra);
@@ -1843,6 +1879,9 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
   // the least dynamic shared memory that leaves no room for a second CTA
   const int smem_one_cta = smem_sm / 2 - smem_reserved + 1;
+  // Scales by TMA when their rows and base are 16-byte aligned.
+  const bool sf_tma = a.K % 256 == 0 && reinterpret_cast<uintptr_t>(a.sfa) % 16 == 0 &&
+                      reinterpret_cast<uintptr_t>(a.sfb) % 16 == 0;
   // Largest cluster (16, else 8, 4, ...) whose CTAs can be co-resident.
   Plan pl;
   int cap = kMaxCluster;
@@ -1869,17 +1908,16 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
       pl = spread;
   }
 
-  const bool tma_sf = (a.K % 256) == 0;
   CUtensorMap ma, mb, msa, msb;
   if (!make_map(&ma, a.qa, a.M, a.K / 2, BKB, BM, true) ||
       !make_map(&mb, a.qb, a.N, a.K / 2, BKB, pl.bn, true))
     return NVFP4_ERR_UNSUPPORTED;
-  if (tma_sf) {
-    if (!make_map(&msa, a.sfa, a.M, a.K / 16, 16, BM, false) ||
-        !make_map(&msb, a.sfb, a.N, a.K / 16, 16, pl.bn, false))
+  if (sf_tma) {
+    if (!make_map(&msa, a.sfa, a.M, a.K / 16, 16 * kSub, BM, false) ||
+        !make_map(&msb, a.sfb, a.N, a.K / 16, 16 * kSub, pl.bn, false))
       return NVFP4_ERR_UNSUPPORTED;
   } else {
-    msa = ma;  // unused
+    msa = ma;  // not read
     msb = mb;
   }
   Params p;
@@ -1899,11 +1937,11 @@ int launch_gemm_topk(const GemmTopkArgs& a, cudaStream_t stream, cudaError_t* er
   p.K = static_cast<int>(a.K);
   p.k = a.k;
   p.epilogue = a.epilogue;
-  p.num_k_tiles = static_cast<int>((a.K / 2 + BKB - 1) / BKB);
+  p.num_k_tiles = static_cast<int>((a.K / 2 + BKB * kSub - 1) / (BKB * kSub));  // pipeline stages of K
   p.n_split = pl.n_split;
   p.k_split = pl.k_split;
   p.stages = pl.stages;
-  p.tma_sf = tma_sf ? 1 : 0;
+  p.sf_tma = sf_tma ? 1 : 0;
   p.region_bytes = pl.region;
   p.direct = pl.direct;
   p.ro = pl.ro;

@@ -136,21 +136,6 @@ __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32
   atomicOr(status, NVFP4_DEVICE_TIMEOUT);
 }
 
-// Named barrier 1 over the four scale/epilogue warps (128 threads); returns
-// whether any of them passed `fail`, so all four take the same branch.
-__device__ __forceinline__ bool bar_any_128(bool fail) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(fail ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
