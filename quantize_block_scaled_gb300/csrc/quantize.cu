@@ -681,6 +681,57 @@ __device__ __forceinline__ void sq_windows(uint32_t h, int emax, uint64_t& w0, u
   below |= (in0 || in1) ? 0u : m;
 }
 
+// Shifts with PTX semantics: an amount of 32 or more (a negative int
+// passed as unsigned) gives 0.
+__device__ __forceinline__ uint32_t shl_sat(uint32_t v, uint32_t s) {
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(s));
+  return r;
+}
+__device__ __forceinline__ uint32_t shr_sat(uint32_t v, uint32_t s) {
+  uint32_t r;
+  asm("shr.b32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(s));
+  return r;
+}
+
+// Rows whose nonzero elements span at most two windows (d <= 34 for all):
+// with s0 = e' + 17 - Emax' (e' = max(E, 1)), window 0 takes m << s0
+// (s0 >= 0) and window 1 takes m << (s0 + 17) (s0 < 0), both written as
+// clamped shifts so that each element lands in exactly one window with no
+// selects; m = |h| + 128 - 128 e' is the significand with its hidden bit.
+// kTwo = false: every element is in window 0 (span <= 17).
+template <bool kTwo>
+__device__ __forceinline__ void sq_fast(uint32_t h, int c0, uint64_t& w0, uint64_t& w1) {
+  const uint32_t u = h & 0x7FFFu;
+  const uint32_t ep = max(u >> 7, 1u);
+  const uint32_t m = u + 128u - (ep << 7);
+  const int s0 = static_cast<int>(ep) + c0;
+  const uint32_t a0 = shl_sat(m, static_cast<uint32_t>(s0));
+  w0 += static_cast<uint64_t>(a0) * a0;
+  if constexpr (kTwo) {
+    const uint32_t a1 = shr_sat(m << 16, static_cast<uint32_t>(-1 - s0));
+    w1 += static_cast<uint64_t>(a1) * a1;
+  }
+}
+
+template <bool kTwo>
+__device__ __forceinline__ void sq_fast_rows(const uint4* v, int nv, int lane, int c0, uint64_t& w0, uint64_t& w1) {
+  uint64_t x0 = 0, x1 = 0;  // a second pair of sums: two independent accumulation chains
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 t = v[i];
+    sq_fast<kTwo>(t.x & 0xFFFFu, c0, w0, w1);
+    sq_fast<kTwo>(t.x >> 16, c0, x0, x1);
+    sq_fast<kTwo>(t.y & 0xFFFFu, c0, w0, w1);
+    sq_fast<kTwo>(t.y >> 16, c0, x0, x1);
+    sq_fast<kTwo>(t.z & 0xFFFFu, c0, w0, w1);
+    sq_fast<kTwo>(t.z >> 16, c0, x0, x1);
+    sq_fast<kTwo>(t.w & 0xFFFFu, c0, w0, w1);
+    sq_fast<kTwo>(t.w >> 16, c0, x0, x1);
+  }
+  w0 += x0;
+  w1 += x1;
+}
+
 // Window w alone (slow pass): the squares of the elements with
 // 17w < d <= 17w + 17 (w = 0: d <= 17), in that window's units.
 __device__ __forceinline__ uint64_t sq_window(uint32_t h, int emax, int w) {
@@ -732,14 +783,35 @@ __device__ float warp_sum_sq_exact(const uint16_t* xr, int64_t cols) {
   const int lane = static_cast<int>(threadIdx.x & 31);
   const uint4* v = reinterpret_cast<const uint4*>(xr);
   const int nv = static_cast<int>(cols / 8);
-  uint32_t m2 = 0;
-  for (int i = lane; i < nv; i += 32) m2 = __vmaxu2(m2, absmax8(v[i]));
-  uint32_t mb = fold16(m2);
+  // the largest |h| and the smallest nonzero |h| (zeros wrap to 0xFFFF in
+  // the 16-bit subtraction and drop out of the minimum)
+  uint32_t m2 = 0, n2 = 0xFFFFFFFFu;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 t = v[i];
+    m2 = __vmaxu2(m2, absmax8(t));
+    const uint32_t k = 0x7FFF7FFFu, one = 0x00010001u;
+    n2 = __vminu2(n2, __vminu2(__vminu2(__vsub2(t.x & k, one), __vsub2(t.y & k, one)),
+                               __vminu2(__vsub2(t.z & k, one), __vsub2(t.w & k, one))));
+  }
+  uint32_t mb = fold16(m2), nb = min(n2 & 0xFFFFu, n2 >> 16);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+  for (int o = 16; o > 0; o >>= 1) {
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+    nb = min(nb, __shfl_xor_sync(0xFFFFFFFFu, nb, o));
+  }
   if (mb == 0) return 0.0f;
   const int emax = max(static_cast<int>(mb >> 7), 1);
+  const int emin = max(static_cast<int>((nb + 1) >> 7), 1);  // exponent of the smallest nonzero |x|
+  const int e0 = 2 * (emax - 134) - 2 * kWinBits;  // window 0's unit: 2^e0
   uint64_t w0 = 0, w1 = 0;
+  if (emax - emin <= 2 * kWinBits) {
+    // nothing below window 1: the two windows are the exact sum
+    if (emax - emin <= kWinBits) sq_fast_rows<false>(v, nv, lane, kWinBits - emax, w0, w1);
+    else sq_fast_rows<true>(v, nv, lane, kWinBits - emax, w0, w1);
+    w0 = warp_sum_u64(w0);
+    w1 = warp_sum_u64(w1);
+    return round_sum(w0 + (w1 >> 34), (w1 & kLow34) != 0, e0);
+  }
   uint32_t below = 0;
   for (int i = lane; i < nv; i += 32) {
     const uint4 t = v[i];
@@ -753,7 +825,6 @@ __device__ float warp_sum_sq_exact(const uint16_t* xr, int64_t cols) {
   w0 = warp_sum_u64(w0);
   w1 = warp_sum_u64(w1);
   below = __reduce_or_sync(0xFFFFFFFFu, below);
-  const int e0 = 2 * (emax - 134) - 2 * kWinBits;  // window 0's unit: 2^e0
   // The windows below window 1 add less than 2^30 of window 1's units.
   if (below == 0 || (w1 & kLow34) < kLow34 + 1 - (1ull << 30))
     return round_sum(w0 + (w1 >> 34), (w1 & kLow34) != 0 || below != 0, e0);
