@@ -908,46 +908,258 @@ __device__ __forceinline__ void warp_mhc_mix(const uint16_t* src, int64_t cols, 
   __syncwarp();
 }
 
-constexpr int kRmsThreads = 256;  // 8 warps, one row per warp at a time
+// ---- two passes (inputs larger than the SMs' shared memory): one CTA per row at a time
+//
+// Thread t of the CTA (NT threads) holds the row's 16-element blocks
+// b = t + j NT (j < J) in registers: it loads them (with the mix, each stream's, summed
+// in stream order), the CTA reduces the row's maximum and smallest nonzero
+// |x|, then the exact sum of squares (two windows, or every window for rows
+// of a very wide range), and every thread normalises its blocks.  Both passes
+// recompute the row the same way, so the second quantizes exactly what the
+// first measured.
+constexpr int kRowWarpsMax = 16;
+constexpr int kBlockRowsMax = 6;  // one-pass kernel: up to this many rows per CTA, all threads per row
 
-// Pass 1 (inputs larger than the SMs' shared memory): y's maximum |.|, then
-// gs by the last block, exactly as the amax kernel does.
-// kMix: the row is first mixed from the token's n_hc streams (mHC pre-mix)
-// into this warp's shared-memory buffer.
-template <bool kMix>
-__global__ void __launch_bounds__(kRmsThreads)
+struct RowScratch {
+  uint32_t mx[kRowWarpsMax], mn[kRowWarpsMax], below[kRowWarpsMax];
+  unsigned long long w0[kRowWarpsMax], w1[kRowWarpsMax];
+};
+
+// Sum over the CTA of two 64-bit values (and an OR of a flag); every thread
+// gets the totals.  One barrier; the caller's next use of the same fields
+// comes after another barrier.
+template <int NT>
+__device__ __forceinline__ void block_sum2(uint64_t& a, uint64_t& b, uint32_t& f, RowScratch& sc) {
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  a = warp_sum_u64(a);
+  b = warp_sum_u64(b);
+  f = __reduce_or_sync(0xFFFFFFFFu, f);
+  if (lane == 0) {
+    sc.w0[warp] = a;
+    sc.w1[warp] = b;
+    sc.below[warp] = f;
+  }
+  __syncthreads();
+  a = 0;
+  b = 0;
+  f = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    a += sc.w0[w];
+    b += sc.w1[w];
+    f |= sc.below[w];
+  }
+}
+
+// Loads of a row's 16-byte vectors: global memory (read-only path) or shared.
+template <bool kShared>
+__device__ __forceinline__ uint4 ld_row(const uint16_t* p) {
+  if constexpr (kShared) return *reinterpret_cast<const uint4*>(p);
+  else return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// y = bf16((x * inv_rms) * w) of this thread's blocks of row r (x: the
+// row, or with the mix the token's first stream, streams cols apart; in
+// global memory, or shared with kShared).
+template <int NT, int J, bool kMix, bool kShared = false>
+__device__ __forceinline__ void block_row_norm(const uint16_t* __restrict__ xr, int64_t cols,
+                                               const uint16_t* __restrict__ wt, float eps,
+                                               const uint16_t* __restrict__ arow, int n_hc, RowScratch& sc,
+                                               uint4 (&y)[J][2]) {
+  const int t = static_cast<int>(threadIdx.x), warp = t >> 5, lane = t & 31;
+  const int nb = static_cast<int>(cols / 16);
+  uint4 x[J][2];
+  if constexpr (kMix) {
+    float acc[J][16];
+    // streams four at a time, all of their loads issued before the
+    // arithmetic (an index past n_hc re-reads stream 0 and is not used)
+#pragma unroll
+    for (int i0 = 0; i0 < 8; i0 += 4) {
+      if (i0 < n_hc) {
+        uint4 v[4][J][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u < n_hc ? i0 + u : 0;
+#pragma unroll
+          for (int j = 0; j < J; ++j) {
+            const int b = t + j * NT;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              v[u][j][h] = b < nb ? ld_row<kShared>(xr + i * cols + b * 16 + h * 8) : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u;
+          if (i < n_hc) {
+            const float ai = lo_bf16(static_cast<uint32_t>(__ldg(arow + i)));
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t ww[4] = {v[u][j][h].x, v[u][j][h].y, v[u][j][h].z, v[u][j][h].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float p0 = __fmul_rn(ai, lo_bf16(ww[k])), p1 = __fmul_rn(ai, hi_bf16(ww[k]));
+                  float& s0 = acc[j][h * 8 + 2 * k];
+                  float& s1 = acc[j][h * 8 + 2 * k + 1];
+                  s0 = i == 0 ? p0 : __fadd_rn(s0, p0);
+                  s1 = i == 0 ? p1 : __fadd_rn(s1, p1);
+                }
+              }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          o[k] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[j][h * 8 + 2 * k]))) |
+                 (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[j][h * 8 + 2 * k + 1]))) << 16);
+        x[j][h] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int b = t + j * NT;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        x[j][h] = b < nb ? ld_row<kShared>(xr + b * 16 + h * 8) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  // the row's largest |h| and smallest nonzero |h| (blocks past the row are zeros)
+  uint32_t m2 = 0, n2 = 0xFFFFFFFFu;
+#pragma unroll
+  for (int j = 0; j < J; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 v = x[j][h];
+      m2 = __vmaxu2(m2, absmax8(v));
+      const uint32_t k = 0x7FFF7FFFu, one = 0x00010001u;
+      n2 = __vminu2(n2, __vminu2(__vminu2(__vsub2(v.x & k, one), __vsub2(v.y & k, one)),
+                                 __vminu2(__vsub2(v.z & k, one), __vsub2(v.w & k, one))));
+    }
+  uint32_t mb = fold16(m2), nm = min(n2 & 0xFFFFu, n2 >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+    nm = min(nm, __shfl_xor_sync(0xFFFFFFFFu, nm, o));
+  }
+  if (lane == 0) {
+    sc.mx[warp] = mb;
+    sc.mn[warp] = nm;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    mb = max(mb, sc.mx[w]);
+    nm = min(nm, sc.mn[w]);
+  }
+  float sum = 0.0f;
+  if (mb != 0) {
+    const int emax = max(static_cast<int>(mb >> 7), 1);
+    const int emin = max(static_cast<int>((nm + 1) >> 7), 1);
+    const int e0 = 2 * (emax - 134) - 2 * kWinBits;  // window 0's unit: 2^e0
+    uint64_t w0 = 0, w1 = 0;
+    uint32_t below = 0;
+    if (emax - emin <= 2 * kWinBits) {  // nothing below window 1
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ww[4] = {x[j][h].x, x[j][h].y, x[j][h].z, x[j][h].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            sq_fast<true>(ww[k] & 0xFFFFu, kWinBits - emax, w0, w1);
+            sq_fast<true>(ww[k] >> 16, kWinBits - emax, w0, w1);
+          }
+        }
+      block_sum2<NT>(w0, w1, below, sc);
+      sum = round_sum(w0 + (w1 >> 34), (w1 & kLow34) != 0, e0);
+    } else {
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ww[4] = {x[j][h].x, x[j][h].y, x[j][h].z, x[j][h].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            sq_windows(ww[k] & 0xFFFFu, emax, w0, w1, below);
+            sq_windows(ww[k] >> 16, emax, w0, w1, below);
+          }
+        }
+      block_sum2<NT>(w0, w1, below, sc);
+      if (below == 0 || (w1 & kLow34) < kLow34 + 1 - (1ull << 30)) {
+        sum = round_sum(w0 + (w1 >> 34), (w1 & kLow34) != 0 || below != 0, e0);
+      } else {
+        // every window, from the bottom up (rare: a carry may cross window 1)
+        const int n_win = (emax - 1) / kWinBits + 1;
+        uint64_t carry = 0;
+        bool sticky = false;
+        for (int wi = n_win - 1; wi >= 0; --wi) {
+          __syncthreads();  // the previous totals have been read
+          uint64_t acc = 0, none = 0;
+          uint32_t nf = 0;
+#pragma unroll
+          for (int j = 0; j < J; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t ww[4] = {x[j][h].x, x[j][h].y, x[j][h].z, x[j][h].w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) acc += sq_window(ww[k] & 0xFFFFu, emax, wi) + sq_window(ww[k] >> 16, emax, wi);
+            }
+          block_sum2<NT>(acc, none, nf, sc);
+          const uint64_t tot = acc + carry;
+          if (wi == 0) {
+            sum = round_sum(tot, sticky, e0);
+          } else {
+            sticky = sticky || (tot & kLow34) != 0;
+            carry = tot >> 34;
+          }
+        }
+      }
+    }
+  }
+  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(cols)), eps)));
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int b = t + j * NT;
+    const uint4* wv = reinterpret_cast<const uint4*>(wt + (b < nb ? b : 0) * 16);
+    y[j][0] = rms_vec(x[j][0], __ldg(wv), inv);
+    y[j][1] = rms_vec(x[j][1], __ldg(wv + 1), inv);
+  }
+}
+
+// Pass 1: y's maximum |.|, then gs by the last block, exactly as the amax kernel does.
+template <int NT, int J, bool kMix>
+__global__ void __launch_bounds__(NT, 512 / NT)
     rmsnorm_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                         const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap, int n_hc,
                         float* __restrict__ gs_out, Workspace* __restrict__ ws) {
   ptx::pdl_launch_dependents();
-  extern __shared__ __align__(16) uint16_t mixbuf[];
-  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  __shared__ RowScratch sc;
   const int nb = static_cast<int>(cols / 16);
   uint32_t m2 = 0;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
-  for (int64_t r = gw; r < rows; r += nw) {
-    const uint16_t* xr = x + r * ld;
-    if constexpr (kMix) {
-      warp_mhc_mix(xr, cols, n_hc, amap + r * n_hc, mixbuf + warp * cols);
-      xr = mixbuf + warp * cols;
-    }
-    const float inv = warp_inv_rms(xr, cols, eps);
-    for (int b = lane; b < nb; b += 32) {
-      const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
-      const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
-      m2 = __vmaxu2(m2, absmax8(rms_vec(xv[0], __ldg(wv), inv)));
-      m2 = __vmaxu2(m2, absmax8(rms_vec(xv[1], __ldg(wv + 1), inv)));
-    }
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    uint4 y[J][2];
+    block_row_norm<NT, J, kMix>(x + r * ld, cols, wt, eps, amap + r * n_hc, n_hc, sc, y);
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      if (static_cast<int>(threadIdx.x) + j * NT < nb)
+        m2 = __vmaxu2(m2, __vmaxu2(absmax8(y[j][0]), absmax8(y[j][1])));
   }
   uint32_t m = fold16(m2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  __shared__ uint32_t warp_max[kRmsThreads / 32];
-  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();  // the last row's scratch has been read
+  if ((threadIdx.x & 31) == 0) sc.mx[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kRmsThreads / 32; ++w) m = max(m, warp_max[w]);
+    for (int w = 1; w < NT / 32; ++w) m = max(m, sc.mx[w]);
     atomicMax(&ws->amax_bits, m << 16);
     __threadfence();
     const uint32_t ticket = atomicAdd(&ws->done, 1u);
@@ -960,52 +1172,49 @@ __global__ void __launch_bounds__(kRmsThreads)
   }
 }
 
-// Pass 2: recompute each row's inv_rms (same order, same value) and quantize y.
-template <bool kMix>
-__global__ void __launch_bounds__(kRmsThreads)
+// Pass 2: recompute each row (same values) and quantize y.
+template <int NT, int J, bool kMix>
+__global__ void __launch_bounds__(NT, 512 / NT)
     rmsnorm_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                             const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap,
                             int n_hc, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                             const float* __restrict__ gs_ptr) {
   ptx::pdl_launch_dependents();
-  extern __shared__ __align__(16) uint16_t mixbuf[];
-  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-  const int nb = static_cast<int>(cols / 16);
+  __shared__ RowScratch sc;
   __shared__ float2 tab[128];
+  const int nb = static_cast<int>(cols / 16);
   const float gs = __ldg(gs_ptr);
   fill_codec(tab, gs);
   __syncthreads();
-  const Codec sc = make_codec(gs, tab);
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kRmsThreads / 32) + warp;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * (kRmsThreads / 32);
-  for (int64_t r = gw; r < rows; r += nw) {
-    const uint16_t* xr = x + r * ld;
-    if constexpr (kMix) {
-      warp_mhc_mix(xr, cols, n_hc, amap + r * n_hc, mixbuf + warp * cols);
-      xr = mixbuf + warp * cols;
-    }
-    const float inv = warp_inv_rms(xr, cols, eps);
-    for (int b = lane; b < nb; b += 32) {
-      const uint4* xv = reinterpret_cast<const uint4*>(xr + b * 16);
-      const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
-      uint32_t sbyte;
-      uint2 codes;
-      quantize_block(rms_vec(xv[0], __ldg(wv), inv), rms_vec(xv[1], __ldg(wv + 1), inv), sc, sbyte, codes);
-      const int64_t blk = r * nb + b;
-      __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
-      sf[blk] = static_cast<uint8_t>(sbyte);
+  const Codec cd = make_codec(gs, tab);
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    uint4 y[J][2];
+    block_row_norm<NT, J, kMix>(x + r * ld, cols, wt, eps, amap + r * n_hc, n_hc, sc, y);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int b = static_cast<int>(threadIdx.x) + j * NT;
+      if (b < nb) {
+        uint32_t sbyte;
+        uint2 codes;
+        quantize_block(y[j][0], y[j][1], cd, sbyte, codes);
+        const int64_t blk = r * nb + b;
+        __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
+        sf[blk] = static_cast<uint8_t>(sbyte);
+      }
     }
   }
 }
 
 // One pass for inputs that fit in the SMs' shared memory: each CTA holds
-// whole rows; every warp normalises its rows in place (y replaces x), the
-// CTAs exchange maxima as in quantize_onepass_kernel (one cluster, or a
-// cooperative grid meeting at the workspace counter), then each CTA
-// quantizes its rows from shared memory.
+// whole rows and normalises them in place (y replaces x) -- a few rows one
+// after the other with all its threads on each (the scheme of the two-pass
+// kernels, from shared memory), more rows one warp each -- the CTAs exchange
+// maxima as in
+// quantize_onepass_kernel (one cluster, or a cooperative grid meeting at the
+// workspace counter), then each CTA quantizes its rows from shared memory.
 // kMix: each token's n_hc streams are copied on chip and mixed (mHC
 // pre-mix) into the first stream's buffer before the norm.
-template <bool kCluster, bool kMix>
+template <bool kCluster, bool kMix, int J>
 __global__ void __launch_bounds__(kOnePassThreads, 1)
     rmsnorm_quantize_onepass_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                                     const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap,
@@ -1043,18 +1252,37 @@ __global__ void __launch_bounds__(kOnePassThreads, 1)
   const bool late_load = __syncthreads_or(!ptx::mbar_wait_bounded(bar_a, 0, &never, 2000000000LL)) != 0;
   if (late_load && threadIdx.x == 0) atomicOr(&ws->status, NVFP4_DEVICE_TIMEOUT);
   const int64_t n_rows_live = late_load ? 0 : n_rows;
+  __shared__ RowScratch rsc;
   uint32_t m2 = 0;
-  for (int64_t rr = warp; rr < n_rows_live; rr += kWarpsOp) {
+  if (n_rows_live > kBlockRowsMax) {
+    // many rows: one warp per row, the rows side by side
+    for (int64_t rr = warp; rr < n_rows_live; rr += kWarpsOp) {
+      uint16_t* yr = data + rr * row_elems;
+      if constexpr (kMix) warp_mhc_mix(yr, cols, n_hc, amap + (r0 + rr) * n_hc, yr);
+      const float inv = warp_inv_rms(yr, cols, eps);
+      for (int b = lane; b < nb; b += 32) {
+        uint4* v = reinterpret_cast<uint4*>(yr + b * 16);
+        const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
+        const uint4 y0 = rms_vec(v[0], __ldg(wv), inv), y1 = rms_vec(v[1], __ldg(wv + 1), inv);
+        v[0] = y0;  // y replaces x: only this lane touches this block
+        v[1] = y1;
+        m2 = __vmaxu2(m2, __vmaxu2(absmax8(y0), absmax8(y1)));
+      }
+    }
+  }
+  // few rows: all the CTA's threads on each row in turn
+  for (int64_t rr = 0; n_rows_live <= kBlockRowsMax && rr < n_rows_live; ++rr) {
     uint16_t* yr = data + rr * row_elems;
-    if constexpr (kMix) warp_mhc_mix(yr, cols, n_hc, amap + (r0 + rr) * n_hc, yr);
-    const float inv = warp_inv_rms(yr, cols, eps);
-    for (int b = lane; b < nb; b += 32) {
-      uint4* v = reinterpret_cast<uint4*>(yr + b * 16);
-      const uint4* wv = reinterpret_cast<const uint4*>(wt + b * 16);
-      const uint4 y0 = rms_vec(v[0], __ldg(wv), inv), y1 = rms_vec(v[1], __ldg(wv + 1), inv);
-      v[0] = y0;  // y replaces x: only this lane touches this block
-      v[1] = y1;
-      m2 = __vmaxu2(m2, __vmaxu2(absmax8(y0), absmax8(y1)));
+    uint4 y[J][2];
+    block_row_norm<kOnePassThreads, J, kMix, true>(yr, cols, wt, eps, amap + (r0 + rr) * n_hc, n_hc, rsc, y);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int b = static_cast<int>(threadIdx.x) + j * kOnePassThreads;
+      if (b < nb) {  // y replaces x: only this thread touches block b (of every stream)
+        reinterpret_cast<uint4*>(yr + b * 16)[0] = y[j][0];
+        reinterpret_cast<uint4*>(yr + b * 16)[1] = y[j][1];
+        m2 = __vmaxu2(m2, __vmaxu2(absmax8(y[j][0]), absmax8(y[j][1])));
+      }
     }
   }
   uint32_t m = fold16(m2);
@@ -1155,7 +1383,12 @@ cudaError_t launch_rmsnorm_quantize_t(const uint16_t* x, int64_t rows, int64_t c
       grid = (rows + per - 1) / per;
       if (grid <= cap) {
         const size_t smem = static_cast<size_t>(per * row_bytes);
-        auto kernel = cluster ? rmsnorm_quantize_onepass_kernel<true, kMix> : rmsnorm_quantize_onepass_kernel<false, kMix>;
+        // one 16-element block per thread per row (cols <= 8192; the mix always), else two
+        auto kernel = cluster ? rmsnorm_quantize_onepass_kernel<true, kMix, 1> : rmsnorm_quantize_onepass_kernel<false, kMix, 1>;
+        if constexpr (!kMix) {
+          if (cols / 16 > kOnePassThreads)
+            kernel = cluster ? rmsnorm_quantize_onepass_kernel<true, false, 2> : rmsnorm_quantize_onepass_kernel<false, false, 2>;
+        }
         bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)) == cudaSuccess;
         if (ok && cluster)
@@ -1191,29 +1424,28 @@ cudaError_t launch_rmsnorm_quantize_t(const uint16_t* x, int64_t rows, int64_t c
       }
     }
   }
-  // two row-parallel passes; with the mix, each warp's row goes through its
-  // own shared-memory buffer
-  const size_t mix_smem = kMix ? static_cast<size_t>(kRmsThreads / 32) * cols * 2 : 0;
-  cudaError_t e = cudaSuccess;
-  if (mix_smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(rmsnorm_amax_kernel<kMix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(mix_smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(rmsnorm_quantize_kernel<kMix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(mix_smem));
-    if (e != cudaSuccess) return e;
+  // two passes, one CTA per row at a time, the row's blocks in registers
+  int64_t grid = rows > 0 ? rows : 1;
+  if (grid > 8ll * sms) grid = 8ll * sms;
+  // one 16-element block per thread (256 or 512 threads: cols <= 8192), else two of 512 threads'
+  const int nbk = static_cast<int>(cols / 16);
+  const int variant = nbk <= 256 ? 0 : (nbk <= 512 ? 1 : 2);
+  // (the mix takes cols <= 8192: variants 0 and 1)
+  auto amax_k = variant == 0 ? rmsnorm_amax_kernel<256, 1, kMix> : rmsnorm_amax_kernel<512, 1, kMix>;
+  auto quant_k = variant == 0 ? rmsnorm_quantize_kernel<256, 1, kMix> : rmsnorm_quantize_kernel<512, 1, kMix>;
+  if constexpr (!kMix) {
+    if (variant == 2) {
+      amax_k = rmsnorm_amax_kernel<512, 2, false>;
+      quant_k = rmsnorm_quantize_kernel<512, 2, false>;
+    }
   }
-  const int64_t warps_needed = rows > 0 ? rows : 1;
-  int64_t grid = (warps_needed + kRmsThreads / 32 - 1) / (kRmsThreads / 32);
-  if (grid > 4ll * sms) grid = 4ll * sms;
+  const unsigned nt = variant == 0 ? 256u : 512u;
   count_launch();
-  rmsnorm_amax_kernel<kMix><<<static_cast<unsigned>(grid), kRmsThreads, mix_smem, stream>>>(
-      x, rows, cols, ld, wt, eps, amap, n_hc, gs, ws);
-  e = cudaGetLastError();
+  amax_k<<<static_cast<unsigned>(grid), nt, 0, stream>>>(x, rows, cols, ld, wt, eps, amap, n_hc, gs, ws);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || rows == 0) return e;
   count_launch();
-  rmsnorm_quantize_kernel<kMix><<<static_cast<unsigned>(grid), kRmsThreads, mix_smem, stream>>>(
-      x, rows, cols, ld, wt, eps, amap, n_hc, q, sf, gs);
+  quant_k<<<static_cast<unsigned>(grid), nt, 0, stream>>>(x, rows, cols, ld, wt, eps, amap, n_hc, q, sf, gs);
   return cudaGetLastError();
 }
 

@@ -65,8 +65,9 @@ def check(got, ref, what):
     assert np.array_equal(q, rq), f"{what}: {int((q != rq).sum())} code bytes differ"
 
 
+# (600, 4, 7168) and (1200, 4, 4096) exceed the SMs' shared memory: the two passes
 @pytest.mark.parametrize("T,n,d", [(1, 4, 7168), (8, 4, 7168), (32, 4, 7168), (3, 1, 512), (5, 2, 2048),
-                                   (300, 3, 4096), (600, 4, 7168)])
+                                   (300, 3, 4096), (600, 4, 7168), (1200, 4, 4096)])
 def test_mhc_rmsnorm_quantize_shapes(nv, ws, T, n, d):
     x, a, w = case(T, n, d, seed=T + 10 * n + d)
     check(run(nv, ws, x, a, w), oracle.mhc_rmsnorm_quantize(x, a, w, EPS), f"{T}x{n}x{d}")
