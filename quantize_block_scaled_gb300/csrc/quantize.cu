@@ -1134,24 +1134,84 @@ __device__ __forceinline__ void block_row_norm(const uint16_t* __restrict__ xr, 
   }
 }
 
+// This CTA's rows r = blockIdx.x + k gridDim.x, each normalised (y into f).
+// With row_bytes != 0 the rows come through two shared-memory buffers: the
+// next row's bulk copy is in flight while a row is processed.  Returns false
+// if a copy did not land in time (NVFP4_DEVICE_TIMEOUT is recorded).
+template <int NT, int J, bool kMix, typename F>
+__device__ __forceinline__ bool for_rows(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                                         const uint16_t* __restrict__ wt, float eps,
+                                         const uint16_t* __restrict__ amap, int n_hc, uint32_t row_bytes,
+                                         uint8_t* buf, uint64_t* bars, RowScratch& sc, uint32_t* status, F f) {
+  if (row_bytes == 0) {
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+      uint4 y[J][2];
+      block_row_norm<NT, J, kMix>(x + r * ld, cols, wt, eps, amap + r * n_hc, n_hc, sc, y);
+      f(r, y);
+    }
+    return true;
+  }
+  const uint32_t bar[2] = {ptx::smem_addr(&bars[0]), ptx::smem_addr(&bars[1])};
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar[0], 1);
+    ptx::mbar_init(bar[1], 1);
+    ptx::fence_mbar_init();
+    if (static_cast<int64_t>(blockIdx.x) < rows) {
+      ptx::mbar_arrive_expect_tx(bar[0], row_bytes);
+      ptx::bulk_load(ptx::smem_addr(buf), x + static_cast<int64_t>(blockIdx.x) * ld, row_bytes, bar[0]);
+    }
+  }
+  __syncthreads();
+  uint32_t never = 0;
+  int it = 0;
+  int64_t issued = blockIdx.x;  // the last row whose copy was issued
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, ++it) {
+    const int cur = it & 1;
+    const int64_t rn = r + gridDim.x;
+    if (threadIdx.x == 0 && rn < rows) {
+      // the other buffer was read in the previous row, before its barriers
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive_expect_tx(bar[cur ^ 1], row_bytes);
+      ptx::bulk_load(ptx::smem_addr(buf + (cur ^ 1) * row_bytes), x + rn * ld, row_bytes, bar[cur ^ 1]);
+    }
+    if (rn < rows) issued = rn;
+    const bool late = __syncthreads_or(!ptx::mbar_wait_bounded(bar[cur], (it >> 1) & 1, &never, 2000000000LL)) != 0;
+    if (late) {
+      if (threadIdx.x == 0) {
+        atomicOr(status, NVFP4_DEVICE_TIMEOUT);
+        // let the copies in flight land before the CTA can exit
+        ptx::mbar_wait_bounded(bar[cur], (it >> 1) & 1, &never, 2000000000LL);
+        if (issued == rn) ptx::mbar_wait_bounded(bar[cur ^ 1], ((it + 1) >> 1) & 1, &never, 2000000000LL);
+      }
+      return false;
+    }
+    uint4 y[J][2];
+    block_row_norm<NT, J, kMix, true>(reinterpret_cast<const uint16_t*>(buf + cur * row_bytes), cols, wt, eps,
+                                      amap + r * n_hc, n_hc, sc, y);
+    f(r, y);
+  }
+  return true;
+}
+
 // Pass 1: y's maximum |.|, then gs by the last block, exactly as the amax kernel does.
 template <int NT, int J, bool kMix>
 __global__ void __launch_bounds__(NT, 512 / NT)
     rmsnorm_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                         const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap, int n_hc,
-                        float* __restrict__ gs_out, Workspace* __restrict__ ws) {
+                        uint32_t row_bytes, float* __restrict__ gs_out, Workspace* __restrict__ ws) {
   ptx::pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t rowbuf[];
   __shared__ RowScratch sc;
+  __shared__ __align__(8) uint64_t bars[2];
   const int nb = static_cast<int>(cols / 16);
   uint32_t m2 = 0;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    uint4 y[J][2];
-    block_row_norm<NT, J, kMix>(x + r * ld, cols, wt, eps, amap + r * n_hc, n_hc, sc, y);
+  for_rows<NT, J, kMix>(x, rows, cols, ld, wt, eps, amap, n_hc, row_bytes, rowbuf, bars, sc, &ws->status,
+                        [&](int64_t, const uint4 (&y)[J][2]) {
 #pragma unroll
-    for (int j = 0; j < J; ++j)
-      if (static_cast<int>(threadIdx.x) + j * NT < nb)
-        m2 = __vmaxu2(m2, __vmaxu2(absmax8(y[j][0]), absmax8(y[j][1])));
-  }
+                          for (int j = 0; j < J; ++j)
+                            if (static_cast<int>(threadIdx.x) + j * NT < nb)
+                              m2 = __vmaxu2(m2, __vmaxu2(absmax8(y[j][0]), absmax8(y[j][1])));
+                        });
   uint32_t m = fold16(m2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -1177,32 +1237,33 @@ template <int NT, int J, bool kMix>
 __global__ void __launch_bounds__(NT, 512 / NT)
     rmsnorm_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                             const uint16_t* __restrict__ wt, float eps, const uint16_t* __restrict__ amap,
-                            int n_hc, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                            const float* __restrict__ gs_ptr) {
+                            int n_hc, uint32_t row_bytes, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                            const float* __restrict__ gs_ptr, uint32_t* __restrict__ status) {
   ptx::pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t rowbuf[];
   __shared__ RowScratch sc;
+  __shared__ __align__(8) uint64_t bars[2];
   __shared__ float2 tab[128];
   const int nb = static_cast<int>(cols / 16);
   const float gs = __ldg(gs_ptr);
   fill_codec(tab, gs);
   __syncthreads();
   const Codec cd = make_codec(gs, tab);
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    uint4 y[J][2];
-    block_row_norm<NT, J, kMix>(x + r * ld, cols, wt, eps, amap + r * n_hc, n_hc, sc, y);
+  for_rows<NT, J, kMix>(x, rows, cols, ld, wt, eps, amap, n_hc, row_bytes, rowbuf, bars, sc, status,
+                        [&](int64_t r, const uint4 (&y)[J][2]) {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int b = static_cast<int>(threadIdx.x) + j * NT;
-      if (b < nb) {
-        uint32_t sbyte;
-        uint2 codes;
-        quantize_block(y[j][0], y[j][1], cd, sbyte, codes);
-        const int64_t blk = r * nb + b;
-        __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
-        sf[blk] = static_cast<uint8_t>(sbyte);
-      }
-    }
-  }
+                          for (int j = 0; j < J; ++j) {
+                            const int b = static_cast<int>(threadIdx.x) + j * NT;
+                            if (b < nb) {
+                              uint32_t sbyte;
+                              uint2 codes;
+                              quantize_block(y[j][0], y[j][1], cd, sbyte, codes);
+                              const int64_t blk = r * nb + b;
+                              __stcs(reinterpret_cast<uint2*>(q) + blk, codes);
+                              sf[blk] = static_cast<uint8_t>(sbyte);
+                            }
+                          }
+                        });
 }
 
 // One pass for inputs that fit in the SMs' shared memory: each CTA holds
@@ -1424,10 +1485,10 @@ cudaError_t launch_rmsnorm_quantize_t(const uint16_t* x, int64_t rows, int64_t c
       }
     }
   }
-  // two passes, one CTA per row at a time, the row's blocks in registers
-  int64_t grid = rows > 0 ? rows : 1;
-  if (grid > 8ll * sms) grid = 8ll * sms;
-  // one 16-element block per thread (256 or 512 threads: cols <= 8192), else two of 512 threads'
+  // two passes, one CTA per row at a time, the row's blocks in registers;
+  // one 16-element block per thread (256 or 512 threads: cols <= 8192), else
+  // two of 512 threads'.  Rows come through two shared-memory buffers
+  // (the next row's bulk copy in flight) when two fit.
   const int nbk = static_cast<int>(cols / 16);
   const int variant = nbk <= 256 ? 0 : (nbk <= 512 ? 1 : 2);
   // (the mix takes cols <= 8192: variants 0 and 1)
@@ -1440,12 +1501,33 @@ cudaError_t launch_rmsnorm_quantize_t(const uint16_t* x, int64_t rows, int64_t c
     }
   }
   const unsigned nt = variant == 0 ? 256u : 512u;
+  const uint32_t rb = static_cast<uint32_t>(row_bytes);
+  const bool staged = 2 * row_bytes <= kOnePassMaxBytes;
+  const size_t smem = staged ? 2 * static_cast<size_t>(rb) : 0;
+  cudaError_t e = cudaSuccess;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(amax_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quant_k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  // persistent: as many CTAs as can be resident, each walking its rows
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_k, static_cast<int>(nt), smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  int64_t grid = static_cast<int64_t>(sms) * per_sm;
+  if (grid > rows) grid = rows > 0 ? rows : 1;
   count_launch();
-  amax_k<<<static_cast<unsigned>(grid), nt, 0, stream>>>(x, rows, cols, ld, wt, eps, amap, n_hc, gs, ws);
-  cudaError_t e = cudaGetLastError();
+  amax_k<<<static_cast<unsigned>(grid), nt, smem, stream>>>(x, rows, cols, ld, wt, eps, amap, n_hc, staged ? rb : 0u,
+                                                            gs, ws);
+  e = cudaGetLastError();
   if (e != cudaSuccess || rows == 0) return e;
   count_launch();
-  quant_k<<<static_cast<unsigned>(grid), nt, 0, stream>>>(x, rows, cols, ld, wt, eps, amap, n_hc, q, sf, gs);
+  quant_k<<<static_cast<unsigned>(grid), nt, smem, stream>>>(x, rows, cols, ld, wt, eps, amap, n_hc,
+                                                             staged ? rb : 0u, q, sf, gs, &ws->status);
   return cudaGetLastError();
 }
 
