@@ -245,7 +245,7 @@ int nvfp4_gemm_topk(const uint8_t* qa, const uint8_t* sfa, const float* gsa,
  * nvfp4_quantize for callers that must not allocate device memory: an engine
  * that gives all of HBM to its own arena up front, or a thread that may not
  * call cudaMalloc/cudaFree because they can block on or synchronise the
- * device.  The pages have no counterpart; it is the same two kernels as
+ * device.  The pages have no counterpart; it runs the same kernels as
  * nvfp4_quantize with the same arguments and results, minus the workspace.
  *
  * Scratch: a 256-byte static device array inside the library (one per GPU
