@@ -56,7 +56,7 @@ __device__ __forceinline__ uint4 ld_policy(const uint4* p, uint64_t pol) {
   return v;
 }
 // Bytes of a large tensor's tail the amax pass marks to keep in L2 (of 126 MB).
-constexpr int64_t kL2KeepBytes = 96ll << 20;
+constexpr int64_t kL2KeepBytes = 64ll << 20;
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
