@@ -21,14 +21,15 @@
 //
 // Per CTA, 6 warps during the main loop:
 //   warp 0     producer: TMA loads of the A and B code tiles (128-byte rows,
-//              128-byte swizzle) into a ring of stages of K = 512.
+//              128-byte swizzle) and of the scale bytes into a ring of
+//              stages of K = 512.
 //   warp 1     MMA issuer (one thread): eight 128 x BN x 64 kind::mxf4nvf4
 //              block-scaled MMAs per stage into one TMEM accumulator, one
 //              commit per stage.
-//   warps 2-5  load each stage's E4M3 scale words from global memory and
-//              write them into tensor memory with tcgen05.st, each warp the
-//              lanes of its own sub-partition, as soon as the stage's
-//              columns are free.
+//   warps 2-5  write each stage's E4M3 scale words (staged with its tiles by
+//              TMA, or loaded from global memory when the scale rows are not
+//              16-byte aligned) into tensor memory with tcgen05.st, each warp
+//              the lanes of its own sub-partition.
 //
 // Then one of two epilogues.
 //  Direct (no K split, k <= 32): the thread that owns TMEM lane r owns row
