@@ -121,3 +121,22 @@ def test_clock_sampler_reads_samples_until_interrupted(tmp_path, monkeypatch):
     assert len(clk.samples) >= 10
     s = clk.summary(t0 - 1.0, t1 + 1.0)
     assert s["window"] == "timed" and s["sm_mhz"] == 2070.0 and s["reasons"] == []
+
+
+def test_traffic_record_needs_the_same_source(tmp_path, monkeypatch):
+    # a recorded DRAM figure is reported only while the kernel source hashes to the recorded sha
+    import hashlib
+    import json
+    src_dir = tmp_path / "quantize_block_scaled_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = src_dir / "k.cu"
+    src.write_text("// kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    rec = {"records": [{"source": "k.cu", "sha": sha, "workload": "w", "dram_bytes_per_launch": 1234}]}
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("k.cu", "w") == 1234
+    assert bench.load_traffic("k.cu", "other") is None
+    src.write_text("// kernel v2\n")  # the kernel changed since the counters were taken
+    assert bench.load_traffic("k.cu", "w") is None
